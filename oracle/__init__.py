@@ -1,0 +1,311 @@
+"""CPU oracle for the context-parallel attention hot path.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, by ``__graft_entry__.smoke()``
+and by ``bench.py``'s CPU-baseline / reference leg. The CUDA library and its
+Python binding never import this package, and this package never imports
+them; the two share only the seeded input generators in ``workloads``.
+
+The arithmetic lives in ``ctx_oracle.c`` (explicit index loops, fp64 softmax,
+OpenMP over query rows); this module marshals numpy arrays into it and adds
+two things that are plain data movement written from the pages:
+
+* ``all_to_all``: ``all_to_all_single`` chunk semantics as the sglang PR
+  #33667 unit test ("_run_all_ranks" / "fake_a2a") states them: every sender's
+  flat buffer is cut into U equal chunks, chunk j goes to rank j, and the
+  receiver concatenates what it got in source-rank order.
+* ``all_gather``: the K/V AllGather of the vllm-omni PR #7641 composed order
+  (concatenation over the A group in rank order).
+
+``py_*`` functions are pure-Python loop twins for tiny shapes.
+
+Every function is pinned by ``tests/test_oracle_pack.py`` and
+``tests/test_oracle_attention.py`` against the pages' own test construction,
+closed forms, invariants or a library routine for the same quantity.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ctx_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle_ctx.so")
+_lib = None
+_lock = threading.Lock()
+
+BF16, FP16 = 0, 1
+_DTYPES = {"bf16": BF16, "fp16": FP16}
+
+
+def build(force: bool = False) -> str:
+    """Compile ctx_oracle.c with gcc + OpenMP into liboracle_ctx.so."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-std=c11",
+           "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            ll, p = ctypes.c_longlong, ctypes.c_void_p
+            lib.orc_pack_qkv.argtypes = [p, p, p, p, ll, ll, ll, ll, ll]
+            lib.orc_unpack_qkv.argtypes = [p, p, p, p, ll, ll, ll, ll, ll]
+            lib.orc_pack_out.argtypes = [p, p, ll, ll, ll, ll, ll]
+            lib.orc_unpack_out.argtypes = [p, p, ll, ll, ll, ll, ll]
+            lib.orc_attention_rows.argtypes = [p, p, p, p, ctypes.c_int, ctypes.c_double,
+                                               ll, ll, ll, ll, ll, ll, p, p, p]
+            lib.orc_attention_probs.argtypes = [p, p, p, ctypes.c_int, ctypes.c_double,
+                                                ll, ll, ll, ll, ll, ll, ll, ll, p]
+            for f in (lib.orc_pack_qkv, lib.orc_unpack_qkv, lib.orc_pack_out,
+                      lib.orc_unpack_out, lib.orc_attention_rows, lib.orc_attention_probs):
+                f.restype = ctypes.c_int
+            lib.orc_num_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def num_threads() -> int:
+    return _load().orc_num_threads()
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _u16(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError("oracle takes 16-bit float bit patterns as uint16 arrays")
+    return a
+
+
+# ---------------------------------------------------------------- exchanges
+
+def pack_qkv(q, k, v, U: int) -> np.ndarray:
+    """[B,S_l,H,D] x3 -> staging [U,3,B,S_l,H/U,D] (destination-major)."""
+    q, k, v = _u16(q), _u16(k), _u16(v)
+    B, S_l, H, D = q.shape
+    if k.shape != q.shape or v.shape != q.shape or H % U:
+        raise ValueError("pack_qkv: shape mismatch or H % U != 0")
+    out = np.empty((U, 3, B, S_l, H // U, D), dtype=np.uint16)
+    rc = _load().orc_pack_qkv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, S_l, H, D, U)
+    assert rc == 0
+    return out
+
+
+def unpack_qkv(recv, U: int):
+    """recv [U,3,B,S_l,h_l,D] -> (Q', K', V') each [B, U*S_l, h_l, D]."""
+    recv = _u16(recv)
+    U2, three, B, S_l, h_l, D = recv.shape
+    assert U2 == U and three == 3
+    outs = [np.empty((B, U * S_l, h_l, D), dtype=np.uint16) for _ in range(3)]
+    rc = _load().orc_unpack_qkv(_ptr(recv), *(_ptr(o) for o in outs), B, S_l, h_l, D, U)
+    assert rc == 0
+    return tuple(outs)
+
+
+def pack_out(o, U: int) -> np.ndarray:
+    """O [B, U*S_l, h_l, D] -> send [U, B, S_l, h_l, D]."""
+    o = _u16(o)
+    B, rows, h_l, D = o.shape
+    assert rows % U == 0
+    S_l = rows // U
+    out = np.empty((U, B, S_l, h_l, D), dtype=np.uint16)
+    assert _load().orc_pack_out(_ptr(o), _ptr(out), B, S_l, h_l, D, U) == 0
+    return out
+
+
+def unpack_out(recv, U: int) -> np.ndarray:
+    """recv [U, B, S_l, h_l, D] -> Y [B, S_l, U*h_l, D]."""
+    recv = _u16(recv)
+    U2, B, S_l, h_l, D = recv.shape
+    assert U2 == U
+    out = np.empty((B, S_l, U * h_l, D), dtype=np.uint16)
+    assert _load().orc_unpack_out(_ptr(recv), _ptr(out), B, S_l, h_l, D, U) == 0
+    return out
+
+
+def all_to_all(sends):
+    """all_to_all_single over one group: sends[r] is rank r's flat send
+    buffer; returns recvs[j] = concat over r of chunk j of sends[r]."""
+    U = len(sends)
+    chunks = [np.split(np.ascontiguousarray(s).reshape(-1), U) for s in sends]
+    return [np.concatenate([chunks[r][j] for r in range(U)]).reshape(sends[j].shape)
+            for j in range(U)]
+
+
+def all_gather(shards, axis: int = 1):
+    """AllGather over one group: concatenation in rank order along ``axis``."""
+    return np.concatenate([np.ascontiguousarray(s) for s in shards], axis=axis)
+
+
+# ---------------------------------------------------------------- attention
+
+def default_scale(D: int) -> float:
+    return 1.0 / math.sqrt(D)
+
+
+def attention_rows(q, k, v, rows, mask=None, scale=None, dtype="bf16"):
+    """fp64 attention for selected query rows.
+
+    q [B,Sq,H,D], k/v [B,Sk,H,D] (uint16 bit patterns), mask None or
+    [B,Sk] uint8 (nonzero = attend), rows an int64 array [n,3] of (b,h,i).
+    Returns (O [n,D] float64, LSE [n] float64, natural log).
+    """
+    q, k, v = _u16(q), _u16(k), _u16(v)
+    B, Sq, H, D = q.shape
+    Bk, Sk, Hk, Dk = k.shape
+    assert (Bk, Hk, Dk) == (B, H, D) and v.shape == k.shape
+    if scale is None:
+        scale = default_scale(D)
+    rows = np.ascontiguousarray(rows, dtype=np.int64).reshape(-1, 3)
+    n = rows.shape[0]
+    m = None
+    if mask is not None:
+        m = np.ascontiguousarray(mask, dtype=np.uint8)
+        assert m.shape == (B, Sk)
+    out = np.empty((n, D), dtype=np.float64)
+    lse = np.empty((n,), dtype=np.float64)
+    rc = _load().orc_attention_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(m) if m is not None else None,
+                                    _DTYPES[dtype], float(scale), B, Sq, Sk, H, D, n,
+                                    _ptr(rows), _ptr(out), _ptr(lse))
+    assert rc == 0, rc
+    return out, lse
+
+
+def all_rows(B: int, H: int, Sq: int) -> np.ndarray:
+    """(b, h, i) triples for every query row, b-major then h then i."""
+    b, h, i = np.meshgrid(np.arange(B), np.arange(H), np.arange(Sq), indexing="ij")
+    return np.stack([b.ravel(), h.ravel(), i.ravel()], axis=1).astype(np.int64)
+
+
+def attention(q, k, v, mask=None, scale=None, dtype="bf16"):
+    """Full attention: O [B,Sq,H,D] float64, LSE [B,H,Sq] float64."""
+    B, Sq, H, D = q.shape
+    rows = all_rows(B, H, Sq)
+    o, lse = attention_rows(q, k, v, rows, mask, scale, dtype)
+    O = o.reshape(B, H, Sq, D).transpose(0, 2, 1, 3).copy()
+    return O, lse.reshape(B, H, Sq)
+
+
+def attention_probs(q, k, b, h, i, mask=None, scale=None, dtype="bf16") -> np.ndarray:
+    """Softmax probabilities of query row (b, h, i) over all keys (fp64)."""
+    q, k = _u16(q), _u16(k)
+    B, Sq, H, D = q.shape
+    Sk = k.shape[1]
+    if scale is None:
+        scale = default_scale(D)
+    m = None if mask is None else np.ascontiguousarray(mask, dtype=np.uint8)
+    p = np.empty((Sk,), dtype=np.float64)
+    _load().orc_attention_probs(_ptr(q), _ptr(k), _ptr(m) if m is not None else None,
+                                _DTYPES[dtype], float(scale), B, Sq, Sk, H, D, b, h, i, _ptr(p))
+    return p
+
+
+# ------------------------------------------------------ composed pipeline
+
+def ulysses_agkv_forward(q_shards, k_shards, v_shards, U: int, A: int,
+                         jk=None, jv=None):
+    """The composed U x A input side, all ranks (vllm-omni PR #7641 order):
+    Ulysses all-to-all inside each U group (ranks a*U .. a*U+U-1), then the
+    K/V AllGather inside each A group (ranks u, U+u, ...), then the joint
+    (text) K/V appended after the gathered image keys.
+
+    Inputs are per-rank [B,S_l,H,D] uint16 shards indexed by g = a*U + u.
+    Returns dict with, per rank g: 'q' [B,S/A,h_l,D] local-Q, and per head
+    group u: 'k', 'v' [B,S(+joint),h_l,D] global K/V.
+    """
+    R = U * A
+    assert len(q_shards) == R
+    staging = [pack_qkv(q_shards[g], k_shards[g], v_shards[g], U) for g in range(R)]
+    loc = [None] * R
+    for a in range(A):
+        grp = [a * U + u for u in range(U)]
+        recvs = all_to_all([staging[g] for g in grp])
+        for u, g in enumerate(grp):
+            loc[g] = unpack_qkv(recvs[u], U)
+    res = {"q": [loc[g][0] for g in range(R)], "k": [], "v": []}
+    for u in range(U):
+        grp = [a * U + u for a in range(A)]
+        kg = all_gather([loc[g][1] for g in grp])
+        vg = all_gather([loc[g][2] for g in grp])
+        if jk is not None:
+            h_l = kg.shape[2]
+            kg = np.concatenate([kg, np.ascontiguousarray(jk[:, :, u * h_l:(u + 1) * h_l])], axis=1)
+            vg = np.concatenate([vg, np.ascontiguousarray(jv[:, :, u * h_l:(u + 1) * h_l])], axis=1)
+        res["k"].append(kg)
+        res["v"].append(vg)
+    return res
+
+
+def ulysses_reverse(o_ranks, U: int, A: int):
+    """Reverse Ulysses exchange for all ranks: o_ranks[g] is rank g's output
+    [B, S/A, h_l, D]; returns per-rank [B, S_l, H, D] sequence-sharded outputs."""
+    R = U * A
+    sends = [pack_out(o_ranks[g], U) for g in range(R)]
+    out = [None] * R
+    for a in range(A):
+        grp = [a * U + u for u in range(U)]
+        recvs = all_to_all([sends[g] for g in grp])
+        for u, g in enumerate(grp):
+            out[g] = unpack_out(recvs[u], U)
+    return out
+
+
+# ------------------------------------------------------- pure-Python twins
+
+def _widen_py(x: int, dtype: str) -> float:
+    if dtype == "bf16":
+        return float(np.array([x << 16], dtype=np.uint32).view(np.float32)[0])
+    return float(np.array([x], dtype=np.uint16).view(np.float16)[0])
+
+
+def py_pack_qkv(q, k, v, U: int) -> np.ndarray:
+    """Pure-Python loop twin of pack_qkv (tiny shapes only)."""
+    B, S_l, H, D = q.shape
+    h_l = H // U
+    out = np.zeros((U, 3, B, S_l, h_l, D), dtype=np.uint16)
+    src = (q, k, v)
+    for r in range(U):
+        for t in range(3):
+            for b in range(B):
+                for s in range(S_l):
+                    for h in range(h_l):
+                        for d in range(D):
+                            out[r, t, b, s, h, d] = src[t][b, s, r * h_l + h, d]
+    return out
+
+
+def py_attention_row(q, k, v, b, h, i, mask=None, scale=None, dtype="bf16"):
+    """Pure-Python twin of one attention row (tiny shapes only)."""
+    D = q.shape[3]
+    Sk = k.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    qs = [_widen_py(int(q[b, i, h, d]), dtype) for d in range(D)]
+    s = []
+    for j in range(Sk):
+        if mask is not None and not mask[b, j]:
+            continue
+        s.append((j, scale * sum(qs[d] * _widen_py(int(k[b, j, h, d]), dtype) for d in range(D))))
+    if not s:
+        return [0.0] * D, -math.inf
+    m = max(x for _, x in s)
+    w = [(j, math.exp(x - m)) for j, x in s]
+    l = sum(x for _, x in w)
+    o = [sum(x * _widen_py(int(v[b, j, h, d]), dtype) for j, x in w) / l for d in range(D)]
+    return o, m + math.log(l)
