@@ -1,0 +1,170 @@
+"""Python binding of libctx (include/ctx.h): argument marshalling only.
+
+Every function here has the name of the C entry point it calls and does no
+computation of its own: it reads shapes, dtypes, device pointers and the
+current CUDA stream from torch tensors, calls the C ABI through ctypes and
+raises ``CtxError`` on any status other than CTX_OK. There is no fallback: if
+libctx.so has not been built, importing works but the first call raises.
+
+torch is used only for device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from .build import LIB_PATH, build  # noqa: F401  (re-exported for callers)
+
+CTX_OK = 0
+STATUS_NAMES = {0: "CTX_OK", 1: "CTX_ERR_INVALID_ARG", 2: "CTX_ERR_UNSUPPORTED", 3: "CTX_ERR_MISALIGNED",
+                4: "CTX_ERR_ALIASING", 5: "CTX_ERR_CUDA", 6: "CTX_ERR_TIMEOUT"}
+CTX_BF16, CTX_FP16 = 0, 1
+
+# Every symbol include/ctx.h declares, with (restype, argtypes).
+_P, _I, _LL, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_float
+SIGNATURES = {
+    "ctx_pack_qkv": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "ctx_sim_all_to_all": (_I, [_P, _P, _I, _I, _LL, _P]),
+    "ctx_unpack_qkv": (_I, [_P, _P, _P, _P, _LL, _LL, _I, _I, _I, _I, _I, _I, _P]),
+    "ctx_attn_lq_gkv": (_I, [_P, _P, _P, _P, _F, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "ctx_pack_out": (_I, [_P, _P, _LL, _I, _I, _I, _I, _I, _I, _P]),
+    "ctx_unpack_out": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "ctx_status_string": (ctypes.c_char_p, [_I]),
+    "ctx_device_status": (_I, [_P]),
+    "ctx_last_cuda_error": (_I, []),
+    "ctx_selftest_wait_timeout": (_I, [_LL, _P]),
+    "ctx_version": (_I, []),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class CtxError(RuntimeError):
+    def __init__(self, fn: str, status: int, cuda_error: int = 0):
+        self.status = status
+        self.cuda_error = cuda_error
+        msg = f"{fn} failed: {STATUS_NAMES.get(status, status)}"
+        if cuda_error:
+            msg += f" (cudaError {cuda_error})"
+        super().__init__(msg)
+
+
+def lib():
+    """The loaded libctx (ctypes.CDLL). Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"libctx.so not found at {LIB_PATH}: build it first "
+                                   "(python -c 'import __graft_entry__ as g; g.build()')")
+            handle = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                f = getattr(handle, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = handle
+    return _lib
+
+
+def _check(fn: str, status: int):
+    if status != CTX_OK:
+        raise CtxError(fn, status, lib().ctx_last_cuda_error() if status == 5 else 0)
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return CTX_BF16
+    if t.dtype == torch.float16:
+        return CTX_FP16
+    raise TypeError(f"libctx moves bf16/fp16 tensors, got {t.dtype}")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def ctx_pack_qkv(q, k, v, staging, U: int, stream=None):
+    """q, k, v [B,S_l,H,D] -> staging [U,3,B,S_l,H/U,D] (all contiguous CUDA tensors)."""
+    B, S_l, H, D = q.shape
+    _check("ctx_pack_qkv", lib().ctx_pack_qkv(_ptr(q), _ptr(k), _ptr(v), _ptr(staging), B, S_l, H, D, U,
+                                              _dtype(q), _stream(stream)))
+    return staging
+
+
+def ctx_sim_all_to_all(send, recv, G: int, U: int, stream=None):
+    """send/recv [G, U, U, chunk] (any dtype): recv[g][j][r] = send[g][r][j]."""
+    chunk_bytes = send.numel() * send.element_size() // (G * U * U)
+    _check("ctx_sim_all_to_all", lib().ctx_sim_all_to_all(_ptr(send), _ptr(recv), G, U, chunk_bytes,
+                                                          _stream(stream)))
+    return recv
+
+
+def ctx_unpack_qkv(recv, q, k, v, U: int, q_batch_stride_rows: int | None = None,
+                   kv_batch_stride_rows: int | None = None, stream=None):
+    """recv [U,3,B,S_l,h_l,D] -> q, k, v: bases of [B, stride_rows, h_l, D] buffers
+    (default strides U*S_l: contiguous [B, U*S_l, h_l, D] outputs)."""
+    U2, three, B, S_l, h_l, D = recv.shape
+    assert U2 == U and three == 3
+    qs = U * S_l if q_batch_stride_rows is None else q_batch_stride_rows
+    ks = U * S_l if kv_batch_stride_rows is None else kv_batch_stride_rows
+    _check("ctx_unpack_qkv", lib().ctx_unpack_qkv(_ptr(recv), _ptr(q), _ptr(k), _ptr(v), qs, ks,
+                                                  B, S_l, h_l, D, U, _dtype(recv), _stream(stream)))
+
+
+def ctx_attn_lq_gkv(q, k, v, out, lse=None, key_mask=None, scale: float | None = None, stream=None):
+    """q [B,Sq,H,D], k/v [B,Sk,H,D] -> out [B,Sq,H,D], lse [B,H,Sq] fp32 (optional)."""
+    B, Sq, H, D = q.shape
+    Sk = k.shape[1]
+    s = float("nan") if scale is None else float(scale)
+    _check("ctx_attn_lq_gkv", lib().ctx_attn_lq_gkv(_ptr(q), _ptr(k), _ptr(v), _ptr(key_mask), s, _ptr(out),
+                                                    _ptr(lse), B, Sq, Sk, H, D, _dtype(q), _stream(stream)))
+    return out
+
+
+def ctx_pack_out(o, send, U: int, o_batch_stride_rows: int | None = None, stream=None):
+    """o: base of a [B, stride_rows, h_l, D] buffer whose first U*S_l rows per
+    batch are this rank's output -> send [U, B, S_l, h_l, D]."""
+    Us, B, S_l, h_l, D = send.shape
+    assert Us == U
+    st = U * S_l if o_batch_stride_rows is None else o_batch_stride_rows
+    _check("ctx_pack_out", lib().ctx_pack_out(_ptr(o), _ptr(send), st, B, S_l, h_l, D, U, _dtype(send),
+                                              _stream(stream)))
+    return send
+
+
+def ctx_unpack_out(recv, y, U: int, stream=None):
+    """recv [U, B, S_l, h_l, D] -> y [B, S_l, U*h_l, D]."""
+    U2, B, S_l, h_l, D = recv.shape
+    _check("ctx_unpack_out", lib().ctx_unpack_out(_ptr(recv), _ptr(y), B, S_l, h_l, D, U, _dtype(recv),
+                                                  _stream(stream)))
+    return y
+
+
+def ctx_device_status(stream=None) -> int:
+    return lib().ctx_device_status(_stream(stream))
+
+
+def ctx_selftest_wait_timeout(limit_ns: int, stream=None) -> int:
+    return lib().ctx_selftest_wait_timeout(int(limit_ns), _stream(stream))
+
+
+def ctx_status_string(status: int) -> str:
+    return lib().ctx_status_string(status).decode()
+
+
+def ctx_version() -> int:
+    return lib().ctx_version()
+
+
+def ctx_last_cuda_error() -> int:
+    return lib().ctx_last_cuda_error()

@@ -1,0 +1,418 @@
+// C ABI of libctx (declared in include/ctx.h): host-side validation, then one
+// launch per call on the caller's stream. Nothing is allocated here; the only
+// device state is one status word per device for bounded-wait timeouts.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/ctx.h"
+#include "internal.h"
+
+namespace ctx {
+
+__device__ int g_status_word;
+
+namespace {
+struct DeviceCache {
+    std::mutex mu;
+    int *status[64] = {nullptr};
+    int sms[64] = {0};
+};
+DeviceCache &cache()
+{
+    static DeviceCache c;
+    return c;
+}
+}  // namespace
+
+int *device_status_word(cudaError_t *err)
+{
+    int dev = 0;
+    *err = cudaGetDevice(&dev);
+    if (*err != cudaSuccess)
+        return nullptr;
+    if (dev < 0 || dev >= 64) {
+        *err = cudaErrorInvalidDevice;
+        return nullptr;
+    }
+    DeviceCache &c = cache();
+    std::lock_guard<std::mutex> g(c.mu);
+    if (!c.status[dev]) {
+        void *p = nullptr;
+        *err = cudaGetSymbolAddress(&p, g_status_word);
+        if (*err != cudaSuccess)
+            return nullptr;
+        c.status[dev] = static_cast<int *>(p);
+    }
+    return c.status[dev];
+}
+
+int sm_count(cudaError_t *err)
+{
+    int dev = 0;
+    *err = cudaGetDevice(&dev);
+    if (*err != cudaSuccess)
+        return 0;
+    if (dev < 0 || dev >= 64) {
+        *err = cudaErrorInvalidDevice;
+        return 0;
+    }
+    DeviceCache &c = cache();
+    std::lock_guard<std::mutex> g(c.mu);
+    if (!c.sms[dev]) {
+        *err = cudaDeviceGetAttribute(&c.sms[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (*err != cudaSuccess)
+            return 0;
+    }
+    return c.sms[dev];
+}
+
+}  // namespace ctx
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+
+using ctx::RelayoutArgs;
+using ctx::RelayoutMode;
+
+struct Extent {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+
+Extent extent(const void *p, long long bytes)
+{
+    uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    return Extent{lo, lo + static_cast<uintptr_t>(bytes)};
+}
+
+bool overlap(Extent a, Extent b)
+{
+    return a.lo < b.hi && b.lo < a.hi;
+}
+
+bool aligned16(const void *p)
+{
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+bool valid_dtype(ctx_dtype d)
+{
+    return d == CTX_BF16 || d == CTX_FP16;
+}
+
+// Product of sizes, false on overflow past 2^62.
+bool mul_ok(long long &acc, long long x)
+{
+    if (x <= 0)
+        return false;
+    if (acc > (1LL << 62) / x)
+        return false;
+    acc *= x;
+    return true;
+}
+
+ctx_status cuda_fail(cudaError_t e)
+{
+    t_last_cuda_error = static_cast<int>(e);
+    return CTX_ERR_CUDA;
+}
+
+// Device (or managed) memory check; runs after every host-only check.
+ctx_status check_device_ptrs(std::initializer_list<const void *> ptrs)
+{
+    for (const void *p : ptrs) {
+        if (!p)
+            continue;
+        cudaPointerAttributes attr;
+        cudaError_t e = cudaPointerGetAttributes(&attr, p);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return cuda_fail(e);
+        }
+        if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+            return CTX_ERR_INVALID_ARG;
+    }
+    return CTX_OK;
+}
+
+ctx_status run_relayout(RelayoutMode mode, const RelayoutArgs &a, void *stream)
+{
+    cudaError_t e = ctx::launch_relayout(mode, a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CTX_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int ctx_version(void)
+{
+    return 100;  // 0.1.0
+}
+
+const char *ctx_status_string(ctx_status s)
+{
+    switch (s) {
+    case CTX_OK: return "CTX_OK";
+    case CTX_ERR_INVALID_ARG: return "CTX_ERR_INVALID_ARG";
+    case CTX_ERR_UNSUPPORTED: return "CTX_ERR_UNSUPPORTED";
+    case CTX_ERR_MISALIGNED: return "CTX_ERR_MISALIGNED";
+    case CTX_ERR_ALIASING: return "CTX_ERR_ALIASING";
+    case CTX_ERR_CUDA: return "CTX_ERR_CUDA";
+    case CTX_ERR_TIMEOUT: return "CTX_ERR_TIMEOUT";
+    }
+    return "CTX_ERR_UNKNOWN";
+}
+
+int ctx_last_cuda_error(void)
+{
+    return t_last_cuda_error;
+}
+
+ctx_status ctx_pack_qkv(const void *q, const void *k, const void *v, void *staging, int B, int S_l, int H, int D,
+                        int U, ctx_dtype dtype, void *stream)
+{
+    if (!q || !k || !v || !staging || !valid_dtype(dtype))
+        return CTX_ERR_INVALID_ARG;
+    long long n = 1;
+    if (!mul_ok(n, B) || !mul_ok(n, S_l) || !mul_ok(n, H) || !mul_ok(n, D) || U <= 0 || H % U != 0)
+        return CTX_ERR_INVALID_ARG;
+    if (D % 8 != 0 || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(staging))
+        return CTX_ERR_MISALIGNED;
+    const long long bytes = n * 2;
+    const Extent st = extent(staging, 3 * bytes);
+    if (overlap(st, extent(q, bytes)) || overlap(st, extent(k, bytes)) || overlap(st, extent(v, bytes)))
+        return CTX_ERR_ALIASING;
+    ctx_status s = check_device_ptrs({q, k, v, staging});
+    if (s != CTX_OK)
+        return s;
+    RelayoutArgs a{};
+    a.src0 = q;
+    a.src1 = k;
+    a.src2 = v;
+    a.dst0 = staging;
+    a.B = B;
+    a.S_l = S_l;
+    a.H = H;
+    a.U = U;
+    a.h_l = H / U;
+    a.run_vec = static_cast<long long>(H / U) * D / 8;
+    a.n_runs = 3LL * U * B * S_l;
+    return run_relayout(RelayoutMode::PackQKV, a, stream);
+}
+
+ctx_status ctx_sim_all_to_all(const void *send, void *recv, int G, int U, long long chunk_bytes, void *stream)
+{
+    if (!send || !recv)
+        return CTX_ERR_INVALID_ARG;
+    long long n = 1;
+    if (!mul_ok(n, G) || !mul_ok(n, U) || !mul_ok(n, U) || !mul_ok(n, chunk_bytes))
+        return CTX_ERR_INVALID_ARG;
+    if (chunk_bytes % 16 != 0 || !aligned16(send) || !aligned16(recv))
+        return CTX_ERR_MISALIGNED;
+    if (overlap(extent(send, n), extent(recv, n)))
+        return CTX_ERR_ALIASING;
+    ctx_status s = check_device_ptrs({send, recv});
+    if (s != CTX_OK)
+        return s;
+    RelayoutArgs a{};
+    a.src0 = send;
+    a.dst0 = recv;
+    a.U = U;
+    a.G = G;
+    a.run_vec = chunk_bytes / 16;
+    a.n_runs = static_cast<long long>(G) * U * U;
+    return run_relayout(RelayoutMode::AllToAll, a, stream);
+}
+
+ctx_status ctx_unpack_qkv(const void *recv, void *q, void *k, void *v, long long q_batch_stride_rows,
+                          long long kv_batch_stride_rows, int B, int S_l, int h_l, int D, int U, ctx_dtype dtype,
+                          void *stream)
+{
+    if (!recv || !q || !k || !v || !valid_dtype(dtype))
+        return CTX_ERR_INVALID_ARG;
+    long long n = 1;
+    if (!mul_ok(n, B) || !mul_ok(n, S_l) || !mul_ok(n, h_l) || !mul_ok(n, D) || !mul_ok(n, U))
+        return CTX_ERR_INVALID_ARG;
+    const long long rows = static_cast<long long>(U) * S_l;
+    if (q_batch_stride_rows < rows || kv_batch_stride_rows < rows)
+        return CTX_ERR_INVALID_ARG;
+    const long long row_bytes = static_cast<long long>(h_l) * D * 2;
+    long long qspan = q_batch_stride_rows, kvspan = kv_batch_stride_rows;
+    if (!mul_ok(qspan, B) || !mul_ok(qspan, row_bytes) || !mul_ok(kvspan, B) || !mul_ok(kvspan, row_bytes))
+        return CTX_ERR_INVALID_ARG;
+    if (D % 8 != 0 || !aligned16(recv) || !aligned16(q) || !aligned16(k) || !aligned16(v))
+        return CTX_ERR_MISALIGNED;
+    const long long q_bytes = ((static_cast<long long>(B) - 1) * q_batch_stride_rows + rows) * row_bytes;
+    const long long kv_bytes = ((static_cast<long long>(B) - 1) * kv_batch_stride_rows + rows) * row_bytes;
+    const Extent r = extent(recv, 3 * n * 2);
+    const Extent eq = extent(q, q_bytes), ek = extent(k, kv_bytes), ev = extent(v, kv_bytes);
+    if (overlap(r, eq) || overlap(r, ek) || overlap(r, ev) || overlap(eq, ek) || overlap(eq, ev) ||
+        overlap(ek, ev))
+        return CTX_ERR_ALIASING;
+    ctx_status s = check_device_ptrs({recv, q, k, v});
+    if (s != CTX_OK)
+        return s;
+    RelayoutArgs a{};
+    a.src0 = recv;
+    a.dst0 = q;
+    a.dst1 = k;
+    a.dst2 = v;
+    a.B = B;
+    a.S_l = S_l;
+    a.h_l = h_l;
+    a.U = U;
+    a.q_batch_stride_rows = q_batch_stride_rows;
+    a.kv_batch_stride_rows = kv_batch_stride_rows;
+    a.run_vec = static_cast<long long>(h_l) * D / 8;
+    a.n_runs = 3LL * U * B * S_l;
+    return run_relayout(RelayoutMode::UnpackQKV, a, stream);
+}
+
+ctx_status ctx_pack_out(const void *o, void *send, long long o_batch_stride_rows, int B, int S_l, int h_l, int D,
+                        int U, ctx_dtype dtype, void *stream)
+{
+    if (!o || !send || !valid_dtype(dtype))
+        return CTX_ERR_INVALID_ARG;
+    long long n = 1;
+    if (!mul_ok(n, B) || !mul_ok(n, S_l) || !mul_ok(n, h_l) || !mul_ok(n, D) || !mul_ok(n, U))
+        return CTX_ERR_INVALID_ARG;
+    const long long rows = static_cast<long long>(U) * S_l;
+    const long long row_bytes = static_cast<long long>(h_l) * D * 2;
+    long long span = o_batch_stride_rows;
+    if (o_batch_stride_rows < rows || !mul_ok(span, B) || !mul_ok(span, row_bytes))
+        return CTX_ERR_INVALID_ARG;
+    if (D % 8 != 0 || !aligned16(o) || !aligned16(send))
+        return CTX_ERR_MISALIGNED;
+    const long long o_bytes = ((static_cast<long long>(B) - 1) * o_batch_stride_rows + rows) * row_bytes;
+    if (overlap(extent(o, o_bytes), extent(send, n * 2)))
+        return CTX_ERR_ALIASING;
+    ctx_status s = check_device_ptrs({o, send});
+    if (s != CTX_OK)
+        return s;
+    RelayoutArgs a{};
+    a.src0 = o;
+    a.dst0 = send;
+    a.B = B;
+    a.S_l = S_l;
+    a.h_l = h_l;
+    a.U = U;
+    a.q_batch_stride_rows = o_batch_stride_rows;
+    a.run_vec = static_cast<long long>(h_l) * D / 8;
+    a.n_runs = static_cast<long long>(U) * B * S_l;
+    return run_relayout(RelayoutMode::PackOut, a, stream);
+}
+
+ctx_status ctx_unpack_out(const void *recv, void *y, int B, int S_l, int h_l, int D, int U, ctx_dtype dtype,
+                          void *stream)
+{
+    if (!recv || !y || !valid_dtype(dtype))
+        return CTX_ERR_INVALID_ARG;
+    long long n = 1;
+    if (!mul_ok(n, B) || !mul_ok(n, S_l) || !mul_ok(n, h_l) || !mul_ok(n, D) || !mul_ok(n, U))
+        return CTX_ERR_INVALID_ARG;
+    if (D % 8 != 0 || !aligned16(recv) || !aligned16(y))
+        return CTX_ERR_MISALIGNED;
+    if (overlap(extent(recv, n * 2), extent(y, n * 2)))
+        return CTX_ERR_ALIASING;
+    ctx_status s = check_device_ptrs({recv, y});
+    if (s != CTX_OK)
+        return s;
+    RelayoutArgs a{};
+    a.src0 = recv;
+    a.dst0 = y;
+    a.B = B;
+    a.S_l = S_l;
+    a.h_l = h_l;
+    a.U = U;
+    a.run_vec = static_cast<long long>(h_l) * D / 8;
+    a.n_runs = static_cast<long long>(U) * B * S_l;
+    return run_relayout(RelayoutMode::UnpackOut, a, stream);
+}
+
+ctx_status ctx_attn_lq_gkv(const void *q, const void *k, const void *v, const unsigned char *key_mask, float scale,
+                           void *out, float *lse, int B, int Sq, int Sk, int H, int D, ctx_dtype dtype, void *stream)
+{
+    if (!q || !k || !v || !out || !valid_dtype(dtype))
+        return CTX_ERR_INVALID_ARG;
+    long long nq = 1, nk = 1;
+    if (!mul_ok(nq, B) || !mul_ok(nq, Sq) || !mul_ok(nq, H) || !mul_ok(nq, D))
+        return CTX_ERR_INVALID_ARG;
+    if (!mul_ok(nk, B) || !mul_ok(nk, Sk) || !mul_ok(nk, H) || !mul_ok(nk, D))
+        return CTX_ERR_INVALID_ARG;
+    if (std::isnan(scale))
+        scale = 1.0f / std::sqrt(static_cast<float>(D));
+    if (!std::isfinite(scale) || !(scale > 0.f))
+        return CTX_ERR_INVALID_ARG;
+    if (D % 8 != 0 || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+        return CTX_ERR_MISALIGNED;
+    if (D != 64 && D != 128)
+        return CTX_ERR_UNSUPPORTED;
+    const Extent eo = extent(out, nq * 2);
+    const Extent eq = extent(q, nq * 2), ek = extent(k, nk * 2), ev = extent(v, nk * 2);
+    if (overlap(eo, eq) || overlap(eo, ek) || overlap(eo, ev))
+        return CTX_ERR_ALIASING;
+    if (key_mask && overlap(eo, extent(key_mask, static_cast<long long>(B) * Sk)))
+        return CTX_ERR_ALIASING;
+    if (lse) {
+        const Extent el = extent(lse, static_cast<long long>(B) * H * Sq * 4);
+        if (overlap(el, eo) || overlap(el, eq) || overlap(el, ek) || overlap(el, ev) ||
+            (key_mask && overlap(el, extent(key_mask, static_cast<long long>(B) * Sk))))
+            return CTX_ERR_ALIASING;
+    }
+    ctx_status s = check_device_ptrs({q, k, v, out, lse, key_mask});
+    if (s != CTX_OK)
+        return s;
+    ctx::AttnArgs a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.mask = key_mask;
+    a.out = out;
+    a.lse = lse;
+    a.B = B;
+    a.Sq = Sq;
+    a.Sk = Sk;
+    a.H = H;
+    a.D = D;
+    a.bf16 = dtype == CTX_BF16;
+    a.scale = scale;
+    cudaError_t e = ctx::launch_attention(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CTX_OK : cuda_fail(e);
+}
+
+ctx_status ctx_device_status(void *stream)
+{
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    int *word = ctx::device_status_word(&e);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    int value = 0;
+    e = cudaMemcpy(&value, word, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    if (value != 0) {
+        const int zero = 0;
+        e = cudaMemcpy(word, &zero, sizeof(int), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess)
+            return cuda_fail(e);
+    }
+    return value == 0 ? CTX_OK : static_cast<ctx_status>(value);
+}
+
+ctx_status ctx_selftest_wait_timeout(long long limit_ns, void *stream)
+{
+    if (limit_ns < 1000 || limit_ns > 5000000000LL)
+        return CTX_ERR_INVALID_ARG;
+    cudaError_t e = ctx::launch_selftest_wait(static_cast<unsigned long long>(limit_ns),
+                                              static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    return ctx_device_status(stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,563 @@
+// Local-Q / global-KV attention forward for sm_103a.
+//
+// What it computes (vllm-omni PR #7641, local-Q / global-KV attention after
+// the K/V AllGather; ChituDiffusion "Fast CP": non-causal MHA): for every
+// (b, h, query i), softmax over the valid keys of scale * q.k, applied to V,
+// plus the natural-log LSE of the scores.
+//
+// How (GB300-first design):
+//   * one CTA = two 128-row query tiles of one (b, h) sharing one K/V stream;
+//   * warp 0 issues TMA loads: both Q tiles once, then K and V blocks of 128
+//     keys into a two-stage ring (128-byte swizzled tiles, mbarrier
+//     complete_tx accounting);
+//   * warp 1 allocates 512 TMEM columns and one elected lane issues every
+//     tcgen05.mma: S_t = Q_t K^T (A and B from shared memory, K-major) into
+//     TMEM columns [128t, 128t+128), and O_t += P_t V with P_t read from TMEM
+//     (it overwrites S_t as 16-bit pairs) and V from shared memory (MN-major)
+//     into columns [256 + Dt, 256 + D(t+1));
+//   * warps 2-5 and 6-9 are the softmax of tile 0 and tile 1: each thread
+//     owns one query row (its TMEM lane), reads its 128 scores with
+//     tcgen05.ld, does the online softmax in the log2 domain with exp2, writes
+//     P back with tcgen05.st and signals the MMA warp. The MMA warp issues
+//     PV_0(j-1), S_0(j), PV_1(j-1), S_1(j), so the tensor core works on one
+//     tile while the other tile's softmax runs;
+//   * O is rescaled only when a row maximum grows by more than 2^8 (a stale
+//     maximum keeps every probability <= 2^8, exact after the final division),
+//     which the public FlashAttention-4 write-up calls conditional rescaling;
+//   * epilogue: O / l rounded to the input type, LSE = ln2 * (m + log2 l).
+// Every wait is bounded (%globaltimer); on expiry the kernel records a
+// timeout in the device status word, drains its own TMA loads and MMAs, frees
+// TMEM and returns.
+#include <cmath>
+#include <cudaTypedefs.h>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace ctx {
+namespace {
+
+constexpr int kBM = 128;      // query rows per tile (= TMEM lanes)
+constexpr int kBN = 128;      // keys per block
+constexpr int kTiles = 2;     // query tiles per CTA
+constexpr int kStages = 2;    // depth of the K ring and of the V ring
+constexpr int kThreads = 320; // 10 warps
+constexpr int kTmemCols = 512;
+constexpr float kRescaleLog2 = 8.0f;
+constexpr float kLn2 = 0.693147180559945309f;
+
+struct Params {
+    const unsigned char *mask;
+    void *out;
+    float *lse;
+    int B, Sq, Sk, H;
+    int n_qpairs;
+    int n_kblocks;
+    float scale_log2;
+    int *status;
+    unsigned long long wait_limit_ns;
+};
+
+template <int D>
+struct Layout {
+    static constexpr int kPanels = D / 64;          // 64-element (128-byte) swizzle panels
+    static constexpr int kQBytes = kBM * D * 2;     // one Q tile
+    static constexpr int kKVBytes = kBN * D * 2;    // one K or V block
+    static constexpr int kQPanel = kBM * 128;       // bytes of one panel of a Q tile
+    static constexpr int kKVPanel = kBN * 128;
+    static constexpr int kQOff = 0;
+    static constexpr int kKOff = kQOff + kTiles * kQBytes;
+    static constexpr int kVOff = kKOff + kStages * kKVBytes;
+    static constexpr int kBarOff = kVOff + kStages * kKVBytes;
+    static constexpr int kNumBars = 1 + 4 * kStages + 3 * kTiles + 1;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    static constexpr int kBytes = kMiscOff + 16;
+    static constexpr int kAlloc = kBytes + 1024;    // room to align the base to 1024 B
+};
+
+// Bounded wait on an mbarrier phase. honor_abort: give up as soon as another
+// role has aborted. Returns false on abort or timeout.
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                         const Params &p, bool honor_abort = true)
+{
+    const uint32_t a = ptx::smem_u32(bar);
+    if (ptx::mbar_try_wait(a, parity))
+        return true;
+    const uint64_t t0 = ptx::globaltimer();
+    uint32_t spins = 0;
+    while (true) {
+        if (ptx::mbar_try_wait(a, parity))
+            return true;
+        if ((++spins & 31u) == 0) {
+            if (honor_abort && *abort_flag)
+                return false;
+            if (ptx::globaltimer() - t0 > p.wait_limit_ns) {
+                *abort_flag = 1;
+                atomicExch(p.status, kStatusTimeout);
+                return false;
+            }
+        }
+    }
+}
+
+// Warp-uniform version for the softmax warps (tcgen05.ld/st are .sync.aligned).
+__device__ __forceinline__ bool wait_bar_warp(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                              const Params &p)
+{
+    const bool ok = wait_bar(bar, parity, abort_flag, p);
+    return __all_sync(0xffffffffu, ok);
+}
+
+template <int D, bool BF16>
+__device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint32_t q_smem, uint32_t k_smem)
+{
+    using L = Layout<D>;
+    constexpr uint32_t idesc = ptx::idesc_f16(kBM, kBN, BF16, false, false);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t pnl = kk / 4, koff = (kk % 4) * 32;
+        const uint64_t a = ptx::sdesc_sw128(q_smem + pnl * L::kQPanel + koff, 16, 1024);
+        const uint64_t b = ptx::sdesc_sw128(k_smem + pnl * L::kKVPanel + koff, 16, 1024);
+        ptx::mma_ss(tmem_s, a, b, idesc, kk > 0 ? 1u : 0u);
+    }
+}
+
+template <int D, bool BF16>
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_smem, bool accumulate)
+{
+    using L = Layout<D>;
+    constexpr uint32_t idesc = ptx::idesc_f16(kBM, D, BF16, false, true);
+#pragma unroll
+    for (int kk = 0; kk < kBN / 16; ++kk) {
+        // 16 keys = two 8-row groups of 128 B; the next 64 d-columns are one panel further
+        const uint64_t b = ptx::sdesc_sw128(v_smem + kk * 16 * 128, L::kKVPanel, 1024);
+        ptx::mma_ts(tmem_o, tmem_p + kk * 8, b, idesc, (accumulate || kk > 0) ? 1u : 0u);
+    }
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const Params p)
+{
+    using L = Layout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
+    uint64_t *q_full = bars;
+    uint64_t *k_full = q_full + 1;
+    uint64_t *k_empty = k_full + kStages;
+    uint64_t *v_full = k_empty + kStages;
+    uint64_t *v_empty = v_full + kStages;
+    uint64_t *s_full = v_empty + kStages;
+    uint64_t *p_full = s_full + kTiles;
+    uint64_t *o_full = p_full + kTiles;
+    uint64_t *mma_done = o_full + kTiles;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qp = blockIdx.x % p.n_qpairs;
+    const int bh = blockIdx.x / p.n_qpairs;
+    const int h = bh % p.H, b = bh / p.H;
+    const int q0 = qp * (kTiles * kBM);
+    const int nblk = p.n_kblocks;
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(q_full, 1);
+        for (int s = 0; s < kStages; ++s) {
+            ptx::mbar_init(k_full + s, 1);
+            ptx::mbar_init(k_empty + s, 1);
+            ptx::mbar_init(v_full + s, 1);
+            ptx::mbar_init(v_empty + s, 1);
+        }
+        for (int t = 0; t < kTiles; ++t) {
+            ptx::mbar_init(s_full + t, 1);
+            ptx::mbar_init(p_full + t, 128);
+            ptx::mbar_init(o_full + t, 1);
+        }
+        ptx::mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(tmem_slot, kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            ptx::tma_prefetch_desc(&tmQ);
+            ptx::tma_prefetch_desc(&tmK);
+            ptx::tma_prefetch_desc(&tmV);
+            ptx::mbar_arrive_expect_tx(q_full, kTiles * L::kQBytes);
+            for (int t = 0; t < kTiles; ++t)
+                for (int pn = 0; pn < L::kPanels; ++pn)
+                    ptx::tma_load_4d(&tmQ, q_full, smem + L::kQOff + t * L::kQBytes + pn * L::kQPanel, pn * 64, h,
+                                     q0 + t * kBM, b);
+            int issued[kStages] = {0};
+            for (int j = 0; j < nblk; ++j) {
+                const int s = j % kStages, u = j / kStages;
+                if (u > 0 && !wait_bar(k_empty + s, (u - 1) & 1, abort_flag, p))
+                    break;
+                ptx::mbar_arrive_expect_tx(k_full + s, L::kKVBytes);
+                for (int pn = 0; pn < L::kPanels; ++pn)
+                    ptx::tma_load_4d(&tmK, k_full + s, smem + L::kKOff + s * L::kKVBytes + pn * L::kKVPanel, pn * 64,
+                                     h, j * kBN, b);
+                if (u > 0 && !wait_bar(v_empty + s, (u - 1) & 1, abort_flag, p)) {
+                    issued[s] = -(u + 1);  // K of use u issued, V not
+                    break;
+                }
+                ptx::mbar_arrive_expect_tx(v_full + s, L::kKVBytes);
+                for (int pn = 0; pn < L::kPanels; ++pn)
+                    ptx::tma_load_4d(&tmV, v_full + s, smem + L::kVOff + s * L::kKVBytes + pn * L::kKVPanel, pn * 64,
+                                     h, j * kBN, b);
+                issued[s] = u + 1;
+            }
+            // Drain: every issued load has landed before the CTA can exit.
+            wait_bar(q_full, 0, abort_flag, p, false);
+            for (int s = 0; s < kStages; ++s) {
+                int n = issued[s];
+                if (n < 0) {
+                    n = -n;
+                    wait_bar(k_full + s, (n - 1) & 1, abort_flag, p, false);
+                    if (n - 1 > 0)
+                        wait_bar(v_full + s, (n - 2) & 1, abort_flag, p, false);
+                } else if (n > 0) {
+                    wait_bar(k_full + s, (n - 1) & 1, abort_flag, p, false);
+                    wait_bar(v_full + s, (n - 1) & 1, abort_flag, p, false);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issue
+        if (lane == 0) {
+            const uint32_t qa0 = ptx::smem_u32(smem + L::kQOff);
+            const uint32_t qa1 = qa0 + L::kQBytes;
+            const uint32_t kbase = ptx::smem_u32(smem + L::kKOff);
+            const uint32_t vbase = ptx::smem_u32(smem + L::kVOff);
+            const uint32_t tS0 = tmem, tS1 = tmem + kBN;
+            const uint32_t tO0 = tmem + 2 * kBN, tO1 = tmem + 2 * kBN + D;
+            bool ok = wait_bar(q_full, 0, abort_flag, p);
+            if (ok)
+                ptx::tc_fence_after();
+            for (int j = 0; ok && j < nblk; ++j) {
+                const int s = j % kStages, u = j / kStages;
+                if (!(ok = wait_bar(k_full + s, u & 1, abort_flag, p)))
+                    break;
+                ptx::tc_fence_after();
+                const int jp = j - 1, sp = (j + kStages - 1) % kStages, up = jp / kStages;
+                if (j > 0) {
+                    if (!(ok = wait_bar(v_full + sp, up & 1, abort_flag, p)))
+                        break;
+                    if (!(ok = wait_bar(p_full + 0, jp & 1, abort_flag, p)))
+                        break;
+                    ptx::tc_fence_after();
+                    issue_pv<D, BF16>(tO0, tS0, vbase + sp * L::kKVBytes, jp > 0);
+                }
+                issue_qk<D, BF16>(tS0, qa0, kbase + s * L::kKVBytes);
+                ptx::tc_commit(s_full + 0);
+                if (j > 0) {
+                    if (!(ok = wait_bar(p_full + 1, jp & 1, abort_flag, p)))
+                        break;
+                    ptx::tc_fence_after();
+                    issue_pv<D, BF16>(tO1, tS1, vbase + sp * L::kKVBytes, jp > 0);
+                    ptx::tc_commit(v_empty + sp);
+                }
+                issue_qk<D, BF16>(tS1, qa1, kbase + s * L::kKVBytes);
+                ptx::tc_commit(s_full + 1);
+                ptx::tc_commit(k_empty + s);
+            }
+            if (ok) {
+                const int jl = nblk - 1, sl = jl % kStages, ul = jl / kStages;
+                ok = wait_bar(v_full + sl, ul & 1, abort_flag, p) && wait_bar(p_full + 0, jl & 1, abort_flag, p);
+                if (ok) {
+                    ptx::tc_fence_after();
+                    issue_pv<D, BF16>(tO0, tS0, vbase + sl * L::kKVBytes, jl > 0);
+                    ptx::tc_commit(o_full + 0);
+                    ok = wait_bar(p_full + 1, jl & 1, abort_flag, p);
+                }
+                if (ok) {
+                    ptx::tc_fence_after();
+                    issue_pv<D, BF16>(tO1, tS1, vbase + sl * L::kKVBytes, jl > 0);
+                    ptx::tc_commit(o_full + 1);
+                    ptx::tc_commit(v_empty + sl);
+                }
+            }
+            // Every MMA issued above has retired before TMEM is released.
+            ptx::tc_commit(mma_done);
+            wait_bar(mma_done, 0, abort_flag, p, false);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int t = (warp - 2) >> 2;  // query tile
+        const int quad = warp & 3;      // TMEM lane quadrant this warp may access
+        const int row = quad * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t tS = tmem + lane_off + t * kBN;
+        const uint32_t tO = tmem + lane_off + 2 * kBN + t * D;
+        const unsigned char *mrow = p.mask ? p.mask + static_cast<size_t>(b) * p.Sk : nullptr;
+        const float c = p.scale_log2;
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nblk; ++j) {
+            const int kb = j * kBN;
+            // validity of the block's keys, one bit per key, identical in every lane
+            uint32_t vb[4];
+            if (mrow) {
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const int key = kb + w * 32 + lane;
+                    const bool v = key < p.Sk && mrow[key] != 0;
+                    vb[w] = __ballot_sync(0xffffffffu, v);
+                }
+            } else {
+                const int vn = p.Sk - kb;
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const int n = vn - 32 * w;
+                    vb[w] = n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
+                }
+            }
+            const bool all_valid = (vb[0] & vb[1] & vb[2] & vb[3]) == 0xffffffffu;
+
+            if (!(ok = wait_bar_warp(s_full + t, j & 1, abort_flag, p)))
+                break;
+            ptx::tc_fence_after();
+            uint32_t sr[kBN];
+            ptx::tmem_ld32(tS + 0, sr + 0);
+            ptx::tmem_ld32(tS + 32, sr + 32);
+            ptx::tmem_ld32(tS + 64, sr + 64);
+            ptx::tmem_ld32(tS + 96, sr + 96);
+            ptx::tmem_ld_wait();
+            ptx::reg_fence32(sr + 0);
+            ptx::reg_fence32(sr + 32);
+            ptx::reg_fence32(sr + 64);
+            ptx::reg_fence32(sr + 96);
+            float s[kBN];
+#pragma unroll
+            for (int i = 0; i < kBN; ++i)
+                s[i] = __uint_as_float(sr[i]);
+            if (!all_valid) {
+#pragma unroll
+                for (int i = 0; i < kBN; ++i)
+                    if (!((vb[i >> 5] >> (i & 31)) & 1u))
+                        s[i] = -INFINITY;
+            }
+            float mx = s[0];
+#pragma unroll
+            for (int i = 1; i < kBN; ++i)
+                mx = fmaxf(mx, s[i]);
+            const float m_new = fmaxf(m_run, mx * c);
+            if (j == 0) {
+                m_run = m_new;
+            } else {
+                const bool need = m_new > m_run + kRescaleLog2;
+                if (__any_sync(0xffffffffu, need)) {
+                    // PV of block j-1 has completed: S(j) was committed after it.
+                    const float alpha = need ? ptx::ex2_approx(m_run - m_new) : 1.0f;
+                    if (need) {
+                        l_run *= alpha;
+                        m_run = m_new;
+                    }
+#pragma unroll 1
+                    for (int c0 = 0; c0 < D / 16; ++c0) {
+                        uint32_t o[16];
+                        ptx::tmem_ld16(tO + c0 * 16, o);
+                        ptx::tmem_ld_wait();
+                        ptx::reg_fence16(o);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        ptx::tmem_st16(tO + c0 * 16, o);
+                    }
+                    ptx::tmem_st_wait();
+                }
+            }
+            const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
+            float lsum = 0.f;
+            // P overwrites the first 64 columns of S, 32 columns (64 keys) at a time
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float p0 = ptx::ex2_approx(fmaf(s[64 * half + 2 * i], c, neg_m));
+                    const float p1 = ptx::ex2_approx(fmaf(s[64 * half + 2 * i + 1], c, neg_m));
+                    lsum += p0 + p1;
+                    pk[i] = ptx::pack2<BF16>(p0, p1);
+                }
+                ptx::tmem_st32(tS + 32 * half, pk);
+            }
+            l_run += lsum;
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(p_full + t);
+        }
+        if (ok && wait_bar_warp(o_full + t, 0, abort_flag, p)) {
+            ptx::tc_fence_after();
+            const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
+            const int qrow = q0 + t * kBM + row;
+            uint4 *orow = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) +
+                                                    ((static_cast<size_t>(b) * p.Sq + qrow) * p.H + h) * D);
+#pragma unroll
+            for (int c0 = 0; c0 < D / 32; ++c0) {
+                uint32_t o[32];
+                ptx::tmem_ld32(tO + c0 * 32, o);
+                ptx::tmem_ld_wait();
+                ptx::reg_fence32(o);
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    w[i] = ptx::pack2<BF16>(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+                if (qrow < p.Sq) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        orow[c0 * 4 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                }
+            }
+            if (p.lse && qrow < p.Sq)
+                p.lse[(static_cast<size_t>(b) * p.H + h) * p.Sq + qrow] =
+                    l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// A single block waiting on an mbarrier that nothing arrives on: exercises the
+// bounded-wait failure path (status word set, clean return).
+__global__ void selftest_wait_kernel(int *status, unsigned long long limit_ns)
+{
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(&bar, 1);
+        abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    Params p{};
+    p.status = status;
+    p.wait_limit_ns = limit_ns;
+    wait_bar(&bar, 0, &abort_flag, p);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// [B, S, H, D] 16-bit tensor viewed as 4-D (d, h, s, b), 64 x 1 x 128 x 1 boxes.
+cudaError_t make_map(CUtensorMap *m, const void *base, int B, int S, int H, int D, bool bf16)
+{
+    auto enc = tensor_map_encoder();
+    if (!enc)
+        return cudaErrorNotSupported;
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(S),
+                          static_cast<cuuint64_t>(B)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2,
+                             static_cast<cuuint64_t>(S) * H * D * 2};
+    cuuint32_t box[4] = {64, 1, 128, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+                     const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int D, bool BF16>
+cudaError_t launch_typed(const AttnArgs &a, cudaStream_t stream)
+{
+    using L = Layout<D>;
+    static bool attr_set[64] = {false};
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess)
+        return err;
+    {
+        std::lock_guard<std::mutex> g(mu);
+        if (dev >= 64 || !attr_set[dev]) {
+            err = cudaFuncSetAttribute(attn_fwd_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       L::kAlloc);
+            if (err != cudaSuccess)
+                return err;
+            if (dev < 64)
+                attr_set[dev] = true;
+        }
+    }
+    CUtensorMap mq, mk, mv;
+    if ((err = make_map(&mq, a.q, a.B, a.Sq, a.H, D, BF16)) != cudaSuccess)
+        return err;
+    if ((err = make_map(&mk, a.k, a.B, a.Sk, a.H, D, BF16)) != cudaSuccess)
+        return err;
+    if ((err = make_map(&mv, a.v, a.B, a.Sk, a.H, D, BF16)) != cudaSuccess)
+        return err;
+    Params p{};
+    p.mask = a.mask;
+    p.out = a.out;
+    p.lse = a.lse;
+    p.B = a.B;
+    p.Sq = a.Sq;
+    p.Sk = a.Sk;
+    p.H = a.H;
+    p.n_qpairs = (a.Sq + kTiles * kBM - 1) / (kTiles * kBM);
+    p.n_kblocks = (a.Sk + kBN - 1) / kBN;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.status = device_status_word(&err);
+    if (err != cudaSuccess)
+        return err;
+    p.wait_limit_ns = kDefaultWaitLimitNs;
+    const long long grid = static_cast<long long>(p.n_qpairs) * a.H * a.B;
+    if (grid > 0x7fffffffLL)
+        return cudaErrorInvalidConfiguration;
+    attn_fwd_kernel<D, BF16><<<static_cast<unsigned>(grid), kThreads, L::kAlloc, stream>>>(mq, mk, mv, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attention(const AttnArgs &a, cudaStream_t stream)
+{
+    if (a.D == 128)
+        return a.bf16 ? launch_typed<128, true>(a, stream) : launch_typed<128, false>(a, stream);
+    if (a.D == 64)
+        return a.bf16 ? launch_typed<64, true>(a, stream) : launch_typed<64, false>(a, stream);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_selftest_wait(unsigned long long limit_ns, cudaStream_t stream)
+{
+    cudaError_t err = cudaSuccess;
+    int *status = device_status_word(&err);
+    if (err != cudaSuccess)
+        return err;
+    selftest_wait_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace ctx

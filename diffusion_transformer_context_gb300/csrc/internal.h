@@ -1,0 +1,59 @@
+// Internal launcher interface between the C-ABI layer (api.cu) and the kernel
+// translation units. Arguments reaching these functions are already validated.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace ctx {
+
+// Device status codes written by kernels (same values as ctx_status).
+constexpr int kStatusOk = 0;
+constexpr int kStatusTimeout = 6;
+
+// Bound for every device-side wait (nanoseconds of %globaltimer).
+constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;
+
+// Address of the current device's status word (set up once per device).
+int *device_status_word(cudaError_t *err);
+
+// Number of SMs of the current device (cached per device).
+int sm_count(cudaError_t *err);
+
+enum class RelayoutMode : int { PackQKV = 0, UnpackQKV = 1, PackOut = 2, UnpackOut = 3, AllToAll = 4 };
+
+// Every relayout step moves "runs": contiguous groups of 16-byte vectors that
+// are contiguous in both source and destination. The mode maps a run index to
+// its source and destination offsets.
+struct RelayoutArgs {
+    const void *src0;  // pack: q; otherwise the (only) source
+    const void *src1;  // pack: k
+    const void *src2;  // pack: v
+    void *dst0;        // unpack: q'; otherwise the (only) destination
+    void *dst1;        // unpack: k'
+    void *dst2;        // unpack: v'
+    long long n_runs;
+    long long run_vec;  // 16-byte vectors per run
+    // shape parameters (meaning depends on the mode)
+    long long B, S_l, H, h_l, U, G;
+    long long q_batch_stride_rows;   // unpack: Q' batch stride; pack_out: O batch stride
+    long long kv_batch_stride_rows;  // unpack: K'/V' batch stride
+};
+
+cudaError_t launch_relayout(RelayoutMode mode, const RelayoutArgs &a, cudaStream_t stream);
+
+struct AttnArgs {
+    const void *q, *k, *v;
+    const unsigned char *mask;
+    void *out;
+    float *lse;
+    int B, Sq, Sk, H, D;
+    bool bf16;
+    float scale;
+};
+
+cudaError_t launch_attention(const AttnArgs &a, cudaStream_t stream);
+
+cudaError_t launch_selftest_wait(unsigned long long limit_ns, cudaStream_t stream);
+
+}  // namespace ctx

@@ -1,0 +1,173 @@
+// Ulysses layout steps: pack / unpack of Q,K,V, the reverse output exchange,
+// and the simulated all_to_all_single between ranks on one GPU.
+//
+// All of them are permutations of "runs": h_l*D contiguous elements (one
+// destination rank's heads of one row) that stay contiguous on both sides
+// (sglang PR #33667, pack_qkv_destination_major: destination r gets heads
+// [r*H/U, (r+1)*H/U) of every row). The kernel is HBM bound: a warp moves one
+// run (or one segment of a long run) with 16-byte vector loads that bypass L1
+// and 16-byte stores, each lane keeping up to 8 loads in flight before it
+// stores, and the grid is sized from the occupancy of the SMs.
+#include <algorithm>
+#include <mutex>
+
+#include "internal.h"
+
+namespace ctx {
+namespace {
+
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Source and destination of run `run` (in 16-byte vectors). rv = run length;
+// a row of H heads is U runs long (H*D/8 = U*rv).
+template <RelayoutMode M>
+__device__ __forceinline__ void map_run(const RelayoutArgs &a, long long run, const uint4 *&src, uint4 *&dst)
+{
+    const long long rv = a.run_vec;
+    if constexpr (M == RelayoutMode::PackQKV) {
+        // run = ((r*3 + t)*B + b)*S_l + s  (destination order)
+        long long s = run % a.S_l, x = run / a.S_l;
+        long long b = x % a.B;
+        x /= a.B;
+        long long t = x % 3, r = x / 3;
+        const uint4 *base = static_cast<const uint4 *>(t == 0 ? a.src0 : (t == 1 ? a.src1 : a.src2));
+        src = base + ((b * a.S_l + s) * a.U + r) * rv;
+        dst = static_cast<uint4 *>(a.dst0) + run * rv;
+    } else if constexpr (M == RelayoutMode::UnpackQKV) {
+        // run = ((r*3 + t)*B + b)*S_l + s  (source order)
+        long long s = run % a.S_l, x = run / a.S_l;
+        long long b = x % a.B;
+        x /= a.B;
+        long long t = x % 3, r = x / 3;
+        uint4 *base = static_cast<uint4 *>(t == 0 ? a.dst0 : (t == 1 ? a.dst1 : a.dst2));
+        const long long stride = t == 0 ? a.q_batch_stride_rows : a.kv_batch_stride_rows;
+        src = static_cast<const uint4 *>(a.src0) + run * rv;
+        dst = base + (b * stride + r * a.S_l + s) * rv;
+    } else if constexpr (M == RelayoutMode::PackOut) {
+        // run = (r*B + b)*S_l + s  (destination order)
+        long long s = run % a.S_l, x = run / a.S_l;
+        long long b = x % a.B, r = x / a.B;
+        src = static_cast<const uint4 *>(a.src0) + (b * a.q_batch_stride_rows + r * a.S_l + s) * rv;
+        dst = static_cast<uint4 *>(a.dst0) + run * rv;
+    } else if constexpr (M == RelayoutMode::UnpackOut) {
+        // run = (r*B + b)*S_l + s  (source order)
+        long long s = run % a.S_l, x = run / a.S_l;
+        long long b = x % a.B, r = x / a.B;
+        src = static_cast<const uint4 *>(a.src0) + run * rv;
+        dst = static_cast<uint4 *>(a.dst0) + ((b * a.S_l + s) * a.U + r) * rv;
+    } else {
+        // AllToAll: run = (g*U + r)*U + j (source order) -> recv[g][j][r]
+        long long j = run % a.U, x = run / a.U;
+        long long r = x % a.U, g = x / a.U;
+        src = static_cast<const uint4 *>(a.src0) + run * rv;
+        dst = static_cast<uint4 *>(a.dst0) + ((g * a.U + j) * a.U + r) * rv;
+    }
+}
+
+template <RelayoutMode M, int VPL>
+__global__ void __launch_bounds__(256) relayout_kernel(RelayoutArgs a, long long n_items, int n_segs)
+{
+    constexpr long long kSegVec = 32LL * VPL;
+    const int lane = threadIdx.x & 31;
+    const long long warp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const long long n_warps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+    for (long long item = warp; item < n_items; item += n_warps) {
+        long long run = item, seg = 0;
+        if (n_segs > 1) {
+            run = item / n_segs;
+            seg = item - run * n_segs;
+        }
+        const uint4 *src;
+        uint4 *dst;
+        map_run<M>(a, run, src, dst);
+        const long long base = seg * kSegVec;
+        const long long lim = min(a.run_vec - base, kSegVec);
+        uint4 buf[VPL];
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const long long c = lane + 32 * i;
+            if (c < lim)
+                buf[i] = ld_stream(src + base + c);
+        }
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const long long c = lane + 32 * i;
+            if (c < lim)
+                dst[base + c] = buf[i];
+        }
+    }
+}
+
+template <RelayoutMode M, int VPL>
+cudaError_t launch_vpl(const RelayoutArgs &a, cudaStream_t stream)
+{
+    static int blocks_per_sm[64] = {0};
+    static std::mutex mu;
+    const int n_segs = static_cast<int>((a.run_vec + 32LL * VPL - 1) / (32LL * VPL));
+    const long long n_items = a.n_runs * n_segs;
+    if (n_items == 0)
+        return cudaSuccess;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess)
+        return err;
+    int bps;
+    {
+        std::lock_guard<std::mutex> g(mu);
+        if (dev < 64 && blocks_per_sm[dev] == 0) {
+            err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm[dev], relayout_kernel<M, VPL>, 256, 0);
+            if (err != cudaSuccess)
+                return err;
+            if (blocks_per_sm[dev] < 1)
+                blocks_per_sm[dev] = 1;
+        }
+        bps = dev < 64 ? blocks_per_sm[dev] : 1;
+    }
+    const int sms = sm_count(&err);
+    if (err != cudaSuccess)
+        return err;
+    const long long want = (n_items + 7) / 8;  // 8 warps per block
+    const long long cap = static_cast<long long>(sms) * bps;
+    const unsigned grid = static_cast<unsigned>(std::max(1LL, std::min(want, cap)));
+    relayout_kernel<M, VPL><<<grid, 256, 0, stream>>>(a, n_items, n_segs);
+    return cudaGetLastError();
+}
+
+template <RelayoutMode M>
+cudaError_t launch_mode(const RelayoutArgs &a, cudaStream_t stream)
+{
+    const long long vpl = std::min(8LL, (a.run_vec + 31) / 32);
+    switch (vpl) {
+    case 1: return launch_vpl<M, 1>(a, stream);
+    case 2: return launch_vpl<M, 2>(a, stream);
+    case 3: return launch_vpl<M, 3>(a, stream);
+    case 4: return launch_vpl<M, 4>(a, stream);
+    case 5: return launch_vpl<M, 5>(a, stream);
+    case 6: return launch_vpl<M, 6>(a, stream);
+    case 7: return launch_vpl<M, 7>(a, stream);
+    default: return launch_vpl<M, 8>(a, stream);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_relayout(RelayoutMode mode, const RelayoutArgs &a, cudaStream_t stream)
+{
+    switch (mode) {
+    case RelayoutMode::PackQKV: return launch_mode<RelayoutMode::PackQKV>(a, stream);
+    case RelayoutMode::UnpackQKV: return launch_mode<RelayoutMode::UnpackQKV>(a, stream);
+    case RelayoutMode::PackOut: return launch_mode<RelayoutMode::PackOut>(a, stream);
+    case RelayoutMode::UnpackOut: return launch_mode<RelayoutMode::UnpackOut>(a, stream);
+    case RelayoutMode::AllToAll: return launch_mode<RelayoutMode::AllToAll>(a, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace ctx

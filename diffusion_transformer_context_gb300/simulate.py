@@ -1,0 +1,160 @@
+"""All U x A virtual ranks of one context-parallel attention layer on one GPU.
+
+Rank g = a*U + u (vllm-omni PR #7641: Ulysses groups are contiguous blocks of
+U ranks, AllGather-KV groups stride by U) holds input rows [g*S_l, (g+1)*S_l)
+of Q, K, V [B, S, H, D]. One step runs, through the C ABI only:
+
+  1. ctx_pack_qkv for every rank into its staging buffer;
+  2. ctx_sim_all_to_all inside every U group (skipped at U = 1, where the
+     exchange is the identity);
+  3. ctx_unpack_qkv for every rank, writing its local Q rows into the
+     all-ranks query buffer and its K/V rows straight into the gathered K/V
+     buffer of its head group at rows [a*S/A, (a+1)*S/A): the K/V AllGather is
+     this placement, no bytes are copied for it;
+  4. one ctx_attn_lq_gkv over all ranks: the ranks of head group u share the
+     gathered K/V, so their local-Q slices stack into one [S, h_l] query set
+     per u, batched over u (rows are independent, so this equals one launch
+     per rank);
+  5. the reverse exchange ctx_pack_out -> ctx_sim_all_to_all ->
+     ctx_unpack_out for every rank (at U = 1 the output rows already are the
+     sequence-sharded result and step 5 is the identity).
+
+Joint (text) keys and values are inputs every rank already holds; they are
+written once, head-sliced, after the S image rows of each gathered K/V buffer
+(the "re-attach" of the same page), and the merged key mask [B, S + joint]
+is replicated per head group.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import (ctx_attn_lq_gkv, ctx_pack_out, ctx_pack_qkv, ctx_sim_all_to_all, ctx_unpack_out,
+               ctx_unpack_qkv)
+
+
+class SimLayer:
+    def __init__(self, wl, device="cuda", dtype=torch.bfloat16, attention: bool | None = None):
+        self.wl = wl
+        self.dev = torch.device(device)
+        self.dtype = dtype
+        U, A, B, S, H, D, J = wl.U, wl.A, wl.B, wl.S, wl.H, wl.D, wl.joint
+        if S % (U * A) or H % U:
+            raise ValueError("S must divide by U*A and H by U")
+        self.R, self.S_l, self.h_l, self.Sk = U * A, S // (U * A), H // U, S + J
+        self.attention = wl.attention if attention is None else attention
+        R, S_l, h_l, Sk = self.R, self.S_l, self.h_l, self.Sk
+        kw = dict(dtype=dtype, device=self.dev)
+        self.x = torch.empty((R, 3, B, S_l, H, D), **kw)           # per-rank inputs
+        chunk = 3 * B * S_l * h_l * D
+        self.send = torch.empty((A, U, U, chunk), **kw)             # [group a, src u, dst chunk]
+        self.recv = torch.empty_like(self.send) if U > 1 else self.send
+        self.qg = torch.empty((U, B, S, h_l, D), **kw)              # local-Q of all ranks
+        self.kg = torch.empty((U, B, Sk, h_l, D), **kw)             # gathered K (+ joint)
+        self.vg = torch.empty((U, B, Sk, h_l, D), **kw)
+        self.mask = torch.ones((U * B, Sk), dtype=torch.uint8, device=self.dev) if wl.joint else None
+        self.out = torch.empty((U, B, S, h_l, D), **kw)
+        self.lse = torch.empty((U * B, h_l, S), dtype=torch.float32, device=self.dev)
+        if U > 1:
+            ochunk = B * S_l * h_l * D
+            self.osend = torch.empty((A, U, U, ochunk), **kw)
+            self.orecv = torch.empty_like(self.osend)
+            self.y = torch.empty((R, B, S_l, H, D), **kw)
+
+    # ---------------------------------------------------------- inputs
+    def load(self, inp, pinned: bool = False):
+        """Copy per-rank shards, joint K/V and the key mask to the device."""
+        wl, U = self.wl, self.wl.U
+        for g in range(self.R):
+            for t, src in enumerate((inp.q, inp.k, inp.v)):
+                self.x[g, t].copy_(inp.shard(src, g))
+        if wl.joint:
+            S, h_l = wl.S, self.h_l
+            for u in range(U):
+                self.kg[u, :, S:].copy_(inp.jk[:, :, u * h_l:(u + 1) * h_l])
+                self.vg[u, :, S:].copy_(inp.jv[:, :, u * h_l:(u + 1) * h_l])
+            m = inp.key_mask()
+            if m is not None:
+                self.mask.copy_(torch.from_numpy(np.tile(m, (U, 1))))
+        torch.cuda.synchronize(self.dev)
+
+    # ---------------------------------------------------------- one step
+    def step(self, stream=None):
+        wl = self.wl
+        U, A, B, S, D = wl.U, wl.A, wl.B, wl.S, wl.D
+        S_l, h_l, Sk = self.S_l, self.h_l, self.Sk
+        for g in range(self.R):
+            a, u = divmod(g, U)
+            x = self.x[g]
+            ctx_pack_qkv(x[0], x[1], x[2], self.send[a, u], U, stream=stream)
+        if U > 1:
+            ctx_sim_all_to_all(self.send, self.recv, A, U, stream=stream)
+        for g in range(self.R):
+            a, u = divmod(g, U)
+            r0 = a * U * S_l
+            ctx_unpack_qkv(self.recv[a, u].view(U, 3, B, S_l, h_l, D), self.qg[u, :, r0:], self.kg[u, :, r0:],
+                           self.vg[u, :, r0:], U, q_batch_stride_rows=S, kv_batch_stride_rows=Sk, stream=stream)
+        if self.attention:
+            ctx_attn_lq_gkv(self.qg.view(U * B, S, h_l, D), self.kg.view(U * B, Sk, h_l, D),
+                            self.vg.view(U * B, Sk, h_l, D), self.out.view(U * B, S, h_l, D), self.lse,
+                            key_mask=self.mask, stream=stream)
+            if U > 1:
+                for g in range(self.R):
+                    a, u = divmod(g, U)
+                    ctx_pack_out(self.out[u, :, a * U * S_l:], self.osend[a, u].view(U, B, S_l, h_l, D), U,
+                                 o_batch_stride_rows=S, stream=stream)
+                ctx_sim_all_to_all(self.osend, self.orecv, A, U, stream=stream)
+                for g in range(self.R):
+                    a, u = divmod(g, U)
+                    ctx_unpack_out(self.orecv[a, u].view(U, B, S_l, h_l, D), self.y[g], U, stream=stream)
+
+    def launches_per_step(self) -> int:
+        U, R = self.wl.U, self.R
+        n = 2 * R + (1 if U > 1 else 0)
+        if self.attention:
+            n += 1 + ((2 * R + 1) if U > 1 else 0)
+        return n
+
+    # ---------------------------------------------------------- results
+    def rank_output(self, g: int) -> torch.Tensor:
+        """Rank g's sequence-sharded attention output [B, S_l, H, D]."""
+        if self.wl.U > 1:
+            return self.y[g]
+        return self.out[0, :, g * self.S_l:(g + 1) * self.S_l]
+
+    def rank_q(self, g: int) -> torch.Tensor:
+        a, u = divmod(g, self.wl.U)
+        rows = self.wl.S // self.wl.A
+        return self.qg[u, :, a * rows:(a + 1) * rows]
+
+    # ---------------------------------------------------------- work model
+    def pack_bytes(self) -> int:
+        """Algorithmic HBM bytes (read + write) of all packs of one step."""
+        wl = self.wl
+        return 2 * 3 * self.R * wl.B * self.S_l * wl.H * wl.D * 2
+
+    def unpack_bytes(self) -> int:
+        return self.pack_bytes()
+
+    def a2a_bytes(self) -> int:
+        return self.pack_bytes() if self.wl.U > 1 else 0
+
+    def reverse_bytes(self) -> int:
+        wl = self.wl
+        if not self.attention or wl.U == 1:
+            return 0
+        one = 2 * self.R * wl.B * self.S_l * wl.H * wl.D * 2  # one pass, read + write
+        return 3 * one  # pack_out, all-to-all, unpack_out
+
+    def attn_flops(self, text_len=None, dense: bool = False) -> float:
+        """4 * Sq * K_valid * D per head (QK^T and PV), summed over all ranks."""
+        wl = self.wl
+        if not self.attention:
+            return 0.0
+        per_b = []
+        for b in range(wl.B):
+            kv = self.Sk
+            if not dense and wl.joint and text_len is not None:
+                kv = wl.S + int(text_len[b])
+            per_b.append(kv)
+        return float(sum(4.0 * wl.U * self.h_l * wl.S * kv * wl.D for kv in per_b))

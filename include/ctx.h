@@ -1,0 +1,213 @@
+/*
+ * ctx.h — C ABI of libctx: the data-parallel hot path of context-parallel
+ * diffusion-transformer attention on one GB300 (sm_103a).
+ *
+ * The path, in the order a rank runs it (vllm-omni PR #7641, "Compose Ulysses
+ * with AllGather-KV as a 2D diffusion SP": Ulysses all-to-all in the U group,
+ * K/V AllGather in the A group, local-Q / global-KV attention, reverse
+ * Ulysses all-to-all):
+ *
+ *   ctx_pack_qkv     per-rank Q/K/V [B,S_l,H,D] -> destination-major staging
+ *                    buffer [U,3,B,S_l,H/U,D] (sglang PR #33667,
+ *                    pack_qkv_destination_major / _usp_input_all_to_all_qkv)
+ *   ctx_sim_all_to_all   all_to_all_single chunk semantics between the
+ *                    simulated ranks of one GPU (sglang PR #33667 unit test)
+ *   ctx_unpack_qkv   received buffer -> [B,U*S_l,H/U,D] x3, written at a
+ *                    caller-chosen row offset/stride so that K/V land in the
+ *                    gathered global buffer (the AllGather placement)
+ *   ctx_attn_lq_gkv  non-causal MHA of local queries against gathered keys,
+ *                    optional per-key mask, scale, fp32 LSE
+ *   ctx_pack_out / ctx_unpack_out   the reverse (output) exchange
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every tensor pointer is a DEVICE pointer (cudaMalloc'd or managed memory);
+ *    the library checks this and returns CTX_ERR_INVALID_ARG for host memory.
+ *  - Tensors are dense, row-major, innermost dimension last, in the layouts
+ *    written beside each argument. Element type is bf16 or fp16 (ctx_dtype);
+ *    16-bit elements are moved bit for bit by the layout steps.
+ *  - Every data pointer must be 16-byte aligned and D a multiple of 8 (rows a
+ *    multiple of 16 bytes); otherwise CTX_ERR_MISALIGNED.
+ *  - The caller owns every buffer, including the staging buffers; the library
+ *    allocates nothing and keeps no state between calls.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream). Calls are asynchronous with respect to the host: CTX_OK means
+ *    the work was validated and enqueued.
+ *  - Arguments are validated on the host before anything is enqueued; a bad
+ *    argument returns an error and enqueues nothing (fail closed: there is no
+ *    fallback path).
+ *  - Inputs and outputs of one call must occupy disjoint address ranges
+ *    (CTX_ERR_ALIASING; the check is conservative: whole extents).
+ *  - A failed launch returns CTX_ERR_CUDA; ctx_last_cuda_error() gives the
+ *    cudaError_t of the last failure on the calling thread.
+ *  - Device-side pipeline waits are bounded: a wait that runs out records
+ *    CTX_ERR_TIMEOUT in a device status word and the kernel returns instead
+ *    of hanging; ctx_device_status() reads and clears it.
+ */
+#ifndef CTX_H_
+#define CTX_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum ctx_status {
+    CTX_OK = 0,
+    CTX_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, bad shape, host pointer */
+    CTX_ERR_UNSUPPORTED = 2,  /* valid request outside the supported set (e.g. D not 64/128) */
+    CTX_ERR_MISALIGNED = 3,   /* pointer not 16-byte aligned or row not a multiple of 16 B */
+    CTX_ERR_ALIASING = 4,     /* an output overlaps an input or another output */
+    CTX_ERR_CUDA = 5,         /* a CUDA runtime / driver call failed */
+    CTX_ERR_TIMEOUT = 6       /* a bounded device-side wait ran out */
+} ctx_status;
+
+typedef enum ctx_dtype { CTX_BF16 = 0, CTX_FP16 = 1 } ctx_dtype;
+
+/*
+ * ctx_pack_qkv — Ulysses send-side relayout (sglang PR #33667, implementation
+ * items 2-3 and the _usp_input_all_to_all_qkv excerpt: one kernel writes Q, K
+ * and V destination-major into one staging buffer, replacing three
+ * permute+contiguous copies).
+ *
+ *   staging[r][t][b][s][h][d] = X_t[b][s][r*h_l + h][d],  X_0,1,2 = q,k,v,
+ *   h_l = H/U, r in [0,U)
+ *
+ * q, k, v  : [B, S_l, H, D] each, device, read only.
+ * staging  : [U, 3, B, S_l, H/U, D], device, written in full. Chunk r (the
+ *            r-th of U equal parts of the flat buffer) is what rank r must
+ *            receive.
+ * Errors   : INVALID_ARG if a size <= 0 or H % U != 0; MISALIGNED; ALIASING
+ *            if staging overlaps q, k or v.
+ */
+ctx_status ctx_pack_qkv(const void *q, const void *k, const void *v, void *staging,
+                        int B, int S_l, int H, int D, int U, ctx_dtype dtype,
+                        void *stream);
+
+/*
+ * ctx_sim_all_to_all — all_to_all_single between simulated ranks on one GPU
+ * (sglang PR #33667 unit test, _run_all_ranks: rank r's chunk j becomes rank
+ * j's chunk r). It stands in for the NCCL collective of a multi-GPU
+ * deployment: part of the single-GPU simulation, not of a rank's work.
+ *
+ * send : [G, U, U, chunk_bytes] bytes: group g, source rank r, chunk j.
+ * recv : [G, U, U, chunk_bytes] bytes: group g, destination rank j, chunk r.
+ *        recv[g][j][r] = send[g][r][j].
+ * chunk_bytes must be a positive multiple of 16. Errors as above.
+ */
+ctx_status ctx_sim_all_to_all(const void *send, void *recv, int G, int U,
+                              long long chunk_bytes, void *stream);
+
+/*
+ * ctx_unpack_qkv — Ulysses receive-side relayout (sglang PR #33667,
+ * _usp_input_all_to_all_qkv excerpt: chunk r holds source rank r's rows,
+ * which become rows [r*S_l, (r+1)*S_l) of the head-sharded sequence; batch
+ * stays outermost).
+ *
+ *   X'_t[b][r*S_l + s][h][d] = recv[r][t][b][s][h][d]
+ *
+ * recv     : [U, 3, B, S_l, h_l, D], device, read only.
+ * q        : output base; element (b, row, h, d) of Q' is at
+ *            q + ((b*q_batch_stride_rows + row)*h_l + h)*D + d.
+ * k, v     : output bases, same form with kv_batch_stride_rows.
+ *            To place a rank's K/V straight into the gathered [B, Sk, h_l, D]
+ *            buffer (the AllGather placement of vllm-omni PR #7641: A-group
+ *            member a owns rows [a*S/A, (a+1)*S/A)), pass
+ *            k = gathered_k + a*(U*S_l)*h_l*D and kv_batch_stride_rows = Sk.
+ * q_batch_stride_rows, kv_batch_stride_rows : >= U*S_l.
+ * Errors   : INVALID_ARG for bad sizes/strides; MISALIGNED; ALIASING if an
+ *            output extent overlaps recv or another output.
+ */
+ctx_status ctx_unpack_qkv(const void *recv, void *q, void *k, void *v,
+                          long long q_batch_stride_rows,
+                          long long kv_batch_stride_rows, int B, int S_l,
+                          int h_l, int D, int U, ctx_dtype dtype, void *stream);
+
+/*
+ * ctx_attn_lq_gkv — local-Q / global-KV attention forward (vllm-omni PR
+ * #7641: each rank attends its query slice against the gathered K/V as a
+ * plain non-causal attention problem; ChituDiffusion "Fast CP" support
+ * matrix: non-causal MHA, D=128). For every b, head h and query row i:
+ *
+ *   s_j = scale * <q[b,i,h,:], k[b,j,h,:]>   over keys j with key_mask[b,j] != 0
+ *   out[b,i,h,:] = sum_j exp(s_j - m) v[b,j,h,:] / sum_j exp(s_j - m)
+ *   lse[b,h,i]   = m + ln sum_j exp(s_j - m),   m = max_j s_j
+ *
+ * A row with no valid key gets out = 0 and lse = -inf.
+ *
+ * q        : [B, Sq, H, D], device.
+ * k, v     : [B, Sk, H, D], device.
+ * key_mask : NULL (all keys valid) or [B, Sk] bytes, nonzero = attend (the
+ *            merged image + joint-text key mask; joint tokens may sit before
+ *            or after the image keys).
+ * scale    : softmax scale; NaN selects 1/sqrt(D). Otherwise finite and > 0.
+ * out      : [B, Sq, H, D], device, same dtype as q.
+ * lse      : NULL or [B, H, Sq] float32, device (natural log).
+ * D        : 64 or 128 (CTX_ERR_UNSUPPORTED otherwise).
+ * Numerics : fp32 accumulation for QK^T, softmax and PV; the probabilities
+ *            are rounded to the input dtype before the PV product; out is
+ *            rounded to nearest even.
+ */
+ctx_status ctx_attn_lq_gkv(const void *q, const void *k, const void *v,
+                           const unsigned char *key_mask, float scale,
+                           void *out, float *lse, int B, int Sq, int Sk, int H,
+                           int D, ctx_dtype dtype, void *stream);
+
+/*
+ * ctx_pack_out — reverse Ulysses exchange, send side (sglang PR #33667,
+ * _usp_output_all_to_all; vllm-omni PR #7641, reverse Ulysses all-to-all):
+ * rows of the head-sharded output go back to the rank that owns them.
+ *
+ *   send[r][b][s][h][d] = o[b][r*S_l + s][h][d]
+ *
+ * o    : device; element (b, row, h, d) is at
+ *        o + ((b*o_batch_stride_rows + row)*h_l + h)*D + d, row < U*S_l
+ *        (a rank's rows inside a larger output buffer need no copy).
+ * o_batch_stride_rows : >= U*S_l.
+ * send : [U, B, S_l, h_l, D], device.
+ */
+ctx_status ctx_pack_out(const void *o, void *send, long long o_batch_stride_rows,
+                        int B, int S_l, int h_l, int D, int U, ctx_dtype dtype,
+                        void *stream);
+
+/*
+ * ctx_unpack_out — reverse Ulysses exchange, receive side: source rank r's
+ * heads go back to heads [r*h_l, (r+1)*h_l) of the sequence-sharded output.
+ *
+ *   y[b][s][r*h_l + h][d] = recv[r][b][s][h][d]
+ *
+ * recv : [U, B, S_l, h_l, D], device.   y : [B, S_l, U*h_l, D], device.
+ */
+ctx_status ctx_unpack_out(const void *recv, void *y, int B, int S_l, int h_l,
+                          int D, int U, ctx_dtype dtype, void *stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *ctx_status_string(ctx_status status);
+
+/*
+ * ctx_device_status — synchronises `stream`, then reads and clears the
+ * device status word of the current device. Returns CTX_OK, CTX_ERR_TIMEOUT
+ * if a bounded device wait ran out since the last call, or CTX_ERR_CUDA if
+ * the synchronisation failed.
+ */
+ctx_status ctx_device_status(void *stream);
+
+/* cudaError_t of the last CTX_ERR_CUDA returned on the calling thread (0 if none). */
+int ctx_last_cuda_error(void);
+
+/*
+ * ctx_selftest_wait_timeout — launches one block whose mbarrier wait can
+ * never complete, bounded at `limit_ns` nanoseconds (1e3 .. 5e9), then
+ * returns ctx_device_status(stream): CTX_ERR_TIMEOUT when the bounded wait
+ * works as designed, with the context still usable. It tests the failure
+ * path of the bounded waits without hanging or faulting a GPU.
+ */
+ctx_status ctx_selftest_wait_timeout(long long limit_ns, void *stream);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int ctx_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CTX_H_ */

@@ -1,0 +1,126 @@
+"""The C-ABI library builds, loads and exports every symbol include/ctx.h
+declares; host-side validation fails closed before touching the GPU.
+
+These run without a GPU: every call below is rejected by the host checks,
+which come before any CUDA runtime call.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ctx.h")
+
+OK, INVALID, UNSUPPORTED, MISALIGNED, ALIASING = 0, 1, 2, 3, 4
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ctx_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import diffusion_transformer_context_gb300 as ctx
+    ctx.build()
+    return ctx.lib()
+
+
+def test_header_declares_the_hot_path():
+    syms = declared_symbols()
+    for s in ("ctx_pack_qkv", "ctx_unpack_qkv", "ctx_attn_lq_gkv", "ctx_pack_out", "ctx_unpack_out",
+              "ctx_sim_all_to_all", "ctx_status_string", "ctx_device_status"):
+        assert s in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    import diffusion_transformer_context_gb300 as ctx
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert name in ctx.SIGNATURES, f"binding lacks {name}"
+    assert set(ctx.SIGNATURES) == set(declared_symbols())
+
+
+def test_binding_names_match_the_c_entry_points():
+    import diffusion_transformer_context_gb300 as ctx
+    for name in declared_symbols():
+        assert callable(getattr(ctx, name)), name
+
+
+def test_status_strings_and_version(lib):
+    import diffusion_transformer_context_gb300 as ctx
+    for code, name in ctx.STATUS_NAMES.items():
+        assert ctx.ctx_status_string(code) == name
+    assert ctx.ctx_status_string(99) == "CTX_ERR_UNKNOWN"
+    assert ctx.ctx_version() >= 100
+
+
+# fake, never dereferenced addresses: validation rejects before any CUDA call
+A0 = 0x10000000
+MB = 1 << 20
+
+
+def test_pack_validation(lib):
+    f = lib.ctx_pack_qkv
+    assert f(None, A0, A0, A0, 1, 4, 4, 8, 2, 0, None) == INVALID
+    assert f(A0, A0 + MB, A0 + 2 * MB, A0 + 3 * MB, 1, 4, 6, 8, 4, 0, None) == INVALID   # H % U
+    assert f(A0, A0 + MB, A0 + 2 * MB, A0 + 3 * MB, 0, 4, 4, 8, 2, 0, None) == INVALID   # B = 0
+    assert f(A0, A0 + MB, A0 + 2 * MB, A0 + 3 * MB, 1, 4, 4, 8, 2, 7, None) == INVALID   # dtype
+    assert f(A0 + 8, A0 + MB, A0 + 2 * MB, A0 + 3 * MB, 1, 4, 4, 8, 2, 0, None) == MISALIGNED
+    assert f(A0, A0 + MB, A0 + 2 * MB, A0 + 3 * MB, 1, 4, 4, 12, 2, 0, None) == MISALIGNED  # D % 8
+    assert f(A0, A0 + MB, A0 + 2 * MB, A0 + 64, 1, 4, 4, 8, 2, 0, None) == ALIASING
+
+
+def test_unpack_validation(lib):
+    f = lib.ctx_unpack_qkv
+    assert f(A0, A0 + MB, A0 + 2 * MB, A0 + 3 * MB, 4, 8, 1, 4, 2, 8, 2, 0, None) == INVALID  # q stride < U*S_l
+    assert f(A0, A0 + MB, A0 + 2 * MB, A0 + 3 * MB, 8, 4, 1, 4, 2, 8, 2, 0, None) == INVALID  # kv stride
+    # k overlaps v
+    assert f(A0, A0 + MB, A0 + 2 * MB, A0 + 2 * MB + 16, 8, 8, 1, 4, 2, 8, 2, 0, None) == ALIASING
+    # recv overlaps q
+    assert f(A0, A0 + 32, A0 + 2 * MB, A0 + 3 * MB, 8, 8, 1, 4, 2, 8, 2, 0, None) == ALIASING
+
+
+def test_attention_validation(lib):
+    f = lib.ctx_attn_lq_gkv
+    q, k, v, o, l = A0, A0 + MB, A0 + 2 * MB, A0 + 3 * MB, A0 + 4 * MB
+    nan = float("nan")
+    assert f(q, k, v, None, nan, o, l, 1, 16, 16, 2, 96, 0, None) == UNSUPPORTED
+    assert f(q, k, v, None, -1.0, o, l, 1, 16, 16, 2, 128, 0, None) == INVALID
+    assert f(q, k, v, None, float("inf"), o, l, 1, 16, 16, 2, 128, 0, None) == INVALID
+    assert f(q, k, v, None, nan, o, l, 1, 0, 16, 2, 128, 0, None) == INVALID
+    assert f(q, k, v, None, nan, o, l, 1, 16, -1, 2, 128, 0, None) == INVALID
+    assert f(q, k, v, None, nan, None, l, 1, 16, 16, 2, 128, 0, None) == INVALID
+    assert f(q + 4, k, v, None, nan, o, l, 1, 16, 16, 2, 128, 0, None) == MISALIGNED
+    assert f(q, k, v, None, nan, o, l + 2, 1, 16, 16, 2, 128, 0, None) == MISALIGNED
+    assert f(q, k, v, None, nan, q + 64, l, 1, 16, 16, 2, 128, 0, None) == ALIASING
+    assert f(q, k, v, None, nan, o, o + 16, 1, 16, 16, 2, 128, 0, None) == ALIASING
+
+
+def test_reverse_and_a2a_validation(lib):
+    assert lib.ctx_pack_out(A0, A0 + MB, 3, 1, 2, 2, 8, 2, 0, None) == INVALID  # stride < U*S_l
+    assert lib.ctx_pack_out(A0, A0 + 16, 4, 1, 2, 2, 8, 2, 0, None) == ALIASING
+    assert lib.ctx_unpack_out(A0, A0 + MB, 1, 2, 2, 12, 2, 0, None) == MISALIGNED
+    assert lib.ctx_unpack_out(A0, None, 1, 2, 2, 8, 2, 0, None) == INVALID
+    assert lib.ctx_sim_all_to_all(A0, A0 + MB, 1, 2, 24, None) == MISALIGNED
+    assert lib.ctx_sim_all_to_all(A0, A0 + 16, 1, 2, 32, None) == ALIASING
+    assert lib.ctx_sim_all_to_all(A0, A0 + MB, 0, 2, 32, None) == INVALID
+
+
+def test_selftest_limit_validation(lib):
+    assert lib.ctx_selftest_wait_timeout(10, None) == INVALID
+    assert lib.ctx_selftest_wait_timeout(10 ** 10, None) == INVALID
+
+
+def test_product_path_has_no_oracle_or_fallback():
+    """The CUDA package never imports the oracle and has no CPU path."""
+    pkg = os.path.join(ROOT, "diffusion_transformer_context_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, fn)).read()
+                assert "import oracle" not in src and "from oracle" not in src, fn
+                assert "ctx_oracle" not in src, fn
