@@ -1,0 +1,431 @@
+"""Benchmark of the simulated context-parallel attention layer on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input,
+all U x A virtual ranks on this GPU: pack -> simulated all-to-all -> unpack
+(AllGather placement) -> local-Q / global-KV attention -> reverse exchange.
+Default workload: the Wan-like 480p AllGather-KV CP8 layer (local-Q
+[1,4095,12,128] per rank against the gathered K/V [1,32760,12,128]).
+
+`value` is the attention FLOPs of the step divided by the device time of the
+whole step (inputs resident in HBM); `roofline` is the attention kernel alone
+(CUDA events on its stream); `relayout` reports the pack/unpack GB/s;
+`e2e` repeats the step through the same public API with the inputs copied
+from pinned host memory and the output read back inside the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle on a bounded sample
+
+Under torchrun (N > 1) every GPU runs its own replica of the layer (weak
+scaling, no collective on the data path); the timed region is bracketed by a
+barrier and the slowest rank's time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "LQ/GKV attn TFLOP/s & % GB300 bf16 peak; QKV pack/unpack GB/s & % HBM"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_sha1() -> str:
+    h = hashlib.sha1()
+    csrc = os.path.join(ROOT, "diffusion_transformer_context_gb300", "csrc")
+    for fn in ("attention.cu", "ptx.cuh"):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per attention launch from the committed ncu summary, or None
+    if the kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "attn_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    entry = d.get(workload)
+    if not entry or entry.get("source_sha1") != kernel_source_sha1():
+        return None
+    return entry.get("bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), float(parts[2]), parts[3], parts[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        busy = [r for r in rows if r[2] > 0.25 * max(x[2] for x in rows)] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in busy for i, v in enumerate(r[4]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in busy), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(busy)}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import workloads
+    import diffusion_transformer_context_gb300 as ctx
+    from diffusion_transformer_context_gb300.simulate import SimLayer
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = workloads.WORKLOADS[args.workload]
+    inp = workloads.make_inputs(wl)
+    sim = SimLayer(wl, device=dev)
+    sim.load(inp)
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    # per-kernel-group events inside each step
+    def timed_step(ev):
+        wl_ = sim.wl
+        U, A, B, S, D = wl_.U, wl_.A, wl_.B, wl_.S, wl_.D
+        S_l, h_l, Sk = sim.S_l, sim.h_l, sim.Sk
+        ev[0].record(stream)
+        for g in range(sim.R):
+            a, u = divmod(g, U)
+            x = sim.x[g]
+            ctx.ctx_pack_qkv(x[0], x[1], x[2], sim.send[a, u], U, stream=stream)
+        ev[1].record(stream)
+        if U > 1:
+            ctx.ctx_sim_all_to_all(sim.send, sim.recv, A, U, stream=stream)
+        ev[2].record(stream)
+        for g in range(sim.R):
+            a, u = divmod(g, U)
+            r0 = a * U * S_l
+            ctx.ctx_unpack_qkv(sim.recv[a, u].view(U, 3, B, S_l, h_l, D), sim.qg[u, :, r0:], sim.kg[u, :, r0:],
+                               sim.vg[u, :, r0:], U, q_batch_stride_rows=S, kv_batch_stride_rows=Sk, stream=stream)
+        ev[3].record(stream)
+        if sim.attention:
+            ctx.ctx_attn_lq_gkv(sim.qg.view(U * B, S, h_l, D), sim.kg.view(U * B, Sk, h_l, D),
+                                sim.vg.view(U * B, Sk, h_l, D), sim.out.view(U * B, S, h_l, D), sim.lse,
+                                key_mask=sim.mask, stream=stream)
+        ev[4].record(stream)
+        if sim.attention and U > 1:
+            for g in range(sim.R):
+                a, u = divmod(g, U)
+                ctx.ctx_pack_out(sim.out[u, :, a * U * S_l:], sim.osend[a, u].view(U, B, S_l, h_l, D), U,
+                                 o_batch_stride_rows=S, stream=stream)
+            ctx.ctx_sim_all_to_all(sim.osend, sim.orecv, A, U, stream=stream)
+            for g in range(sim.R):
+                a, u = divmod(g, U)
+                ctx.ctx_unpack_out(sim.orecv[a, u].view(U, B, S_l, h_l, D), sim.y[g], U, stream=stream)
+        ev[5].record(stream)
+
+    for _ in range(args.warmup):
+        sim.step(stream=stream)
+    st = ctx.ctx_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {ctx.ctx_status_string(st)}")
+
+    sampler = ClockSampler(local_rank) if (rank == 0 and not args.no_clocks) else None
+    if sampler:
+        sampler.start()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    t0.record(stream)
+    for i in range(args.steps):
+        timed_step(evs[i])
+    t1.record(stream)
+    barrier()
+    clocks = sampler.stop() if sampler else None
+    st = ctx.ctx_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status after timed steps: {ctx.ctx_status_string(st)}")
+    total_ms = t0.elapsed_time(t1)
+    parts = {k: [] for k in ("pack", "a2a", "unpack", "attn", "reverse")}
+    for ev in evs:
+        for name, (i0, i1) in zip(parts, ((0, 1), (1, 2), (2, 3), (3, 4), (4, 5))):
+            parts[name].append(ev[i0].elapsed_time(ev[i1]))
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # ---------------------------------------------------------- e2e (host buffers)
+    e2e = None
+    if not args.no_e2e:
+        host_x = torch.empty(sim.x.shape, dtype=sim.x.dtype).pin_memory()
+        host_x.copy_(sim.x.cpu())
+        result = sim.y if (sim.attention and wl.U > 1) else sim.out
+        host_y = torch.empty(result.shape, dtype=result.dtype).pin_memory()
+        for _ in range(max(1, args.warmup)):
+            sim.x.copy_(host_x, non_blocking=True)
+            sim.step(stream=stream)
+            host_y.copy_(result, non_blocking=True)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        e0.record(stream)
+        for _ in range(args.steps):
+            sim.x.copy_(host_x, non_blocking=True)
+            sim.step(stream=stream)
+            host_y.copy_(result, non_blocking=True)
+        e1.record(stream)
+        barrier()
+        e2e_ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        flops = sim.attn_flops(inp.text_len)
+        e2e = {"value": round(world * flops * args.steps / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": host_x.numel() * host_x.element_size(),
+               "d2h_bytes_per_step": host_y.numel() * host_y.element_size(),
+               "ms_per_step": round(e2e_ms / args.steps, 4)}
+    return sim, inp, total_ms, parts, clocks, e2e
+
+
+def cpu_baseline_sample(wl_name: str, seconds: float, seed: int = 1234):
+    """Times the oracle as it stands on a bounded sample of the workload's
+    attention rows (and the layout steps of one rank); returns a dict."""
+    import numpy as np
+    import oracle
+    import workloads
+
+    oracle.build()
+    wl = workloads.WORKLOADS[wl_name]
+    inp = workloads.make_inputs(wl)
+    U, A = wl.U, wl.A
+    u16 = workloads.as_u16
+    # one rank's layout steps (pack + unpack), timed
+    g = 0
+    t = time.perf_counter()
+    st = oracle.pack_qkv(u16(inp.shard(inp.q, g)), u16(inp.shard(inp.k, g)), u16(inp.shard(inp.v, g)), U)
+    oracle.unpack_qkv(st, U)
+    relayout_s = time.perf_counter() - t
+    relayout_bytes = 2 * 2 * st.nbytes
+    # attention: head group 0, gathered K/V, query rows of every rank
+    h_l = wl.h_l
+    q = u16(inp.q[:, :, :h_l])
+    k = u16(inp.k[:, :, :h_l])
+    v = u16(inp.v[:, :, :h_l])
+    mask = None
+    if wl.joint:
+        k = np.concatenate([k, u16(inp.jk[:, :, :h_l])], axis=1)
+        v = np.concatenate([v, u16(inp.jv[:, :, :h_l])], axis=1)
+        mask = inp.key_mask()
+    Sk = k.shape[1]
+    rng = np.random.default_rng(seed)
+
+    def rows(n):
+        return np.stack([rng.integers(0, wl.B, n), rng.integers(0, h_l, n), rng.integers(0, wl.S, n)], axis=1)
+
+    def flops_of(bhi):
+        if mask is None:
+            return 4.0 * Sk * wl.D * len(bhi)
+        return float(sum(4.0 * int(mask[b].sum()) * wl.D for b in bhi[:, 0]))
+
+    t = time.perf_counter()
+    probe = rows(max(16, 4 * oracle.num_threads()))
+    oracle.attention_rows(q, k, v, probe, mask)
+    per_row = max(1e-6, (time.perf_counter() - t) / len(probe))
+    n = max(8, int(seconds / per_row))
+    bhi = rows(n)
+    t = time.perf_counter()
+    oracle.attention_rows(q, k, v, bhi, mask)
+    dt = time.perf_counter() - t
+    return {"value": round(flops_of(bhi) / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{n} random query rows of {wl_name} (fp64 oracle, all keys each), {dt:.1f} s; "
+                      f"layout of one rank: {relayout_bytes / relayout_s / 1e9:.2f} GB/s",
+            "relayout_gbs": round(relayout_bytes / relayout_s / 1e9, 3)}
+
+
+def run_reference(args, rank):
+    """--impl reference: the oracle, on the host cores, a bounded sample per step."""
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    import workloads
+
+    oracle.build()
+    wl = workloads.WORKLOADS[args.workload]
+    inp = workloads.make_inputs(wl)
+    h_l = wl.h_l
+    u16 = workloads.as_u16
+    q, k, v = u16(inp.q[:, :, :h_l]), u16(inp.k[:, :, :h_l]), u16(inp.v[:, :, :h_l])
+    mask = None
+    if wl.joint:
+        k = np.concatenate([k, u16(inp.jk[:, :, :h_l])], axis=1)
+        v = np.concatenate([v, u16(inp.jv[:, :, :h_l])], axis=1)
+        mask = inp.key_mask()
+    Sk = k.shape[1]
+    rng = np.random.default_rng(1234)
+    n_rows = args.ref_rows
+
+    def one_step():
+        bhi = np.stack([rng.integers(0, wl.B, n_rows), rng.integers(0, h_l, n_rows),
+                        rng.integers(0, wl.S, n_rows)], axis=1)
+        t = time.perf_counter()
+        oracle.attention_rows(q, k, v, bhi, mask)
+        dt = time.perf_counter() - t
+        fl = float(sum(4.0 * (Sk if mask is None else int(mask[b].sum())) * wl.D for b in bhi[:, 0]))
+        return fl, dt
+
+    for _ in range(args.warmup):
+        one_step()
+    fl_tot = dt_tot = 0.0
+    for _ in range(args.steps):
+        fl, dt = one_step()
+        fl_tot += fl
+        dt_tot += dt
+    value = fl_tot / dt_tot / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * dt_tot / args.steps, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "sample_rows_per_step": n_rows},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                             "kind": "oracle",
+                             "sample": f"{n_rows} random query rows of {args.workload} per step, all keys"},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="wan480")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-rows", type=int, default=64)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours" and not os.environ.get("CTX_BENCH_ALLOW_SHORT_WARMUP"):
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    sim, inp, total_ms, parts, clocks, e2e = run_gpu(args, rank, world, local_rank)
+    peaks, peak_kind = load_peaks()
+    K = args.steps
+    attn_flops = sim.attn_flops(inp.text_len)
+    ms_step = total_ms / K
+    value = world * attn_flops / (ms_step * 1e-3) / 1e12
+
+    def avg(x):
+        return sum(x) / len(x)
+
+    attn_ms = avg(parts["attn"])
+    tflops = attn_flops / (attn_ms * 1e-3) / 1e12 if attn_ms > 0 else 0.0
+    peak_tf = peaks["bf16_tflops"]
+    relayout_bytes = sim.pack_bytes() + sim.unpack_bytes()
+    relayout_ms = avg(parts["pack"]) + avg(parts["unpack"])
+    relayout_gbs = relayout_bytes / (relayout_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(args.workload)
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "B": sim.wl.B, "S": sim.wl.S, "H": sim.wl.H, "D": sim.wl.D,
+                   "U": sim.wl.U, "A": sim.wl.A, "joint": sim.wl.joint, "virtual_ranks": sim.R,
+                   "attn_call": f"B'={sim.wl.U * sim.wl.B} Sq={sim.wl.S} Sk={sim.Sk} H={sim.h_l} D={sim.wl.D}",
+                   "l2": "inputs_larger_than_l2", "parallelism": f"replicas{world}"},
+        "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel", "achieved": round(tflops, 2),
+                     "peak": peak_tf, "unit": "TFLOP/s", "frac": round(tflops / peak_tf, 4),
+                     "peak_source": f"{peak_kind} bf16_tflops (burst)",
+                     "algorithmic_flops_per_launch": attn_flops, "launch_ms": round(attn_ms, 4),
+                     "traffic": traffic},
+        "relayout": {"bound": "hbm", "achieved": round(relayout_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(relayout_gbs / peaks["hbm_gbs"], 4),
+                     "pack_ms": round(avg(parts["pack"]), 4), "unpack_ms": round(avg(parts["unpack"]), 4),
+                     "a2a_ms": round(avg(parts["a2a"]), 4), "reverse_ms": round(avg(parts["reverse"]), 4),
+                     "algorithmic_bytes_pack_plus_unpack": relayout_bytes},
+        "gpu_launches": sim.launches_per_step() * K,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_sample(args.workload, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,118 @@
+"""The whole simulated layer on the GPU (all U x A ranks: pack -> all-to-all
+-> unpack into the gathered buffers -> attention -> reverse exchange)
+against the oracle's composed pipeline (vllm-omni PR #7641 order).
+
+Layout results are compared bit for bit; attention within the tolerance of
+test_gpu_attention; the reverse exchange bit for bit on the GPU's own
+attention output.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from gpu_util import u16
+
+pytestmark = pytest.mark.gpu
+
+O_MAX, O_MEAN, LSE_TOL = 2e-2, 2e-3, 1e-3
+
+
+@pytest.fixture(scope="module")
+def ctx():
+    import diffusion_transformer_context_gb300 as m
+    m.build()
+    return m
+
+
+def _oracle_side(orc, inp):
+    wl = inp.wl
+    R = wl.ranks
+    sh = [[u16(inp.shard(t, g)) for t in (inp.q, inp.k, inp.v)] for g in range(R)]
+    jk = u16(inp.jk) if inp.jk is not None else None
+    jv = u16(inp.jv) if inp.jv is not None else None
+    return orc.ulysses_agkv_forward([s[0] for s in sh], [s[1] for s in sh], [s[2] for s in sh],
+                                    wl.U, wl.A, jk, jv)
+
+
+def _check_layer(ctx, orc, wl, n_rows=None):
+    from diffusion_transformer_context_gb300.simulate import SimLayer
+    inp = workloads.make_inputs(wl)
+    sim = SimLayer(wl)
+    sim.load(inp)
+    sim.step()
+    st = ctx.ctx_device_status()
+    assert st == 0, ctx.ctx_status_string(st)
+    res = _oracle_side(orc, inp)
+    U, A = wl.U, wl.A
+    # layout steps: bit-exact
+    for u in range(U):
+        assert np.array_equal(u16(sim.kg[u]), res["k"][u]), f"K group {u}"
+        assert np.array_equal(u16(sim.vg[u]), res["v"][u]), f"V group {u}"
+    for g in range(wl.ranks):
+        assert np.array_equal(u16(sim.rank_q(g)), res["q"][g]), f"Q rank {g}"
+    if not sim.attention:
+        return
+    mask = inp.key_mask()
+    # attention of every rank (rank g: its local-Q against its head group's K/V)
+    out = sim.out.float().cpu().numpy()
+    lse = sim.lse.cpu().numpy().reshape(U, wl.B, sim.h_l, wl.S)
+    rows_per_rank = wl.S // A
+    errs = []
+    for g in range(wl.ranks):
+        a, u = divmod(g, U)
+        qg, kg, vg = res["q"][g], res["k"][u], res["v"][u]
+        if n_rows is None:
+            eO, eL = orc.attention(qg, kg, vg, mask)
+            gO = out[u][:, a * rows_per_rank:(a + 1) * rows_per_rank]
+            gL = lse[u][:, :, a * rows_per_rank:(a + 1) * rows_per_rank]
+            errs.append(np.abs(gO - eO))
+            assert np.abs(gL - eL).max() <= LSE_TOL
+        else:
+            rows_i = workloads.sample_rows(rows_per_rank, n_rows)
+            rng = np.random.default_rng(g)
+            bhi = np.stack([rng.integers(0, wl.B, rows_i.size), rng.integers(0, sim.h_l, rows_i.size),
+                            rows_i], axis=1)
+            eo, el = orc.attention_rows(qg, kg, vg, bhi, mask)
+            go = np.stack([out[u][b, a * rows_per_rank + i, h] for b, h, i in bhi])
+            gl = np.array([lse[u][b, h, a * rows_per_rank + i] for b, h, i in bhi])
+            errs.append(np.abs(go - eo))
+            assert np.abs(gl - el).max() <= LSE_TOL
+    e = np.concatenate([x.ravel() for x in errs])
+    assert e.max() <= O_MAX and e.mean() <= O_MEAN, (e.max(), e.mean())
+    # reverse exchange of the GPU's own output: bit-exact
+    o_ranks = [u16(sim.out[u][:, a * rows_per_rank:(a + 1) * rows_per_rank])
+               for a in range(A) for u in range(U)]
+    back = orc.ulysses_reverse(o_ranks, U, A)
+    for g in range(wl.ranks):
+        assert np.array_equal(u16(sim.rank_output(g)), back[g]), f"reverse rank {g}"
+
+
+def test_tiny(ctx, orc):
+    _check_layer(ctx, orc, workloads.WORKLOADS["tiny"])
+
+
+def test_pack_workload(ctx, orc):
+    _check_layer(ctx, orc, workloads.WORKLOADS["pack"])
+
+
+@pytest.mark.parametrize("wl", [
+    workloads.custom("u2a2_joint_b2", B=2, S=512, H=8, D=128, U=2, A=2, joint=64, text_len_range=(1, 64)),
+    workloads.custom("u4a2_d64", B=1, S=1024, H=8, D=64, U=4, A=2),
+    workloads.custom("u1a4_ragged", B=1, S=1000, H=3, D=128, U=1, A=4),
+    workloads.custom("u3a1", B=2, S=378, H=6, D=128, U=3, A=1),
+], ids=lambda w: w.name)
+def test_composed_small(ctx, orc, wl):
+    _check_layer(ctx, orc, wl)
+
+
+def test_qwen_layer(ctx, orc):
+    _check_layer(ctx, orc, workloads.WORKLOADS["qwen"], n_rows=128)
+
+
+def test_wan480_layer(ctx, orc):
+    _check_layer(ctx, orc, workloads.WORKLOADS["wan480"], n_rows=48)
+
+
+def test_wan14b_layer(ctx, orc):
+    _check_layer(ctx, orc, workloads.WORKLOADS["wan14b"], n_rows=24)
