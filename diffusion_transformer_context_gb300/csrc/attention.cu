@@ -351,10 +351,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!((vb[i >> 5] >> (i & 31)) & 1u))
                         s[i] = -INFINITY;
             }
-            float mx = s[0];
+            // row max: eight independent chains of 3-input max, then a tree
+            float acc[8];
 #pragma unroll
-            for (int i = 1; i < kBN; ++i)
-                mx = fmaxf(mx, s[i]);
+            for (int i = 0; i < 8; ++i)
+                acc[i] = s[i];
+#pragma unroll
+            for (int i = 8; i < kBN; i += 16) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    acc[q] = ptx::max3(acc[q], s[i + q], s[i + 8 + q]);
+            }
+            const float mx = ptx::max3(ptx::max3(acc[0], acc[1], acc[2]), ptx::max3(acc[3], acc[4], acc[5]),
+                                       fmaxf(acc[6], acc[7]));
             const float m_new = fmaxf(m_run, mx * c);
             if (j == 0) {
                 m_run = m_new;
@@ -382,21 +391,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
-            float lsum = 0.f;
+            const uint64_t c2 = ptx::f2_pack(c, c), nm2 = ptx::f2_pack(neg_m, neg_m);
+            uint64_t sum2[4] = {0, 0, 0, 0};  // four independent packed partial sums
             // P overwrites the first 64 columns of S, 32 columns (64 keys) at a time
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 uint32_t pk[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const float p0 = ptx::ex2_approx(fmaf(s[64 * half + 2 * i], c, neg_m));
-                    const float p1 = ptx::ex2_approx(fmaf(s[64 * half + 2 * i + 1], c, neg_m));
-                    lsum += p0 + p1;
+                    const int col = 64 * half + 2 * i;
+                    const uint64_t arg = ptx::f2_fma(ptx::f2_pack(s[col], s[col + 1]), c2, nm2);
+                    const float p0 = ptx::ex2_approx(ptx::f2_lo(arg));
+                    const float p1 = ptx::ex2_approx(ptx::f2_hi(arg));
+                    sum2[i & 3] = ptx::f2_add(sum2[i & 3], ptx::f2_pack(p0, p1));
                     pk[i] = ptx::pack2<BF16>(p0, p1);
                 }
                 ptx::tmem_st32(tS + 32 * half, pk);
             }
-            l_run += lsum;
+            const uint64_t t01 = ptx::f2_add(sum2[0], sum2[1]), t23 = ptx::f2_add(sum2[2], sum2[3]);
+            const uint64_t tot = ptx::f2_add(t01, t23);
+            l_run += ptx::f2_lo(tot) + ptx::f2_hi(tot);
             ptx::tmem_st_wait();
             ptx::tc_fence_before();
             ptx::mbar_arrive(p_full + t);

@@ -257,6 +257,44 @@ __device__ __forceinline__ float ex2_approx(float x)
     return y;
 }
 
+__device__ __forceinline__ float max3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Packed pair of fp32 (x in the low half).
+__device__ __forceinline__ uint64_t f2_pack(float x, float y)
+{
+    return static_cast<uint64_t>(__float_as_uint(x)) | (static_cast<uint64_t>(__float_as_uint(y)) << 32);
+}
+
+__device__ __forceinline__ float f2_lo(uint64_t v)
+{
+    return __uint_as_float(static_cast<uint32_t>(v));
+}
+
+__device__ __forceinline__ float f2_hi(uint64_t v)
+{
+    return __uint_as_float(static_cast<uint32_t>(v >> 32));
+}
+
+// a*b + c on both halves (one packed FFMA2).
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // Two floats -> packed pair of 16-bit floats, `lo` in the low half.
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi)
