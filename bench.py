@@ -132,7 +132,7 @@ def run_gpu(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     wl = workloads.WORKLOADS[args.workload]
     inp = workloads.make_inputs(wl)
-    sim = SimLayer(wl, device=dev)
+    sim = SimLayer(wl, device=dev, balanced=not args.unbalanced)
     sim.load(inp)
     stream = torch.cuda.current_stream(dev)
 
@@ -164,7 +164,7 @@ def run_gpu(args, rank, world, local_rank):
         if sim.attention:
             ctx.ctx_attn_lq_gkv(sim.qg.view(U * B, S, h_l, D), sim.kg.view(U * B, Sk, h_l, D),
                                 sim.vg.view(U * B, Sk, h_l, D), sim.out.view(U * B, S, h_l, D), sim.lse,
-                                key_mask=sim.mask, stream=stream)
+                                key_mask=sim.mask, workspace=sim.ws, stream=stream)
         ev[4].record(stream)
         if sim.attention and U > 1:
             for g in range(sim.R):
@@ -360,6 +360,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--unbalanced", action="store_true", help="attention without workspace: one CTA per unit")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=64)
     args = ap.parse_args()
@@ -404,7 +405,8 @@ def main():
         "config": {"workload": args.workload, "B": sim.wl.B, "S": sim.wl.S, "H": sim.wl.H, "D": sim.wl.D,
                    "U": sim.wl.U, "A": sim.wl.A, "joint": sim.wl.joint, "virtual_ranks": sim.R,
                    "attn_call": f"B'={sim.wl.U * sim.wl.B} Sq={sim.wl.S} Sk={sim.Sk} H={sim.h_l} D={sim.wl.D}",
-                   "l2": "inputs_larger_than_l2", "parallelism": f"replicas{world}"},
+                   "l2": "inputs_larger_than_l2", "parallelism": f"replicas{world}",
+                   "attn_schedule": "one CTA per unit" if sim.ws is None else "persistent, key-split tail"},
         "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel", "achieved": round(tflops, 2),
                      "peak": peak_tf, "unit": "TFLOP/s", "frac": round(tflops / peak_tf, 4),
                      "peak_source": f"{peak_kind} bf16_tflops (burst)",

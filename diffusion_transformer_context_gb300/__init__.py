@@ -29,7 +29,8 @@ SIGNATURES = {
     "ctx_pack_qkv": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "ctx_sim_all_to_all": (_I, [_P, _P, _I, _I, _LL, _P]),
     "ctx_unpack_qkv": (_I, [_P, _P, _P, _P, _LL, _LL, _I, _I, _I, _I, _I, _I, _P]),
-    "ctx_attn_lq_gkv": (_I, [_P, _P, _P, _P, _F, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "ctx_attn_lq_gkv": (_I, [_P, _P, _P, _P, _F, _P, _P, _P, _LL, _I, _I, _I, _I, _I, _I, _P]),
+    "ctx_attn_lq_gkv_workspace_size": (_LL, [_I, _I, _I, _I, _I]),
     "ctx_pack_out": (_I, [_P, _P, _LL, _I, _I, _I, _I, _I, _I, _P]),
     "ctx_unpack_out": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "ctx_status_string": (ctypes.c_char_p, [_I]),
@@ -121,14 +122,32 @@ def ctx_unpack_qkv(recv, q, k, v, U: int, q_batch_stride_rows: int | None = None
                                                   B, S_l, h_l, D, U, _dtype(recv), _stream(stream)))
 
 
-def ctx_attn_lq_gkv(q, k, v, out, lse=None, key_mask=None, scale: float | None = None, stream=None):
-    """q [B,Sq,H,D], k/v [B,Sk,H,D] -> out [B,Sq,H,D], lse [B,H,Sq] fp32 (optional)."""
+def ctx_attn_lq_gkv(q, k, v, out, lse=None, key_mask=None, scale: float | None = None, workspace=None,
+                    stream=None):
+    """q [B,Sq,H,D], k/v [B,Sk,H,D] -> out [B,Sq,H,D], lse [B,H,Sq] fp32 (optional).
+    workspace: None, or a zero-filled device buffer of at least
+    ctx_attn_lq_gkv_workspace_size(...) bytes for the balanced schedule."""
     B, Sq, H, D = q.shape
     Sk = k.shape[1]
     s = float("nan") if scale is None else float(scale)
+    wb = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check("ctx_attn_lq_gkv", lib().ctx_attn_lq_gkv(_ptr(q), _ptr(k), _ptr(v), _ptr(key_mask), s, _ptr(out),
-                                                    _ptr(lse), B, Sq, Sk, H, D, _dtype(q), _stream(stream)))
+                                                    _ptr(lse), _ptr(workspace), wb, B, Sq, Sk, H, D, _dtype(q),
+                                                    _stream(stream)))
     return out
+
+
+def ctx_attn_lq_gkv_workspace_size(B: int, Sq: int, Sk: int, H: int, D: int) -> int:
+    n = lib().ctx_attn_lq_gkv_workspace_size(B, Sq, Sk, H, D)
+    if n < 0:
+        raise CtxError("ctx_attn_lq_gkv_workspace_size", 1)
+    return n
+
+
+def attn_workspace(B: int, Sq: int, Sk: int, H: int, D: int, device="cuda"):
+    """A zero-filled workspace tensor of the size the balanced schedule needs."""
+    n = ctx_attn_lq_gkv_workspace_size(B, Sq, Sk, H, D)
+    return torch.zeros(max(n, 256), dtype=torch.uint8, device=device)
 
 
 def ctx_pack_out(o, send, U: int, o_batch_stride_rows: int | None = None, stream=None):

@@ -332,7 +332,8 @@ ctx_status ctx_unpack_out(const void *recv, void *y, int B, int S_l, int h_l, in
 }
 
 ctx_status ctx_attn_lq_gkv(const void *q, const void *k, const void *v, const unsigned char *key_mask, float scale,
-                           void *out, float *lse, int B, int Sq, int Sk, int H, int D, ctx_dtype dtype, void *stream)
+                           void *out, float *lse, void *workspace, long long workspace_bytes, int B, int Sq, int Sk,
+                           int H, int D, ctx_dtype dtype, void *stream)
 {
     if (!q || !k || !v || !out || !valid_dtype(dtype))
         return CTX_ERR_INVALID_ARG;
@@ -345,26 +346,36 @@ ctx_status ctx_attn_lq_gkv(const void *q, const void *k, const void *v, const un
         scale = 1.0f / std::sqrt(static_cast<float>(D));
     if (!std::isfinite(scale) || !(scale > 0.f))
         return CTX_ERR_INVALID_ARG;
+    if (workspace && workspace_bytes <= 0)
+        return CTX_ERR_INVALID_ARG;
     if (D % 8 != 0 || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
-        (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+        (reinterpret_cast<uintptr_t>(lse) & 3u) != 0 || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return CTX_ERR_MISALIGNED;
     if (D != 64 && D != 128)
         return CTX_ERR_UNSUPPORTED;
     const Extent eo = extent(out, nq * 2);
     const Extent eq = extent(q, nq * 2), ek = extent(k, nk * 2), ev = extent(v, nk * 2);
-    if (overlap(eo, eq) || overlap(eo, ek) || overlap(eo, ev))
+    const Extent em = key_mask ? extent(key_mask, static_cast<long long>(B) * Sk) : Extent{0, 0};
+    const Extent el = lse ? extent(lse, static_cast<long long>(B) * H * Sq * 4) : Extent{0, 0};
+    const Extent ew = workspace ? extent(workspace, workspace_bytes) : Extent{0, 0};
+    if (overlap(eo, eq) || overlap(eo, ek) || overlap(eo, ev) || overlap(eo, em))
         return CTX_ERR_ALIASING;
-    if (key_mask && overlap(eo, extent(key_mask, static_cast<long long>(B) * Sk)))
+    if (overlap(el, eo) || overlap(el, eq) || overlap(el, ek) || overlap(el, ev) || overlap(el, em))
         return CTX_ERR_ALIASING;
-    if (lse) {
-        const Extent el = extent(lse, static_cast<long long>(B) * H * Sq * 4);
-        if (overlap(el, eo) || overlap(el, eq) || overlap(el, ek) || overlap(el, ev) ||
-            (key_mask && overlap(el, extent(key_mask, static_cast<long long>(B) * Sk))))
-            return CTX_ERR_ALIASING;
-    }
-    ctx_status s = check_device_ptrs({q, k, v, out, lse, key_mask});
+    if (overlap(ew, eo) || overlap(ew, eq) || overlap(ew, ek) || overlap(ew, ev) || overlap(ew, em) ||
+        overlap(ew, el))
+        return CTX_ERR_ALIASING;
+    ctx_status s = check_device_ptrs({q, k, v, out, lse, key_mask, workspace});
     if (s != CTX_OK)
         return s;
+    if (workspace) {
+        cudaError_t e = cudaSuccess;
+        const long long need = ctx::attention_workspace_size(B, Sq, Sk, H, D, &e);
+        if (e != cudaSuccess)
+            return cuda_fail(e);
+        if (workspace_bytes < need)
+            return CTX_ERR_INVALID_ARG;
+    }
     ctx::AttnArgs a{};
     a.q = q;
     a.k = k;
@@ -379,8 +390,24 @@ ctx_status ctx_attn_lq_gkv(const void *q, const void *k, const void *v, const un
     a.D = D;
     a.bf16 = dtype == CTX_BF16;
     a.scale = scale;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
     cudaError_t e = ctx::launch_attention(a, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? CTX_OK : cuda_fail(e);
+}
+
+long long ctx_attn_lq_gkv_workspace_size(int B, int Sq, int Sk, int H, int D)
+{
+    long long n = 1;
+    if (!mul_ok(n, B) || !mul_ok(n, Sq) || !mul_ok(n, Sk) || !mul_ok(n, H) || (D != 64 && D != 128))
+        return -1;
+    cudaError_t e = cudaSuccess;
+    const long long bytes = ctx::attention_workspace_size(B, Sq, Sk, H, D, &e);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    return bytes;
 }
 
 ctx_status ctx_device_status(void *stream)

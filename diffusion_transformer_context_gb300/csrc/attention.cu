@@ -28,6 +28,7 @@
 // Every wait is bounded (%globaltimer); on expiry the kernel records a
 // timeout in the device status word, drains its own TMA loads and MMAs, frees
 // TMEM and returns.
+#include <algorithm>
 #include <cmath>
 #include <cudaTypedefs.h>
 #include <mutex>
@@ -54,9 +55,16 @@ struct Params {
     int B, Sq, Sk, H;
     int n_qpairs;
     int n_kblocks;
+    int n_units;           // work units: (query-tile pair, head, batch)
+    int grid;              // persistent CTAs
+    int dp_waves;          // whole-unit waves: CTA c takes units c, c+grid, ...
+    long long tail_iters;  // key blocks of the remaining units, split evenly over the grid
     float scale_log2;
     int *status;
     unsigned long long wait_limit_ns;
+    int *counters;         // [n_units][kTiles] arrivals at split units (zero between calls)
+    float2 *part_ml;       // [2*grid][kTiles*kBM] (m, l) of partial segments
+    float4 *part_o;        // [2*grid][D/4][kTiles*kBM] unnormalised O of partial segments
 };
 
 template <int D>
@@ -70,11 +78,72 @@ struct Layout {
     static constexpr int kKOff = kQOff + kTiles * kQBytes;
     static constexpr int kVOff = kKOff + kStages * kKVBytes;
     static constexpr int kBarOff = kVOff + kStages * kKVBytes;
-    static constexpr int kNumBars = 1 + 4 * kStages + 3 * kTiles + 1;
+    // q_full, q_empty, k_full[S], k_empty[S], v_full[S], v_empty[S],
+    // s_full[T], p_full[T], o_full[T], o_empty[T], seg_done[T], merge_go[T], mma_done
+    static constexpr int kNumBars = 2 + 4 * kStages + 6 * kTiles + 1;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-    static constexpr int kBytes = kMiscOff + 16;
+    static constexpr int kBytes = kMiscOff + 32;
     static constexpr int kAlloc = kBytes + 1024;    // room to align the base to 1024 B
 };
+
+// One contiguous run of key blocks [jb, je) of one work unit.
+struct Segment {
+    int unit, jb, je, slot;
+    bool full;
+};
+
+// Segment `si` of CTA c, computed from its index alone (identical in every
+// warp role, and no iterator state lives across the key-block loops): first
+// the whole-unit waves (concurrent CTAs work on neighbouring units, so they
+// share the same heads' K/V in L2), then an even share of the remaining
+// units' key blocks, cut at unit boundaries (so every SM finishes at the same
+// time; units cut between CTAs are merged by log-sum-exp).
+__device__ __forceinline__ bool segment_at(const Params &p, int c, int si, Segment &s)
+{
+    if (si < p.dp_waves) {
+        s.unit = si * p.grid + c;
+        s.jb = 0;
+        s.je = p.n_kblocks;
+        s.full = true;
+        s.slot = -1;
+        return true;
+    }
+    const long long nb = p.n_kblocks;
+    const long long tb = static_cast<long long>(c) * p.tail_iters / p.grid;
+    const long long te = static_cast<long long>(c + 1) * p.tail_iters / p.grid;
+    const int k = si - p.dp_waves;
+    const long long u0 = tb / nb;
+    const long long start = (k == 0) ? tb : (u0 + k) * nb;
+    if (start >= te)
+        return false;
+    const long long end = min(te, (u0 + k + 1) * nb);
+    const long long u = start / nb;
+    s.unit = p.dp_waves * p.grid + static_cast<int>(u);
+    s.jb = static_cast<int>(start - u * nb);
+    s.je = s.jb + static_cast<int>(end - start);
+    s.full = (s.jb == 0 && s.je == p.n_kblocks);
+    s.slot = (k == 0) ? 2 * c : 2 * c + 1;
+    return true;
+}
+
+// Hides the value of i from the optimiser, so a segment recomputed after a
+// hot loop is not kept live in registers across it.
+__device__ __forceinline__ int opaque(int i)
+{
+    asm volatile("" : "+r"(i));
+    return i;
+}
+
+__device__ __forceinline__ long long tail_start(const Params &p, int c)
+{
+    return static_cast<long long>(c) * p.tail_iters / p.grid;
+}
+
+// CTA whose tail range holds tail iteration `it`.
+__device__ __forceinline__ int tail_cta_of(const Params &p, long long it)
+{
+    return static_cast<int>(((it + 1) * p.grid + p.tail_iters - 1) / p.tail_iters) - 1;
+}
 
 // Bounded wait on an mbarrier phase. honor_abort: give up as soon as another
 // role has aborted. Returns false on abort or timeout.
@@ -136,6 +205,25 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint3
     }
 }
 
+// Stores one output row (D values scaled by inv) and its LSE.
+template <int D, bool BF16>
+__device__ __forceinline__ void store_row(const Params &p, int b, int h, int qrow, const float *o, float inv,
+                                          float lse_val)
+{
+    if (qrow >= p.Sq)
+        return;
+    uint4 *orow = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) +
+                                            ((static_cast<size_t>(b) * p.Sq + qrow) * p.H + h) * D);
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i)
+        orow[i] = make_uint4(ptx::pack2<BF16>(o[8 * i + 0] * inv, o[8 * i + 1] * inv),
+                             ptx::pack2<BF16>(o[8 * i + 2] * inv, o[8 * i + 3] * inv),
+                             ptx::pack2<BF16>(o[8 * i + 4] * inv, o[8 * i + 5] * inv),
+                             ptx::pack2<BF16>(o[8 * i + 6] * inv, o[8 * i + 7] * inv));
+    if (p.lse)
+        p.lse[(static_cast<size_t>(b) * p.H + h) * p.Sq + qrow] = lse_val;
+}
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -146,26 +234,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
     uint64_t *q_full = bars;
-    uint64_t *k_full = q_full + 1;
+    uint64_t *q_empty = q_full + 1;
+    uint64_t *k_full = q_empty + 1;
     uint64_t *k_empty = k_full + kStages;
     uint64_t *v_full = k_empty + kStages;
     uint64_t *v_empty = v_full + kStages;
     uint64_t *s_full = v_empty + kStages;
     uint64_t *p_full = s_full + kTiles;
     uint64_t *o_full = p_full + kTiles;
-    uint64_t *mma_done = o_full + kTiles;
+    uint64_t *o_empty = o_full + kTiles;
+    uint64_t *seg_done = o_empty + kTiles;
+    uint64_t *merge_go = seg_done + kTiles;
+    uint64_t *mma_done = merge_go + kTiles;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
+    volatile int *merge_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 8);  // [kTiles]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int qp = blockIdx.x % p.n_qpairs;
-    const int bh = blockIdx.x / p.n_qpairs;
-    const int h = bh % p.H, b = bh / p.H;
-    const int q0 = qp * (kTiles * kBM);
-    const int nblk = p.n_kblocks;
+    const int cta = blockIdx.x;
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(q_full, 1);
+        ptx::mbar_init(q_empty, 1);
         for (int s = 0; s < kStages; ++s) {
             ptx::mbar_init(k_full + s, 1);
             ptx::mbar_init(k_empty + s, 1);
@@ -176,6 +266,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(s_full + t, 1);
             ptx::mbar_init(p_full + t, 128);
             ptx::mbar_init(o_full + t, 1);
+            ptx::mbar_init(o_empty + t, 128);
+            ptx::mbar_init(seg_done + t, 128);
+            ptx::mbar_init(merge_go + t, 1);
+            merge_flag[t] = 0;
         }
         ptx::mbar_init(mma_done, 1);
         *abort_flag = 0;
@@ -196,43 +290,50 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tma_prefetch_desc(&tmQ);
             ptx::tma_prefetch_desc(&tmK);
             ptx::tma_prefetch_desc(&tmV);
-            ptx::mbar_arrive_expect_tx(q_full, kTiles * L::kQBytes);
-            for (int t = 0; t < kTiles; ++t)
-                for (int pn = 0; pn < L::kPanels; ++pn)
-                    ptx::tma_load_4d(&tmQ, q_full, smem + L::kQOff + t * L::kQBytes + pn * L::kQPanel, pn * 64, h,
-                                     q0 + t * kBM, b);
-            int issued[kStages] = {0};
-            for (int j = 0; j < nblk; ++j) {
-                const int s = j % kStages, u = j / kStages;
-                if (u > 0 && !wait_bar(k_empty + s, (u - 1) & 1, abort_flag, p))
+            Segment sg;
+            int kv = 0, segi = 0;
+            int last_k[kStages], last_v[kStages];
+            for (int s = 0; s < kStages; ++s)
+                last_k[s] = last_v[s] = -1;
+            bool ok = true;
+            while (ok && segment_at(p, cta, segi, sg)) {
+                const int qp = sg.unit % p.n_qpairs, bh = sg.unit / p.n_qpairs;
+                const int h = bh % p.H, b = bh / p.H;
+                const int q0 = qp * (kTiles * kBM);
+                if (segi > 0 && !(ok = wait_bar(q_empty, (segi - 1) & 1, abort_flag, p)))
                     break;
-                ptx::mbar_arrive_expect_tx(k_full + s, L::kKVBytes);
-                for (int pn = 0; pn < L::kPanels; ++pn)
-                    ptx::tma_load_4d(&tmK, k_full + s, smem + L::kKOff + s * L::kKVBytes + pn * L::kKVPanel, pn * 64,
-                                     h, j * kBN, b);
-                if (u > 0 && !wait_bar(v_empty + s, (u - 1) & 1, abort_flag, p)) {
-                    issued[s] = -(u + 1);  // K of use u issued, V not
-                    break;
+                ptx::mbar_arrive_expect_tx(q_full, kTiles * L::kQBytes);
+                for (int t = 0; t < kTiles; ++t)
+                    for (int pn = 0; pn < L::kPanels; ++pn)
+                        ptx::tma_load_4d(&tmQ, q_full, smem + L::kQOff + t * L::kQBytes + pn * L::kQPanel, pn * 64,
+                                         h, q0 + t * kBM, b);
+                ++segi;
+                for (int j = sg.jb; j < sg.je; ++j, ++kv) {
+                    const int s = kv % kStages, u = kv / kStages;
+                    if (u > 0 && !(ok = wait_bar(k_empty + s, (u - 1) & 1, abort_flag, p)))
+                        break;
+                    ptx::mbar_arrive_expect_tx(k_full + s, L::kKVBytes);
+                    for (int pn = 0; pn < L::kPanels; ++pn)
+                        ptx::tma_load_4d(&tmK, k_full + s, smem + L::kKOff + s * L::kKVBytes + pn * L::kKVPanel,
+                                         pn * 64, h, j * kBN, b);
+                    last_k[s] = u;
+                    if (u > 0 && !(ok = wait_bar(v_empty + s, (u - 1) & 1, abort_flag, p)))
+                        break;
+                    ptx::mbar_arrive_expect_tx(v_full + s, L::kKVBytes);
+                    for (int pn = 0; pn < L::kPanels; ++pn)
+                        ptx::tma_load_4d(&tmV, v_full + s, smem + L::kVOff + s * L::kKVBytes + pn * L::kKVPanel,
+                                         pn * 64, h, j * kBN, b);
+                    last_v[s] = u;
                 }
-                ptx::mbar_arrive_expect_tx(v_full + s, L::kKVBytes);
-                for (int pn = 0; pn < L::kPanels; ++pn)
-                    ptx::tma_load_4d(&tmV, v_full + s, smem + L::kVOff + s * L::kKVBytes + pn * L::kKVPanel, pn * 64,
-                                     h, j * kBN, b);
-                issued[s] = u + 1;
             }
             // Drain: every issued load has landed before the CTA can exit.
-            wait_bar(q_full, 0, abort_flag, p, false);
+            if (segi > 0)
+                wait_bar(q_full, (segi - 1) & 1, abort_flag, p, false);
             for (int s = 0; s < kStages; ++s) {
-                int n = issued[s];
-                if (n < 0) {
-                    n = -n;
-                    wait_bar(k_full + s, (n - 1) & 1, abort_flag, p, false);
-                    if (n - 1 > 0)
-                        wait_bar(v_full + s, (n - 2) & 1, abort_flag, p, false);
-                } else if (n > 0) {
-                    wait_bar(k_full + s, (n - 1) & 1, abort_flag, p, false);
-                    wait_bar(v_full + s, (n - 1) & 1, abort_flag, p, false);
-                }
+                if (last_k[s] >= 0)
+                    wait_bar(k_full + s, last_k[s] & 1, abort_flag, p, false);
+                if (last_v[s] >= 0)
+                    wait_bar(v_full + s, last_v[s] & 1, abort_flag, p, false);
             }
         }
     } else if (warp == 1) {
@@ -244,51 +345,68 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t vbase = ptx::smem_u32(smem + L::kVOff);
             const uint32_t tS0 = tmem, tS1 = tmem + kBN;
             const uint32_t tO0 = tmem + 2 * kBN, tO1 = tmem + 2 * kBN + D;
-            bool ok = wait_bar(q_full, 0, abort_flag, p);
-            if (ok)
-                ptx::tc_fence_after();
-            for (int j = 0; ok && j < nblk; ++j) {
-                const int s = j % kStages, u = j / kStages;
-                if (!(ok = wait_bar(k_full + s, u & 1, abort_flag, p)))
+            Segment sg;
+            int kv = 0, g = 0, segi = 0;
+            bool ok = true;
+            while (ok && segment_at(p, cta, segi, sg)) {
+                const int n = sg.je - sg.jb;
+                if (!(ok = wait_bar(q_full, segi & 1, abort_flag, p)))
                     break;
                 ptx::tc_fence_after();
-                const int jp = j - 1, sp = (j + kStages - 1) % kStages, up = jp / kStages;
-                if (j > 0) {
-                    if (!(ok = wait_bar(v_full + sp, up & 1, abort_flag, p)))
-                        break;
-                    if (!(ok = wait_bar(p_full + 0, jp & 1, abort_flag, p)))
+                for (int i = 0; i < n; ++i) {
+                    const int cur = kv + i, s = cur % kStages, u = cur / kStages;
+                    if (!(ok = wait_bar(k_full + s, u & 1, abort_flag, p)))
                         break;
                     ptx::tc_fence_after();
-                    issue_pv<D, BF16>(tO0, tS0, vbase + sp * L::kKVBytes, jp > 0);
+                    const int prv = cur - 1, sp = (cur + kStages - 1) % kStages, up = prv / kStages;
+                    if (i > 0) {
+                        if (!(ok = wait_bar(v_full + sp, up & 1, abort_flag, p)))
+                            break;
+                        if (!(ok = wait_bar(p_full + 0, (g + i - 1) & 1, abort_flag, p)))
+                            break;
+                        if (i == 1 && segi > 0 && !(ok = wait_bar(o_empty + 0, (segi - 1) & 1, abort_flag, p)))
+                            break;
+                        ptx::tc_fence_after();
+                        issue_pv<D, BF16>(tO0, tS0, vbase + sp * L::kKVBytes, i > 1);
+                    }
+                    issue_qk<D, BF16>(tS0, qa0, kbase + s * L::kKVBytes);
+                    ptx::tc_commit(s_full + 0);
+                    if (i > 0) {
+                        if (!(ok = wait_bar(p_full + 1, (g + i - 1) & 1, abort_flag, p)))
+                            break;
+                        if (i == 1 && segi > 0 && !(ok = wait_bar(o_empty + 1, (segi - 1) & 1, abort_flag, p)))
+                            break;
+                        ptx::tc_fence_after();
+                        issue_pv<D, BF16>(tO1, tS1, vbase + sp * L::kKVBytes, i > 1);
+                        ptx::tc_commit(v_empty + sp);
+                    }
+                    issue_qk<D, BF16>(tS1, qa1, kbase + s * L::kKVBytes);
+                    ptx::tc_commit(s_full + 1);
+                    ptx::tc_commit(k_empty + s);
                 }
-                issue_qk<D, BF16>(tS0, qa0, kbase + s * L::kKVBytes);
-                ptx::tc_commit(s_full + 0);
-                if (j > 0) {
-                    if (!(ok = wait_bar(p_full + 1, jp & 1, abort_flag, p)))
-                        break;
-                    ptx::tc_fence_after();
-                    issue_pv<D, BF16>(tO1, tS1, vbase + sp * L::kKVBytes, jp > 0);
-                    ptx::tc_commit(v_empty + sp);
-                }
-                issue_qk<D, BF16>(tS1, qa1, kbase + s * L::kKVBytes);
-                ptx::tc_commit(s_full + 1);
-                ptx::tc_commit(k_empty + s);
-            }
-            if (ok) {
-                const int jl = nblk - 1, sl = jl % kStages, ul = jl / kStages;
-                ok = wait_bar(v_full + sl, ul & 1, abort_flag, p) && wait_bar(p_full + 0, jl & 1, abort_flag, p);
-                if (ok) {
-                    ptx::tc_fence_after();
-                    issue_pv<D, BF16>(tO0, tS0, vbase + sl * L::kKVBytes, jl > 0);
-                    ptx::tc_commit(o_full + 0);
-                    ok = wait_bar(p_full + 1, jl & 1, abort_flag, p);
-                }
-                if (ok) {
-                    ptx::tc_fence_after();
-                    issue_pv<D, BF16>(tO1, tS1, vbase + sl * L::kKVBytes, jl > 0);
-                    ptx::tc_commit(o_full + 1);
-                    ptx::tc_commit(v_empty + sl);
-                }
+                if (!ok)
+                    break;
+                ptx::tc_commit(q_empty);  // the segment's QK^T products are all issued
+                const int lst = kv + n - 1, sl = lst % kStages, ul = lst / kStages;
+                ok = wait_bar(v_full + sl, ul & 1, abort_flag, p) &&
+                     wait_bar(p_full + 0, (g + n - 1) & 1, abort_flag, p) &&
+                     (n > 1 || segi == 0 || wait_bar(o_empty + 0, (segi - 1) & 1, abort_flag, p));
+                if (!ok)
+                    break;
+                ptx::tc_fence_after();
+                issue_pv<D, BF16>(tO0, tS0, vbase + sl * L::kKVBytes, n > 1);
+                ptx::tc_commit(o_full + 0);
+                ok = wait_bar(p_full + 1, (g + n - 1) & 1, abort_flag, p) &&
+                     (n > 1 || segi == 0 || wait_bar(o_empty + 1, (segi - 1) & 1, abort_flag, p));
+                if (!ok)
+                    break;
+                ptx::tc_fence_after();
+                issue_pv<D, BF16>(tO1, tS1, vbase + sl * L::kKVBytes, n > 1);
+                ptx::tc_commit(o_full + 1);
+                ptx::tc_commit(v_empty + sl);
+                kv += n;
+                g += n;
+                ++segi;
             }
             // Every MMA issued above has retired before TMEM is released.
             ptx::tc_commit(mma_done);
@@ -300,146 +418,276 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = (warp - 2) >> 2;  // query tile
         const int quad = warp & 3;      // TMEM lane quadrant this warp may access
         const int row = quad * 32 + lane;
+        const int prow = t * kBM + row;  // row inside the unit's 256 query rows
+        const bool tile_leader = ((warp - 2) & 3) == 0 && lane == 0;
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t tS = tmem + lane_off + t * kBN;
         const uint32_t tO = tmem + lane_off + 2 * kBN + t * D;
-        const unsigned char *mrow = p.mask ? p.mask + static_cast<size_t>(b) * p.Sk : nullptr;
         const float c = p.scale_log2;
-        float m_run = -INFINITY, l_run = 0.f;
+        int g = 0, segi = 0, pc = 0;
         bool ok = true;
-        for (int j = 0; j < nblk; ++j) {
-            const int kb = j * kBN;
-            // validity of the block's keys, one bit per key, identical in every lane
-            uint32_t vb[4];
-            if (mrow) {
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const int key = kb + w * 32 + lane;
-                    const bool v = key < p.Sk && mrow[key] != 0;
-                    vb[w] = __ballot_sync(0xffffffffu, v);
-                }
-            } else {
-                const int vn = p.Sk - kb;
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const int n = vn - 32 * w;
-                    vb[w] = n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
-                }
+        while (ok) {
+            const unsigned char *mrow;
+            int n, jb;
+            {
+                Segment sg;
+                if (!segment_at(p, cta, segi, sg))
+                    break;
+                const int bh = sg.unit / p.n_qpairs, b = bh / p.H;
+                mrow = p.mask ? p.mask + static_cast<size_t>(b) * p.Sk : nullptr;
+                n = sg.je - sg.jb;
+                jb = sg.jb;
             }
-            const bool all_valid = (vb[0] & vb[1] & vb[2] & vb[3]) == 0xffffffffu;
+            float m_run = -INFINITY, l_run = 0.f;
+            for (int i = 0; i < n; ++i) {
+                const int kb = (jb + i) * kBN;
+                // validity of the block's keys, one bit per key, identical in every lane
+                uint32_t vb[4];
+                if (mrow) {
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const int key = kb + w * 32 + lane;
+                        const bool v = key < p.Sk && mrow[key] != 0;
+                        vb[w] = __ballot_sync(0xffffffffu, v);
+                    }
+                } else {
+                    const int vn = p.Sk - kb;
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const int nn = vn - 32 * w;
+                        vb[w] = nn >= 32 ? 0xffffffffu : (nn <= 0 ? 0u : ((1u << nn) - 1u));
+                    }
+                }
+                const bool all_valid = (vb[0] & vb[1] & vb[2] & vb[3]) == 0xffffffffu;
 
-            if (!(ok = wait_bar_warp(s_full + t, j & 1, abort_flag, p)))
+                if (!(ok = wait_bar_warp(s_full + t, (g + i) & 1, abort_flag, p)))
+                    break;
+                ptx::tc_fence_after();
+                float mx;
+                {
+                    uint32_t sr[kBN];
+                    ptx::tmem_ld32(tS + 0, sr + 0);
+                    ptx::tmem_ld32(tS + 32, sr + 32);
+                    ptx::tmem_ld32(tS + 64, sr + 64);
+                    ptx::tmem_ld32(tS + 96, sr + 96);
+                    ptx::tmem_ld_wait();
+                    ptx::reg_fence32(sr + 0);
+                    ptx::reg_fence32(sr + 32);
+                    ptx::reg_fence32(sr + 64);
+                    ptx::reg_fence32(sr + 96);
+                    float s[kBN];
+#pragma unroll
+                    for (int k = 0; k < kBN; ++k)
+                        s[k] = __uint_as_float(sr[k]);
+                    if (!all_valid) {
+#pragma unroll
+                        for (int k = 0; k < kBN; ++k)
+                            if (!((vb[k >> 5] >> (k & 31)) & 1u))
+                                s[k] = -INFINITY;
+                    }
+                    float acc[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        acc[k] = s[k];
+#pragma unroll
+                    for (int k = 8; k < kBN; k += 16) {
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            acc[q] = ptx::max3(acc[q], s[k + q], s[k + 8 + q]);
+                    }
+                    mx = ptx::max3(ptx::max3(acc[0], acc[1], acc[2]), ptx::max3(acc[3], acc[4], acc[5]),
+                                   fmaxf(acc[6], acc[7]));
+                }
+                const float m_new = fmaxf(m_run, mx * c);
+                if (i == 0) {
+                    m_run = m_new;
+                } else {
+                    const bool need = m_new > m_run + kRescaleLog2;
+                    if (__any_sync(0xffffffffu, need)) {
+                        const float alpha = need ? ptx::ex2_approx(m_run - m_new) : 1.0f;
+                        if (need) {
+                            l_run *= alpha;
+                            m_run = m_new;
+                        }
+#pragma unroll 1
+                        for (int c0 = 0; c0 < D / 16; ++c0) {
+                            uint32_t o[16];
+                            ptx::tmem_ld16(tO + c0 * 16, o);
+                            ptx::tmem_ld_wait();
+                            ptx::reg_fence16(o);
+#pragma unroll
+                            for (int k = 0; k < 16; ++k)
+                                o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                            ptx::tmem_st16(tO + c0 * 16, o);
+                        }
+                        ptx::tmem_st_wait();
+                    }
+                }
+                const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
+                const uint64_t c2 = ptx::f2_pack(c, c), nm2 = ptx::f2_pack(neg_m, neg_m);
+                uint64_t sum2[4] = {0, 0, 0, 0};
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t sh[64];
+                    ptx::tmem_ld32(tS + 64 * half, sh);
+                    ptx::tmem_ld32(tS + 64 * half + 32, sh + 32);
+                    ptx::tmem_ld_wait();
+                    ptx::reg_fence32(sh);
+                    ptx::reg_fence32(sh + 32);
+                    if (!all_valid) {
+#pragma unroll
+                        for (int k = 0; k < 64; ++k)
+                            if (!((vb[2 * half + (k >> 5)] >> (k & 31)) & 1u))
+                                sh[k] = __float_as_uint(-INFINITY);
+                    }
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        const uint64_t arg = ptx::f2_fma(
+                            ptx::f2_pack(__uint_as_float(sh[2 * k]), __uint_as_float(sh[2 * k + 1])), c2, nm2);
+                        const float p0 = ptx::ex2_approx(ptx::f2_lo(arg));
+                        const float p1 = ptx::ex2_approx(ptx::f2_hi(arg));
+                        sum2[k & 3] = ptx::f2_add(sum2[k & 3], ptx::f2_pack(p0, p1));
+                        pk[k] = ptx::pack2<BF16>(p0, p1);
+                    }
+                    ptx::tmem_st32(tS + 32 * half, pk);
+                }
+                const uint64_t t01 = ptx::f2_add(sum2[0], sum2[1]), t23 = ptx::f2_add(sum2[2], sum2[3]);
+                const uint64_t tot = ptx::f2_add(t01, t23);
+                l_run += ptx::f2_lo(tot) + ptx::f2_hi(tot);
+                ptx::tmem_st_wait();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(p_full + t);
+            }
+            if (!ok)
+                break;
+            if (!(ok = wait_bar_warp(o_full + t, segi & 1, abort_flag, p)))
                 break;
             ptx::tc_fence_after();
-            uint32_t sr[kBN];
-            ptx::tmem_ld32(tS + 0, sr + 0);
-            ptx::tmem_ld32(tS + 32, sr + 32);
-            ptx::tmem_ld32(tS + 64, sr + 64);
-            ptx::tmem_ld32(tS + 96, sr + 96);
-            ptx::tmem_ld_wait();
-            ptx::reg_fence32(sr + 0);
-            ptx::reg_fence32(sr + 32);
-            ptx::reg_fence32(sr + 64);
-            ptx::reg_fence32(sr + 96);
-            float s[kBN];
+            Segment sg;
+            segment_at(p, cta, opaque(segi), sg);
+            const int qp = sg.unit % p.n_qpairs, bh = sg.unit / p.n_qpairs;
+            const int h = bh % p.H, b = bh / p.H;
+            const int qrow = qp * (kTiles * kBM) + prow;
+            if (sg.full) {
+                const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
+                const float lse_val = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
 #pragma unroll
-            for (int i = 0; i < kBN; ++i)
-                s[i] = __uint_as_float(sr[i]);
-            if (!all_valid) {
+                for (int c0 = 0; c0 < D / 32; ++c0) {
+                    uint32_t o[32];
+                    ptx::tmem_ld32(tO + c0 * 32, o);
+                    ptx::tmem_ld_wait();
+                    ptx::reg_fence32(o);
+                    float of[32];
 #pragma unroll
-                for (int i = 0; i < kBN; ++i)
-                    if (!((vb[i >> 5] >> (i & 31)) & 1u))
-                        s[i] = -INFINITY;
-            }
-            // row max: eight independent chains of 3-input max, then a tree
-            float acc[8];
+                    for (int k = 0; k < 32; ++k)
+                        of[k] = __uint_as_float(o[k]);
+                    if (qrow < p.Sq) {
+                        uint4 *orow = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) +
+                                                                ((static_cast<size_t>(b) * p.Sq + qrow) * p.H + h) * D);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                acc[i] = s[i];
-#pragma unroll
-            for (int i = 8; i < kBN; i += 16) {
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    acc[q] = ptx::max3(acc[q], s[i + q], s[i + 8 + q]);
-            }
-            const float mx = ptx::max3(ptx::max3(acc[0], acc[1], acc[2]), ptx::max3(acc[3], acc[4], acc[5]),
-                                       fmaxf(acc[6], acc[7]));
-            const float m_new = fmaxf(m_run, mx * c);
-            if (j == 0) {
-                m_run = m_new;
+                        for (int k = 0; k < 4; ++k)
+                            orow[c0 * 4 + k] = make_uint4(ptx::pack2<BF16>(of[8 * k + 0] * inv, of[8 * k + 1] * inv),
+                                                          ptx::pack2<BF16>(of[8 * k + 2] * inv, of[8 * k + 3] * inv),
+                                                          ptx::pack2<BF16>(of[8 * k + 4] * inv, of[8 * k + 5] * inv),
+                                                          ptx::pack2<BF16>(of[8 * k + 6] * inv, of[8 * k + 7] * inv));
+                    }
+                }
+                if (p.lse && qrow < p.Sq)
+                    p.lse[(static_cast<size_t>(b) * p.H + h) * p.Sq + qrow] = lse_val;
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(o_empty + t);
             } else {
-                const bool need = m_new > m_run + kRescaleLog2;
-                if (__any_sync(0xffffffffu, need)) {
-                    // PV of block j-1 has completed: S(j) was committed after it.
-                    const float alpha = need ? ptx::ex2_approx(m_run - m_new) : 1.0f;
-                    if (need) {
-                        l_run *= alpha;
-                        m_run = m_new;
+                // Partial segment: unnormalised O and (m, l) go to this CTA's slot.
+                float4 *po = p.part_o + static_cast<size_t>(sg.slot) * (D / 4) * (kTiles * kBM) + prow;
+#pragma unroll
+                for (int c0 = 0; c0 < D / 32; ++c0) {
+                    uint32_t o[32];
+                    ptx::tmem_ld32(tO + c0 * 32, o);
+                    ptx::tmem_ld_wait();
+                    ptx::reg_fence32(o);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        __stcg(po + static_cast<size_t>(c0 * 8 + k) * (kTiles * kBM),
+                               make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
+                                           __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3])));
+                }
+                __stcg(p.part_ml + static_cast<size_t>(sg.slot) * (kTiles * kBM) + prow, make_float2(m_run, l_run));
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(o_empty + t);
+                __threadfence();
+                ptx::mbar_arrive(seg_done + t);
+                const long long ut = sg.unit - static_cast<long long>(p.dp_waves) * p.grid;
+                const long long first = ut * p.n_kblocks;
+                const int c_lo = tail_cta_of(p, first), c_hi = tail_cta_of(p, first + p.n_kblocks - 1);
+                if (tile_leader) {
+                    int last = 0;
+                    if (wait_bar(seg_done + t, pc & 1, abort_flag, p)) {
+                        int *cnt = p.counters + static_cast<size_t>(sg.unit) * kTiles + t;
+                        const int old = atomicAdd(cnt, 1);
+                        last = (old == c_hi - c_lo);
+                        if (last)
+                            *cnt = 0;  // leave the workspace zeroed for the next call
+                        __threadfence();
                     }
+                    merge_flag[t] = last;
+                    ptx::mbar_arrive(merge_go + t);
+                }
+                if (!(ok = wait_bar_warp(merge_go + t, pc & 1, abort_flag, p)))
+                    break;
+                ++pc;
+                if (merge_flag[t]) {
+                    // Last segment of this unit to finish: combine every segment by log-sum-exp.
+                    float M = -INFINITY;
+                    for (int cc = c_lo; cc <= c_hi; ++cc) {
+                        const int sl = (tail_start(p, cc) >= first) ? 2 * cc : 2 * cc + 1;
+                        M = fmaxf(M, __ldcg(p.part_ml + static_cast<size_t>(sl) * (kTiles * kBM) + prow).x);
+                    }
+                    float lsum = 0.f;
+                    for (int cc = c_lo; cc <= c_hi; ++cc) {
+                        const int sl = (tail_start(p, cc) >= first) ? 2 * cc : 2 * cc + 1;
+                        const float2 ml = __ldcg(p.part_ml + static_cast<size_t>(sl) * (kTiles * kBM) + prow);
+                        lsum += (ml.x == -INFINITY) ? 0.f : ptx::ex2_approx(ml.x - M) * ml.y;
+                    }
+                    const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
+                    uint4 *orow = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) +
+                                                            ((static_cast<size_t>(b) * p.Sq + qrow) * p.H + h) * D);
 #pragma unroll 1
-                    for (int c0 = 0; c0 < D / 16; ++c0) {
-                        uint32_t o[16];
-                        ptx::tmem_ld16(tO + c0 * 16, o);
-                        ptx::tmem_ld_wait();
-                        ptx::reg_fence16(o);
+                    for (int c0 = 0; c0 < D / 32; ++c0) {
+                        float o[32];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        ptx::tmem_st16(tO + c0 * 16, o);
+                        for (int k = 0; k < 32; ++k)
+                            o[k] = 0.f;
+                        for (int cc = c_lo; cc <= c_hi; ++cc) {
+                            const int sl = (tail_start(p, cc) >= first) ? 2 * cc : 2 * cc + 1;
+                            const float2 ml = __ldcg(p.part_ml + static_cast<size_t>(sl) * (kTiles * kBM) + prow);
+                            const float w = (ml.x == -INFINITY) ? 0.f : ptx::ex2_approx(ml.x - M);
+                            const float4 *src = p.part_o + (static_cast<size_t>(sl) * (D / 4) + c0 * 8) * (kTiles * kBM) + prow;
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) {
+                                const float4 v = __ldcg(src + static_cast<size_t>(k) * (kTiles * kBM));
+                                o[4 * k] += w * v.x;
+                                o[4 * k + 1] += w * v.y;
+                                o[4 * k + 2] += w * v.z;
+                                o[4 * k + 3] += w * v.w;
+                            }
+                        }
+                        if (qrow < p.Sq) {
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                orow[c0 * 4 + k] = make_uint4(ptx::pack2<BF16>(o[8 * k + 0] * inv, o[8 * k + 1] * inv),
+                                                              ptx::pack2<BF16>(o[8 * k + 2] * inv, o[8 * k + 3] * inv),
+                                                              ptx::pack2<BF16>(o[8 * k + 4] * inv, o[8 * k + 5] * inv),
+                                                              ptx::pack2<BF16>(o[8 * k + 6] * inv, o[8 * k + 7] * inv));
+                        }
                     }
-                    ptx::tmem_st_wait();
+                    if (p.lse && qrow < p.Sq)
+                        p.lse[(static_cast<size_t>(b) * p.H + h) * p.Sq + qrow] =
+                            lsum > 0.f ? (M + log2f(lsum)) * kLn2 : -INFINITY;
                 }
             }
-            const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
-            const uint64_t c2 = ptx::f2_pack(c, c), nm2 = ptx::f2_pack(neg_m, neg_m);
-            uint64_t sum2[4] = {0, 0, 0, 0};  // four independent packed partial sums
-            // P overwrites the first 64 columns of S, 32 columns (64 keys) at a time
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int col = 64 * half + 2 * i;
-                    const uint64_t arg = ptx::f2_fma(ptx::f2_pack(s[col], s[col + 1]), c2, nm2);
-                    const float p0 = ptx::ex2_approx(ptx::f2_lo(arg));
-                    const float p1 = ptx::ex2_approx(ptx::f2_hi(arg));
-                    sum2[i & 3] = ptx::f2_add(sum2[i & 3], ptx::f2_pack(p0, p1));
-                    pk[i] = ptx::pack2<BF16>(p0, p1);
-                }
-                ptx::tmem_st32(tS + 32 * half, pk);
-            }
-            const uint64_t t01 = ptx::f2_add(sum2[0], sum2[1]), t23 = ptx::f2_add(sum2[2], sum2[3]);
-            const uint64_t tot = ptx::f2_add(t01, t23);
-            l_run += ptx::f2_lo(tot) + ptx::f2_hi(tot);
-            ptx::tmem_st_wait();
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(p_full + t);
-        }
-        if (ok && wait_bar_warp(o_full + t, 0, abort_flag, p)) {
-            ptx::tc_fence_after();
-            const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
-            const int qrow = q0 + t * kBM + row;
-            uint4 *orow = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) +
-                                                    ((static_cast<size_t>(b) * p.Sq + qrow) * p.H + h) * D);
-#pragma unroll
-            for (int c0 = 0; c0 < D / 32; ++c0) {
-                uint32_t o[32];
-                ptx::tmem_ld32(tO + c0 * 32, o);
-                ptx::tmem_ld_wait();
-                ptx::reg_fence32(o);
-                uint32_t w[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    w[i] = ptx::pack2<BF16>(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
-                if (qrow < p.Sq) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        orow[c0 * 4 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-                }
-            }
-            if (p.lse && qrow < p.Sq)
-                p.lse[(static_cast<size_t>(b) * p.H + h) * p.Sq + qrow] =
-                    l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+            g += n;
+            ++segi;
         }
     }
 
@@ -503,6 +751,49 @@ cudaError_t make_map(CUtensorMap *m, const void *base, int B, int S, int H, int 
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+struct Schedule {
+    int n_units, n_kblocks, grid, dp_waves;
+    long long tail_iters;
+};
+
+// Work split for one call. Without a workspace every CTA takes one whole unit
+// (grid = units). With one, a persistent grid of one CTA per SM runs whole-unit
+// waves and then shares the key blocks of the last (grid..2*grid) units evenly.
+Schedule plan(int B, int Sq, int Sk, int H, int sms, bool split)
+{
+    Schedule s{};
+    const int n_qpairs = (Sq + kTiles * kBM - 1) / (kTiles * kBM);
+    s.n_units = n_qpairs * H * B;
+    s.n_kblocks = (Sk + kBN - 1) / kBN;
+    if (!split) {
+        s.grid = s.n_units;
+        s.dp_waves = 1;
+        s.tail_iters = 0;
+        return s;
+    }
+    const long long total = static_cast<long long>(s.n_units) * s.n_kblocks;
+    s.grid = static_cast<int>(std::min<long long>(sms, total));
+    const int waves = s.n_units / s.grid;
+    s.dp_waves = (s.n_units % s.grid == 0) ? waves : std::max(0, waves - 1);
+    s.tail_iters = static_cast<long long>(s.n_units - s.dp_waves * s.grid) * s.n_kblocks;
+    return s;
+}
+
+long long ws_counter_bytes(const Schedule &s)
+{
+    return (static_cast<long long>(s.n_units) * kTiles * 4 + 255) / 256 * 256;
+}
+
+long long ws_ml_bytes(const Schedule &s)
+{
+    return 2LL * s.grid * kTiles * kBM * 8;
+}
+
+long long ws_bytes(const Schedule &s, int D)
+{
+    return ws_counter_bytes(s) + ws_ml_bytes(s) + 2LL * s.grid * (D / 4) * kTiles * kBM * 16;
+}
+
 template <int D, bool BF16>
 cudaError_t launch_typed(const AttnArgs &a, cudaStream_t stream)
 {
@@ -524,6 +815,12 @@ cudaError_t launch_typed(const AttnArgs &a, cudaStream_t stream)
                 attr_set[dev] = true;
         }
     }
+    const int sms = sm_count(&err);
+    if (err != cudaSuccess)
+        return err;
+    const Schedule sc = plan(a.B, a.Sq, a.Sk, a.H, sms, a.workspace != nullptr);
+    if (a.workspace && a.workspace_bytes < ws_bytes(sc, D))
+        return cudaErrorInvalidValue;
     CUtensorMap mq, mk, mv;
     if ((err = make_map(&mq, a.q, a.B, a.Sq, a.H, D, BF16)) != cudaSuccess)
         return err;
@@ -540,20 +837,35 @@ cudaError_t launch_typed(const AttnArgs &a, cudaStream_t stream)
     p.Sk = a.Sk;
     p.H = a.H;
     p.n_qpairs = (a.Sq + kTiles * kBM - 1) / (kTiles * kBM);
-    p.n_kblocks = (a.Sk + kBN - 1) / kBN;
+    p.n_kblocks = sc.n_kblocks;
+    p.n_units = sc.n_units;
+    p.grid = sc.grid;
+    p.dp_waves = sc.dp_waves;
+    p.tail_iters = sc.tail_iters;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.status = device_status_word(&err);
     if (err != cudaSuccess)
         return err;
     p.wait_limit_ns = kDefaultWaitLimitNs;
-    const long long grid = static_cast<long long>(p.n_qpairs) * a.H * a.B;
-    if (grid > 0x7fffffffLL)
-        return cudaErrorInvalidConfiguration;
-    attn_fwd_kernel<D, BF16><<<static_cast<unsigned>(grid), kThreads, L::kAlloc, stream>>>(mq, mk, mv, p);
+    if (a.workspace) {
+        uint8_t *ws = static_cast<uint8_t *>(a.workspace);
+        p.counters = reinterpret_cast<int *>(ws);
+        p.part_ml = reinterpret_cast<float2 *>(ws + ws_counter_bytes(sc));
+        p.part_o = reinterpret_cast<float4 *>(ws + ws_counter_bytes(sc) + ws_ml_bytes(sc));
+    }
+    attn_fwd_kernel<D, BF16><<<static_cast<unsigned>(sc.grid), kThreads, L::kAlloc, stream>>>(mq, mk, mv, p);
     return cudaGetLastError();
 }
 
 }  // namespace
+
+long long attention_workspace_size(int B, int Sq, int Sk, int H, int D, cudaError_t *err)
+{
+    const int sms = sm_count(err);
+    if (*err != cudaSuccess)
+        return -1;
+    return ws_bytes(plan(B, Sq, Sk, H, sms, true), D);
+}
 
 cudaError_t launch_attention(const AttnArgs &a, cudaStream_t stream)
 {

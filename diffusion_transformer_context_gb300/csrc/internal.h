@@ -50,9 +50,14 @@ struct AttnArgs {
     int B, Sq, Sk, H, D;
     bool bf16;
     float scale;
+    void *workspace;             // NULL: one CTA per work unit, no split
+    long long workspace_bytes;
 };
 
 cudaError_t launch_attention(const AttnArgs &a, cudaStream_t stream);
+
+// Bytes of workspace the balanced (split) schedule needs on the current device.
+long long attention_workspace_size(int B, int Sq, int Sk, int H, int D, cudaError_t *err);
 
 cudaError_t launch_selftest_wait(unsigned long long limit_ns, cudaStream_t stream);
 

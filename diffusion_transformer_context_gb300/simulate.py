@@ -29,12 +29,13 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (ctx_attn_lq_gkv, ctx_pack_out, ctx_pack_qkv, ctx_sim_all_to_all, ctx_unpack_out,
+from . import (attn_workspace, ctx_attn_lq_gkv, ctx_pack_out, ctx_pack_qkv, ctx_sim_all_to_all, ctx_unpack_out,
                ctx_unpack_qkv)
 
 
 class SimLayer:
-    def __init__(self, wl, device="cuda", dtype=torch.bfloat16, attention: bool | None = None):
+    def __init__(self, wl, device="cuda", dtype=torch.bfloat16, attention: bool | None = None,
+                 balanced: bool = True):
         self.wl = wl
         self.dev = torch.device(device)
         self.dtype = dtype
@@ -55,6 +56,8 @@ class SimLayer:
         self.mask = torch.ones((U * B, Sk), dtype=torch.uint8, device=self.dev) if wl.joint else None
         self.out = torch.empty((U, B, S, h_l, D), **kw)
         self.lse = torch.empty((U * B, h_l, S), dtype=torch.float32, device=self.dev)
+        # workspace of the balanced (persistent, key-split) attention schedule
+        self.ws = attn_workspace(U * B, S, Sk, h_l, D, device=self.dev) if (balanced and self.attention) else None
         if U > 1:
             ochunk = B * S_l * h_l * D
             self.osend = torch.empty((A, U, U, ochunk), **kw)
@@ -97,7 +100,7 @@ class SimLayer:
         if self.attention:
             ctx_attn_lq_gkv(self.qg.view(U * B, S, h_l, D), self.kg.view(U * B, Sk, h_l, D),
                             self.vg.view(U * B, Sk, h_l, D), self.out.view(U * B, S, h_l, D), self.lse,
-                            key_mask=self.mask, stream=stream)
+                            key_mask=self.mask, workspace=self.ws, stream=stream)
             if U > 1:
                 for g in range(self.R):
                     a, u = divmod(g, U)

@@ -142,15 +142,34 @@ ctx_status ctx_unpack_qkv(const void *recv, void *q, void *k, void *v,
  * scale    : softmax scale; NaN selects 1/sqrt(D). Otherwise finite and > 0.
  * out      : [B, Sq, H, D], device, same dtype as q.
  * lse      : NULL or [B, H, Sq] float32, device (natural log).
+ * workspace, workspace_bytes :
+ *            NULL / 0: one CTA per (256 query rows, head, batch) unit.
+ *            Otherwise device memory of at least
+ *            ctx_attn_lq_gkv_workspace_size(B, Sq, Sk, H, D) bytes, 256-byte
+ *            aligned, filled with zeros before its first use: a persistent
+ *            grid (one CTA per SM) runs whole-unit waves, then splits the key
+ *            range of the leftover units evenly over all SMs and merges the
+ *            pieces by log-sum-exp. A successful call leaves the workspace
+ *            zeroed again; after CTX_ERR_TIMEOUT it must be re-zeroed. Calls
+ *            that may run concurrently must not share a workspace.
  * D        : 64 or 128 (CTX_ERR_UNSUPPORTED otherwise).
  * Numerics : fp32 accumulation for QK^T, softmax and PV; the probabilities
  *            are rounded to the input dtype before the PV product; out is
- *            rounded to nearest even.
+ *            rounded to nearest even. Results do not depend on the workspace
+ *            beyond fp32 rounding of the merge.
  */
 ctx_status ctx_attn_lq_gkv(const void *q, const void *k, const void *v,
                            const unsigned char *key_mask, float scale,
-                           void *out, float *lse, int B, int Sq, int Sk, int H,
-                           int D, ctx_dtype dtype, void *stream);
+                           void *out, float *lse, void *workspace,
+                           long long workspace_bytes, int B, int Sq, int Sk,
+                           int H, int D, ctx_dtype dtype, void *stream);
+
+/*
+ * ctx_attn_lq_gkv_workspace_size — bytes of workspace ctx_attn_lq_gkv needs
+ * for its balanced schedule on the current device (it depends on the SM
+ * count). Returns -1 for invalid sizes or when no device can be queried.
+ */
+long long ctx_attn_lq_gkv_workspace_size(int B, int Sq, int Sk, int H, int D);
 
 /*
  * ctx_pack_out — reverse Ulysses exchange, send side (sglang PR #33667,

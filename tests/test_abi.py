@@ -87,17 +87,26 @@ def test_unpack_validation(lib):
 def test_attention_validation(lib):
     f = lib.ctx_attn_lq_gkv
     q, k, v, o, l = A0, A0 + MB, A0 + 2 * MB, A0 + 3 * MB, A0 + 4 * MB
+    w = A0 + 8 * MB
     nan = float("nan")
-    assert f(q, k, v, None, nan, o, l, 1, 16, 16, 2, 96, 0, None) == UNSUPPORTED
-    assert f(q, k, v, None, -1.0, o, l, 1, 16, 16, 2, 128, 0, None) == INVALID
-    assert f(q, k, v, None, float("inf"), o, l, 1, 16, 16, 2, 128, 0, None) == INVALID
-    assert f(q, k, v, None, nan, o, l, 1, 0, 16, 2, 128, 0, None) == INVALID
-    assert f(q, k, v, None, nan, o, l, 1, 16, -1, 2, 128, 0, None) == INVALID
-    assert f(q, k, v, None, nan, None, l, 1, 16, 16, 2, 128, 0, None) == INVALID
-    assert f(q + 4, k, v, None, nan, o, l, 1, 16, 16, 2, 128, 0, None) == MISALIGNED
-    assert f(q, k, v, None, nan, o, l + 2, 1, 16, 16, 2, 128, 0, None) == MISALIGNED
-    assert f(q, k, v, None, nan, q + 64, l, 1, 16, 16, 2, 128, 0, None) == ALIASING
-    assert f(q, k, v, None, nan, o, o + 16, 1, 16, 16, 2, 128, 0, None) == ALIASING
+    assert f(q, k, v, None, nan, o, l, None, 0, 1, 16, 16, 2, 96, 0, None) == UNSUPPORTED
+    assert f(q, k, v, None, -1.0, o, l, None, 0, 1, 16, 16, 2, 128, 0, None) == INVALID
+    assert f(q, k, v, None, float("inf"), o, l, None, 0, 1, 16, 16, 2, 128, 0, None) == INVALID
+    assert f(q, k, v, None, nan, o, l, None, 0, 1, 0, 16, 2, 128, 0, None) == INVALID
+    assert f(q, k, v, None, nan, o, l, None, 0, 1, 16, -1, 2, 128, 0, None) == INVALID
+    assert f(q, k, v, None, nan, None, l, None, 0, 1, 16, 16, 2, 128, 0, None) == INVALID
+    assert f(q, k, v, None, nan, o, l, w, 0, 1, 16, 16, 2, 128, 0, None) == INVALID      # workspace, no size
+    assert f(q + 4, k, v, None, nan, o, l, None, 0, 1, 16, 16, 2, 128, 0, None) == MISALIGNED
+    assert f(q, k, v, None, nan, o, l + 2, None, 0, 1, 16, 16, 2, 128, 0, None) == MISALIGNED
+    assert f(q, k, v, None, nan, o, l, w + 16, MB, 1, 16, 16, 2, 128, 0, None) == MISALIGNED
+    assert f(q, k, v, None, nan, q + 64, l, None, 0, 1, 16, 16, 2, 128, 0, None) == ALIASING
+    assert f(q, k, v, None, nan, o, o + 16, None, 0, 1, 16, 16, 2, 128, 0, None) == ALIASING
+    assert f(q, k, v, None, nan, o, l, k, MB, 1, 16, 16, 2, 128, 0, None) == ALIASING    # workspace over K
+
+
+def test_workspace_size_rejects_bad_sizes(lib):
+    assert lib.ctx_attn_lq_gkv_workspace_size(1, 0, 16, 2, 128) == -1
+    assert lib.ctx_attn_lq_gkv_workspace_size(1, 16, 16, 2, 96) == -1
 
 
 def test_reverse_and_a2a_validation(lib):

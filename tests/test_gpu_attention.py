@@ -27,8 +27,9 @@ def ctx():
     return m
 
 
-def _run(ctx, q, k, v, mask=None, scale=None, guard=False):
+def _run(ctx, q, k, v, mask=None, scale=None, guard=False, split=False):
     B, Sq, H, D = q.shape
+    Sk = k.shape[1]
     if guard:
         out = Guarded((B, Sq, H, D), q.dtype)
         lse = Guarded((B, H, Sq), torch.float32)
@@ -36,12 +37,17 @@ def _run(ctx, q, k, v, mask=None, scale=None, guard=False):
     else:
         o_t = torch.empty((B, Sq, H, D), dtype=q.dtype, device="cuda")
         l_t = torch.empty((B, H, Sq), dtype=torch.float32, device="cuda")
+    ws = ctx.attn_workspace(B, Sq, Sk, H, D) if split else None
     m = None if mask is None else torch.from_numpy(mask).cuda()
-    ctx.ctx_attn_lq_gkv(q.cuda(), k.cuda(), v.cuda(), o_t, l_t, key_mask=m, scale=scale)
+    ctx.ctx_attn_lq_gkv(q.cuda(), k.cuda(), v.cuda(), o_t, l_t, key_mask=m, scale=scale, workspace=ws)
     st = ctx.ctx_device_status()
     assert st == 0, ctx.ctx_status_string(st)
     if guard:
         assert out.intact() and lse.intact()
+    if split:
+        # the arrival counters at the head of the workspace are zero again
+        n_units = ((Sq + 255) // 256) * H * B
+        assert int(ws[:n_units * 2 * 4].count_nonzero()) == 0
     return o_t.float().cpu().numpy(), l_t.cpu().numpy()
 
 
@@ -69,11 +75,12 @@ SMALL = [  # B, Sq, Sk, H, D
 ]
 
 
+@pytest.mark.parametrize("split", [False, True], ids=["per_unit", "balanced"])
 @pytest.mark.parametrize("B,Sq,Sk,H,D", SMALL)
-def test_small_shapes_full(ctx, orc, B, Sq, Sk, H, D):
+def test_small_shapes_full(ctx, orc, B, Sq, Sk, H, D, split):
     gen = torch.Generator().manual_seed(1234)
     q, k, v = (workloads.randn(s, gen) for s in ((B, Sq, H, D), (B, Sk, H, D), (B, Sk, H, D)))
-    O, L = _run(ctx, q, k, v, guard=True)
+    O, L = _run(ctx, q, k, v, guard=True, split=split)
     _check_full(orc, q, k, v, O, L)
 
 
@@ -85,8 +92,9 @@ def test_fp16(ctx, orc):
     _check_full(orc, q, k, v, O, L, dtype="fp16")
 
 
+@pytest.mark.parametrize("split", [False, True], ids=["per_unit", "balanced"])
 @pytest.mark.parametrize("kind", ["random", "rear_text", "front_text", "first_block_empty", "row_empty"])
-def test_key_mask(ctx, orc, kind):
+def test_key_mask(ctx, orc, kind, split):
     gen = torch.Generator().manual_seed(11)
     B, Sq, Sk, H, D = 2, 200, 600, 2, 128
     q, k, v = (workloads.randn(s, gen) for s in ((B, Sq, H, D), (B, Sk, H, D), (B, Sk, H, D)))
@@ -104,7 +112,7 @@ def test_key_mask(ctx, orc, kind):
         mask[:, :300] = 0
     elif kind == "row_empty":
         mask[1, :] = 0
-    O, L = _run(ctx, q, k, v, mask=mask, guard=True)
+    O, L = _run(ctx, q, k, v, mask=mask, guard=True, split=split)
     _check_full(orc, q, k, v, O, L, mask=mask)
     if kind == "row_empty":
         assert (O[1] == 0).all() and np.isneginf(L[1]).all()
@@ -158,10 +166,10 @@ def test_lse_optional(ctx, orc):
 
 # ---------------------------------------------------------------- full sizes
 
-def _sampled(ctx, orc, B, Sq, Sk, H, D, n_rows, mask=None, seed=1234):
+def _sampled(ctx, orc, B, Sq, Sk, H, D, n_rows, mask=None, seed=1234, split=True):
     gen = torch.Generator().manual_seed(seed)
     q, k, v = (workloads.randn(s, gen) for s in ((B, Sq, H, D), (B, Sk, H, D), (B, Sk, H, D)))
-    O, L = _run(ctx, q, k, v, mask=mask)
+    O, L = _run(ctx, q, k, v, mask=mask, split=split)
     rows_i = workloads.sample_rows(Sq, n_rows)
     rng = np.random.default_rng(seed)
     bhi = np.stack([rng.integers(0, B, rows_i.size), rng.integers(0, H, rows_i.size), rows_i], axis=1)
@@ -192,6 +200,28 @@ def test_wan480_full_size_sampled(ctx, orc):
 def test_wan14b_full_size_sampled(ctx, orc):
     wl = workloads.WORKLOADS["wan14b"]
     _sampled(ctx, orc, wl.U * wl.B, wl.S, wl.Sk, wl.h_l, wl.D, 256)
+
+
+@pytest.mark.parametrize("B,Sq,Sk,H", [(1, 4095, 32760, 12), (1, 300, 4096, 1), (2, 2000, 3000, 5),
+                                       (1, 40000, 700, 16)])
+def test_balanced_schedule_matches_per_unit(ctx, B, Sq, Sk, H):
+    """The key-split schedule (units cut between SMs, merged by log-sum-exp)
+    agrees with one CTA per unit to fp32 rounding of the merge: same bf16
+    output up to one ulp, LSE to 1e-5. Shapes: one rank of the Wan-like 480p
+    layer (192 units on the SMs: every unit split), a single unit split over
+    many SMs, and uneven wave remainders."""
+    gen = torch.Generator().manual_seed(21)
+    q, k, v = (workloads.randn(s, gen).cuda() for s in ((B, Sq, H, 128), (B, Sk, H, 128), (B, Sk, H, 128)))
+    o1, l1 = torch.empty_like(q), torch.empty((B, H, Sq), device="cuda")
+    o2, l2 = torch.empty_like(q), torch.empty((B, H, Sq), device="cuda")
+    ws = ctx.attn_workspace(B, Sq, Sk, H, 128)
+    ctx.ctx_attn_lq_gkv(q, k, v, o1, l1)
+    ctx.ctx_attn_lq_gkv(q, k, v, o2, l2, workspace=ws)
+    ctx.ctx_attn_lq_gkv(q, k, v, o2, l2, workspace=ws)  # reuse: counters were left at zero
+    assert ctx.ctx_device_status() == 0
+    d = (o1.float() - o2.float()).abs()
+    assert float(d.max()) <= 2.0 ** -7 * max(1.0, float(o1.float().abs().max()))
+    assert float((l1 - l2).abs().max()) <= 1e-5
 
 
 # ---------------------------------------------------------------- failure path
