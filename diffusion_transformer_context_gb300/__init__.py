@@ -31,6 +31,7 @@ SIGNATURES = {
     "ctx_unpack_qkv": (_I, [_P, _P, _P, _P, _LL, _LL, _I, _I, _I, _I, _I, _I, _P]),
     "ctx_attn_lq_gkv": (_I, [_P, _P, _P, _P, _F, _P, _P, _P, _LL, _I, _I, _I, _I, _I, _I, _P]),
     "ctx_attn_lq_gkv_workspace_size": (_LL, [_I, _I, _I, _I, _I]),
+    "ctx_attn_lq_gkv_noalloc": (_I, [_P, _P, _P, _P, _F, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "ctx_pack_out": (_I, [_P, _P, _LL, _I, _I, _I, _I, _I, _I, _P]),
     "ctx_unpack_out": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "ctx_status_string": (ctypes.c_char_p, [_I]),
@@ -142,6 +143,19 @@ def ctx_attn_lq_gkv_workspace_size(B: int, Sq: int, Sk: int, H: int, D: int) -> 
     if n < 0:
         raise CtxError("ctx_attn_lq_gkv_workspace_size", 1)
     return n
+
+
+def ctx_attn_lq_gkv_noalloc(q, k, v, out, lse=None, key_mask=None, scale: float | None = None, stream=None):
+    """ctx_attn_lq_gkv with the balanced schedule and the library's own fixed
+    scratch array: nothing is allocated by anyone. Calls that can overlap on
+    the GPU must be serialised by the caller."""
+    B, Sq, H, D = q.shape
+    Sk = k.shape[1]
+    s = float("nan") if scale is None else float(scale)
+    _check("ctx_attn_lq_gkv_noalloc", lib().ctx_attn_lq_gkv_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(key_mask), s, _ptr(out), _ptr(lse), B, Sq, Sk, H, D, _dtype(q),
+        _stream(stream)))
+    return out
 
 
 def attn_workspace(B: int, Sq: int, Sk: int, H: int, D: int, device="cuda"):

@@ -144,6 +144,11 @@ ctx_status run_relayout(RelayoutMode mode, const RelayoutArgs &a, void *stream)
 
 }  // namespace
 
+void ctx::record_cuda_error(cudaError_t e)
+{
+    t_last_cuda_error = static_cast<int>(e);
+}
+
 extern "C" {
 
 int ctx_version(void)

@@ -61,4 +61,7 @@ long long attention_workspace_size(int B, int Sq, int Sk, int H, int D, cudaErro
 
 cudaError_t launch_selftest_wait(unsigned long long limit_ns, cudaStream_t stream);
 
+// Records a CUDA error for ctx_last_cuda_error() on the calling thread.
+void record_cuda_error(cudaError_t e);
+
 }  // namespace ctx

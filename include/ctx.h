@@ -172,6 +172,30 @@ ctx_status ctx_attn_lq_gkv(const void *q, const void *k, const void *v,
 long long ctx_attn_lq_gkv_workspace_size(int B, int Sq, int Sk, int H, int D);
 
 /*
+ * ctx_attn_lq_gkv_noalloc — ctx_attn_lq_gkv with the balanced schedule, for
+ * callers that cannot allocate device memory (a host framework that owns
+ * every buffer and passes only inputs and outputs, an embedding C program
+ * with no device allocator, a path that must not let cudaMalloc synchronise
+ * the device). The reference pages have no counterpart: it exists for this
+ * library's callers.
+ *
+ * Same arguments, layouts and results as ctx_attn_lq_gkv, without the
+ * workspace: the library keeps a fixed 44 MiB scratch array in device memory
+ * (held by every GPU that loads the library until the process exits) and
+ * allocates nothing on any call. The first call on each device looks up the
+ * array's device address; make that first call before any stream capture.
+ * Calls share the array: calls that can overlap on the GPU race and must be
+ * serialised by the caller. The arrival counters are cleared after every
+ * call. Returns CTX_ERR_UNSUPPORTED when the problem needs more scratch than
+ * 44 MiB (more than 131072 work units of 256 query rows, or a grid of more
+ * than 160 SMs at D = 128).
+ */
+ctx_status ctx_attn_lq_gkv_noalloc(const void *q, const void *k, const void *v,
+                                   const unsigned char *key_mask, float scale,
+                                   void *out, float *lse, int B, int Sq, int Sk,
+                                   int H, int D, ctx_dtype dtype, void *stream);
+
+/*
  * ctx_pack_out — reverse Ulysses exchange, send side (sglang PR #33667,
  * _usp_output_all_to_all; vllm-omni PR #7641, reverse Ulysses all-to-all):
  * rows of the head-sharded output go back to the rank that owns them.
