@@ -141,44 +141,29 @@ def run_gpu(args, rank, world, local_rank):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    # per-kernel-group events inside each step
+    if not args.eager:
+        sim.capture()
+
+    def run_phase(name):
+        if args.eager:
+            getattr(sim, name)(stream=stream)
+        else:
+            sim.replay(name)
+
+    # one step, with events between its phases (exchange_in: pack + all-to-all
+    # + unpack; attend: attention; exchange_out: reverse exchange)
     def timed_step(ev):
-        wl_ = sim.wl
-        U, A, B, S, D = wl_.U, wl_.A, wl_.B, wl_.S, wl_.D
-        S_l, h_l, Sk = sim.S_l, sim.h_l, sim.Sk
-        ev[0].record(stream)
-        for g in range(sim.R):
-            a, u = divmod(g, U)
-            x = sim.x[g]
-            ctx.ctx_pack_qkv(x[0], x[1], x[2], sim.send[a, u], U, stream=stream)
-        ev[1].record(stream)
-        if U > 1:
-            ctx.ctx_sim_all_to_all(sim.send, sim.recv, A, U, stream=stream)
-        ev[2].record(stream)
-        for g in range(sim.R):
-            a, u = divmod(g, U)
-            r0 = a * U * S_l
-            ctx.ctx_unpack_qkv(sim.recv[a, u].view(U, 3, B, S_l, h_l, D), sim.qg[u, :, r0:], sim.kg[u, :, r0:],
-                               sim.vg[u, :, r0:], U, q_batch_stride_rows=S, kv_batch_stride_rows=Sk, stream=stream)
-        ev[3].record(stream)
-        if sim.attention:
-            ctx.ctx_attn_lq_gkv(sim.qg.view(U * B, S, h_l, D), sim.kg.view(U * B, Sk, h_l, D),
-                                sim.vg.view(U * B, Sk, h_l, D), sim.out.view(U * B, S, h_l, D), sim.lse,
-                                key_mask=sim.mask, workspace=sim.ws, stream=stream)
-        ev[4].record(stream)
-        if sim.attention and U > 1:
-            for g in range(sim.R):
-                a, u = divmod(g, U)
-                ctx.ctx_pack_out(sim.out[u, :, a * U * S_l:], sim.osend[a, u].view(U, B, S_l, h_l, D), U,
-                                 o_batch_stride_rows=S, stream=stream)
-            ctx.ctx_sim_all_to_all(sim.osend, sim.orecv, A, U, stream=stream)
-            for g in range(sim.R):
-                a, u = divmod(g, U)
-                ctx.ctx_unpack_out(sim.orecv[a, u].view(U, B, S_l, h_l, D), sim.y[g], U, stream=stream)
-        ev[5].record(stream)
+        for i, name in enumerate(sim.PHASES):
+            ev[i].record(stream)
+            run_phase(name)
+        ev[len(sim.PHASES)].record(stream)
+
+    def plain_step():
+        for name in sim.PHASES:
+            run_phase(name)
 
     for _ in range(args.warmup):
-        sim.step(stream=stream)
+        plain_step()
     st = ctx.ctx_device_status(stream)
     if st != 0:
         raise RuntimeError(f"device status after warm-up: {ctx.ctx_status_string(st)}")
@@ -186,7 +171,7 @@ def run_gpu(args, rank, world, local_rank):
     sampler = ClockSampler(local_rank) if (rank == 0 and not args.no_clocks) else None
     if sampler:
         sampler.start()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(sim.PHASES) + 1)] for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     t0.record(stream)
@@ -199,10 +184,7 @@ def run_gpu(args, rank, world, local_rank):
     if st != 0:
         raise RuntimeError(f"device status after timed steps: {ctx.ctx_status_string(st)}")
     total_ms = t0.elapsed_time(t1)
-    parts = {k: [] for k in ("pack", "a2a", "unpack", "attn", "reverse")}
-    for ev in evs:
-        for name, (i0, i1) in zip(parts, ((0, 1), (1, 2), (2, 3), (3, 4), (4, 5))):
-            parts[name].append(ev[i0].elapsed_time(ev[i1]))
+    parts = {name: [ev[i].elapsed_time(ev[i + 1]) for ev in evs] for i, name in enumerate(sim.PHASES)}
     if world > 1:
         t = torch.tensor([total_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -217,14 +199,14 @@ def run_gpu(args, rank, world, local_rank):
         host_y = torch.empty(result.shape, dtype=result.dtype).pin_memory()
         for _ in range(max(1, args.warmup)):
             sim.x.copy_(host_x, non_blocking=True)
-            sim.step(stream=stream)
+            plain_step()
             host_y.copy_(result, non_blocking=True)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier()
         e0.record(stream)
         for _ in range(args.steps):
             sim.x.copy_(host_x, non_blocking=True)
-            sim.step(stream=stream)
+            plain_step()
             host_y.copy_(result, non_blocking=True)
         e1.record(stream)
         barrier()
@@ -361,6 +343,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--unbalanced", action="store_true", help="attention without workspace: one CTA per unit")
+    ap.add_argument("--eager", action="store_true", help="launch every kernel from Python instead of CUDA graphs")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=64)
     args = ap.parse_args()
@@ -390,12 +373,13 @@ def main():
     def avg(x):
         return sum(x) / len(x)
 
-    attn_ms = avg(parts["attn"])
+    attn_ms = avg(parts["attend"])
     tflops = attn_flops / (attn_ms * 1e-3) / 1e12 if attn_ms > 0 else 0.0
     peak_tf = peaks["bf16_tflops"]
-    relayout_bytes = sim.pack_bytes() + sim.unpack_bytes()
-    relayout_ms = avg(parts["pack"]) + avg(parts["unpack"])
+    relayout_bytes = sim.pack_bytes() + sim.a2a_bytes() + sim.unpack_bytes()
+    relayout_ms = avg(parts["exchange_in"])
     relayout_gbs = relayout_bytes / (relayout_ms * 1e-3) / 1e9
+    reverse_ms = avg(parts["exchange_out"])
     traffic = recorded_traffic(args.workload)
 
     line = {
@@ -406,17 +390,18 @@ def main():
                    "U": sim.wl.U, "A": sim.wl.A, "joint": sim.wl.joint, "virtual_ranks": sim.R,
                    "attn_call": f"B'={sim.wl.U * sim.wl.B} Sq={sim.wl.S} Sk={sim.Sk} H={sim.h_l} D={sim.wl.D}",
                    "l2": "inputs_larger_than_l2", "parallelism": f"replicas{world}",
-                   "attn_schedule": "one CTA per unit" if sim.ws is None else "persistent, key-split tail"},
+                   "attn_schedule": "one CTA per unit" if sim.ws is None else "persistent, key-split tail",
+                   "launch": "eager" if args.eager else "cuda graphs (one per phase)"},
         "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel", "achieved": round(tflops, 2),
                      "peak": peak_tf, "unit": "TFLOP/s", "frac": round(tflops / peak_tf, 4),
                      "peak_source": f"{peak_kind} bf16_tflops (burst)",
                      "algorithmic_flops_per_launch": attn_flops, "launch_ms": round(attn_ms, 4),
                      "traffic": traffic},
-        "relayout": {"bound": "hbm", "achieved": round(relayout_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(relayout_gbs / peaks["hbm_gbs"], 4),
-                     "pack_ms": round(avg(parts["pack"]), 4), "unpack_ms": round(avg(parts["unpack"]), 4),
-                     "a2a_ms": round(avg(parts["a2a"]), 4), "reverse_ms": round(avg(parts["reverse"]), 4),
-                     "algorithmic_bytes_pack_plus_unpack": relayout_bytes},
+        "relayout": {"bound": "hbm", "what": "pack + all-to-all + unpack of all ranks",
+                     "achieved": round(relayout_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(relayout_gbs / peaks["hbm_gbs"], 4), "ms": round(relayout_ms, 4),
+                     "algorithmic_bytes": relayout_bytes,
+                     "reverse_ms": round(reverse_ms, 4), "reverse_bytes": sim.reverse_bytes()},
         "gpu_launches": sim.launches_per_step() * K,
         "clocks": clocks,
         "e2e": e2e,

@@ -82,7 +82,8 @@ class SimLayer:
         torch.cuda.synchronize(self.dev)
 
     # ---------------------------------------------------------- one step
-    def step(self, stream=None):
+    def exchange_in(self, stream=None):
+        """Steps 1-3: pack, all-to-all, unpack into the gathered buffers."""
         wl = self.wl
         U, A, B, S, D = wl.U, wl.A, wl.B, wl.S, wl.D
         S_l, h_l, Sk = self.S_l, self.h_l, self.Sk
@@ -97,19 +98,63 @@ class SimLayer:
             r0 = a * U * S_l
             ctx_unpack_qkv(self.recv[a, u].view(U, 3, B, S_l, h_l, D), self.qg[u, :, r0:], self.kg[u, :, r0:],
                            self.vg[u, :, r0:], U, q_batch_stride_rows=S, kv_batch_stride_rows=Sk, stream=stream)
-        if self.attention:
-            ctx_attn_lq_gkv(self.qg.view(U * B, S, h_l, D), self.kg.view(U * B, Sk, h_l, D),
-                            self.vg.view(U * B, Sk, h_l, D), self.out.view(U * B, S, h_l, D), self.lse,
-                            key_mask=self.mask, workspace=self.ws, stream=stream)
-            if U > 1:
-                for g in range(self.R):
-                    a, u = divmod(g, U)
-                    ctx_pack_out(self.out[u, :, a * U * S_l:], self.osend[a, u].view(U, B, S_l, h_l, D), U,
-                                 o_batch_stride_rows=S, stream=stream)
-                ctx_sim_all_to_all(self.osend, self.orecv, A, U, stream=stream)
-                for g in range(self.R):
-                    a, u = divmod(g, U)
-                    ctx_unpack_out(self.orecv[a, u].view(U, B, S_l, h_l, D), self.y[g], U, stream=stream)
+
+    def attend(self, stream=None):
+        """Step 4: local-Q / global-KV attention of every rank."""
+        if not self.attention:
+            return
+        wl = self.wl
+        U, B, S, D = wl.U, wl.B, wl.S, wl.D
+        h_l, Sk = self.h_l, self.Sk
+        ctx_attn_lq_gkv(self.qg.view(U * B, S, h_l, D), self.kg.view(U * B, Sk, h_l, D),
+                        self.vg.view(U * B, Sk, h_l, D), self.out.view(U * B, S, h_l, D), self.lse,
+                        key_mask=self.mask, workspace=self.ws, stream=stream)
+
+    def exchange_out(self, stream=None):
+        """Step 5: the reverse exchange (identity at U = 1)."""
+        wl = self.wl
+        U, A, B, S, D = wl.U, wl.A, wl.B, wl.S, wl.D
+        S_l, h_l = self.S_l, self.h_l
+        if not self.attention or U == 1:
+            return
+        for g in range(self.R):
+            a, u = divmod(g, U)
+            ctx_pack_out(self.out[u, :, a * U * S_l:], self.osend[a, u].view(U, B, S_l, h_l, D), U,
+                         o_batch_stride_rows=S, stream=stream)
+        ctx_sim_all_to_all(self.osend, self.orecv, A, U, stream=stream)
+        for g in range(self.R):
+            a, u = divmod(g, U)
+            ctx_unpack_out(self.orecv[a, u].view(U, B, S_l, h_l, D), self.y[g], U, stream=stream)
+
+    PHASES = ("exchange_in", "attend", "exchange_out")
+
+    def step(self, stream=None):
+        for name in self.PHASES:
+            getattr(self, name)(stream=stream)
+
+    # ---------------------------------------------------------- CUDA graphs
+    def capture(self):
+        """Captures each phase of the step as a CUDA graph (same kernels, same
+        buffers: replay removes the host launch cost and the gaps between the
+        back-to-back layout launches). Run one eager step first so that the
+        library's per-device set-up happens outside the capture."""
+        self.step()
+        torch.cuda.synchronize(self.dev)
+        self.graphs = {}
+        for name in self.PHASES:
+            if name == "exchange_out" and (not self.attention or self.wl.U == 1):
+                continue  # the identity: nothing to launch
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                getattr(self, name)()
+            self.graphs[name] = g
+        torch.cuda.synchronize(self.dev)
+
+    def replay(self, phase=None):
+        for name in (self.PHASES if phase is None else (phase,)):
+            g = self.graphs.get(name)
+            if g is not None:
+                g.replay()
 
     def launches_per_step(self) -> int:
         U, R = self.wl.U, self.R
