@@ -118,6 +118,25 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(busy)}
 
 
+# ------------------------------------------------------------------ ranks
+
+def max_over_ranks(x: float, world: int, device="cpu") -> float:
+    """The slowest rank's time: every rank gets the maximum (all_reduce MAX)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank: float, world: int, ms: float) -> float:
+    """Weak scaling: every rank does the same work; the job's throughput is
+    all ranks' FLOPs over the slowest rank's time."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------ GPU arm
 
 def run_gpu(args, rank, world, local_rank):
@@ -185,10 +204,7 @@ def run_gpu(args, rank, world, local_rank):
         raise RuntimeError(f"device status after timed steps: {ctx.ctx_status_string(st)}")
     total_ms = t0.elapsed_time(t1)
     parts = {name: [ev[i].elapsed_time(ev[i + 1]) for ev in evs] for i, name in enumerate(sim.PHASES)}
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
 
     # ---------------------------------------------------------- e2e (host buffers)
     e2e = None
@@ -210,13 +226,9 @@ def run_gpu(args, rank, world, local_rank):
             host_y.copy_(result, non_blocking=True)
         e1.record(stream)
         barrier()
-        e2e_ms = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
         flops = sim.attn_flops(inp.text_len)
-        e2e = {"value": round(world * flops * args.steps / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+        e2e = {"value": round(whole_job_tflops(flops * args.steps, world, e2e_ms), 3), "unit": "TFLOP/s",
                "h2d_bytes_per_step": host_x.numel() * host_x.element_size(),
                "d2h_bytes_per_step": host_y.numel() * host_y.element_size(),
                "ms_per_step": round(e2e_ms / args.steps, 4)}
@@ -368,7 +380,7 @@ def main():
     K = args.steps
     attn_flops = sim.attn_flops(inp.text_len)
     ms_step = total_ms / K
-    value = world * attn_flops / (ms_step * 1e-3) / 1e12
+    value = whole_job_tflops(attn_flops, world, ms_step)
 
     def avg(x):
         return sum(x) / len(x)
