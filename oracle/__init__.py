@@ -73,6 +73,8 @@ def _load():
             for f in (lib.orc_pack_qkv, lib.orc_unpack_qkv, lib.orc_pack_out,
                       lib.orc_unpack_out, lib.orc_attention_rows, lib.orc_attention_probs):
                 f.restype = ctypes.c_int
+            lib.orc_lse_merge.argtypes = [p, p, ctypes.c_int, ll, ll, ll, p, p]
+            lib.orc_lse_merge.restype = ctypes.c_int
             lib.orc_num_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -264,6 +266,23 @@ def ulysses_reverse(o_ranks, U: int, A: int):
         for u, g in enumerate(grp):
             out[g] = unpack_out(recvs[u], U)
     return out
+
+
+def lse_merge(o_parts, lse_parts, dtype="bf16"):
+    """Combine attention results over disjoint key segments.
+
+    o_parts [P, B, Sq, H, D] uint16, lse_parts [P, B, H, Sq] float (natural
+    log). Returns (O [B, Sq, H, D] float64, LSE [B, H, Sq] float64)."""
+    o_parts = _u16(o_parts)
+    P, B, Sq, H, D = o_parts.shape
+    # row order (b, h, i) for both operands
+    o_rows = np.ascontiguousarray(o_parts.transpose(0, 1, 3, 2, 4)).reshape(P, B * H * Sq, D)
+    l_rows = np.ascontiguousarray(np.asarray(lse_parts, dtype=np.float64)).reshape(P, B * H * Sq)
+    out = np.empty((B * H * Sq, D), dtype=np.float64)
+    lse = np.empty((B * H * Sq,), dtype=np.float64)
+    rc = _load().orc_lse_merge(_ptr(o_rows), _ptr(l_rows), _DTYPES[dtype], P, B * H * Sq, D, _ptr(out), _ptr(lse))
+    assert rc == 0
+    return out.reshape(B, H, Sq, D).transpose(0, 2, 1, 3).copy(), lse.reshape(B, H, Sq)
 
 
 # ------------------------------------------------------- pure-Python twins

@@ -263,3 +263,44 @@ int orc_attention_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     }
     return bad ? 2 : 0;
 }
+
+/* Combination of attention results over P disjoint key segments (the merge
+ * that consumes the LSE): for every row,
+ *   lse = ln sum_p exp(lse_p),   out = sum_p exp(lse_p - lse) * o_p
+ * o_parts [P][rows][D] 16-bit, lse_parts [P][rows] (natural log, -inf for a
+ * segment without valid keys), out [rows][D] and lse [rows] in fp64. A row
+ * whose segments are all empty gets out = 0 and lse = -inf. */
+int orc_lse_merge(const uint16_t *o_parts, const double *lse_parts, int dtype, long long P,
+                  long long rows, long long D, double *out, double *lse)
+{
+    if (P <= 0 || rows < 0 || D <= 0)
+        return 1;
+    for (long long r = 0; r < rows; ++r) {
+        double m = -INFINITY;
+        for (long long p = 0; p < P; ++p)
+            if (lse_parts[p * rows + r] > m)
+                m = lse_parts[p * rows + r];
+        double *o = out + r * D;
+        for (long long d = 0; d < D; ++d)
+            o[d] = 0.0;
+        if (m == -INFINITY) {
+            lse[r] = -INFINITY;
+            continue;
+        }
+        double l = 0.0;
+        for (long long p = 0; p < P; ++p)
+            if (lse_parts[p * rows + r] != -INFINITY)
+                l += exp(lse_parts[p * rows + r] - m);
+        const double total = m + log(l);
+        lse[r] = total;
+        for (long long p = 0; p < P; ++p) {
+            const double lp = lse_parts[p * rows + r];
+            if (lp == -INFINITY)
+                continue;
+            const double w = exp(lp - total);
+            for (long long d = 0; d < D; ++d)
+                o[d] += w * orc_widen(o_parts[(p * rows + r) * D + d], dtype);
+        }
+    }
+    return 0;
+}
