@@ -191,18 +191,23 @@ def run_gpu(args, rank, world, local_rank):
     if sampler:
         sampler.start()
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(sim.PHASES) + 1)] for _ in range(args.steps)]
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # Inputs smaller than L2 would stay cached from one step to the next:
+    # then a buffer larger than L2 is written between steps (outside the
+    # timed spans, which are the per-step event pairs).
+    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = sim.x.numel() * sim.x.element_size() < 2 * l2_bytes
+    scrub = torch.empty(4 * l2_bytes, dtype=torch.uint8, device=dev) if flush else None
     barrier()
-    t0.record(stream)
     for i in range(args.steps):
+        if scrub is not None:
+            scrub.fill_(i & 0xff)
         timed_step(evs[i])
-    t1.record(stream)
     barrier()
     clocks = sampler.stop() if sampler else None
     st = ctx.ctx_device_status(stream)
     if st != 0:
         raise RuntimeError(f"device status after timed steps: {ctx.ctx_status_string(st)}")
-    total_ms = t0.elapsed_time(t1)
+    total_ms = sum(ev[0].elapsed_time(ev[-1]) for ev in evs)
     parts = {name: [ev[i].elapsed_time(ev[i + 1]) for ev in evs] for i, name in enumerate(sim.PHASES)}
     total_ms = max_over_ranks(total_ms, world, dev)
 
@@ -232,6 +237,7 @@ def run_gpu(args, rank, world, local_rank):
                "h2d_bytes_per_step": host_x.numel() * host_x.element_size(),
                "d2h_bytes_per_step": host_y.numel() * host_y.element_size(),
                "ms_per_step": round(e2e_ms / args.steps, 4)}
+    sim.l2_flushed = flush
     return sim, inp, total_ms, parts, clocks, e2e
 
 
@@ -254,6 +260,10 @@ def cpu_baseline_sample(wl_name: str, seconds: float, seed: int = 1234):
     oracle.unpack_qkv(st, U)
     relayout_s = time.perf_counter() - t
     relayout_bytes = 2 * 2 * st.nbytes
+    if not wl.attention:
+        gbs = relayout_bytes / relayout_s / 1e9
+        return {"value": round(gbs, 3), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+                "sample": f"layout of one rank: {gbs:.2f} GB/s", "relayout_gbs": round(gbs, 3)}
     # attention: head group 0, gathered K/V, query rows of every rank
     h_l = wl.h_l
     q = u16(inp.q[:, :, :h_l])
@@ -344,6 +354,78 @@ def run_reference(args, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_merge_bench(args):
+    """--kernel lse_merge: the log-sum-exp merge of two key-segment attention
+    outputs of the Wan-like 480p layer (8 ranks batched: [2, 1, 32760, 12, 128])."""
+    import numpy as np
+    import torch
+
+    import workloads
+    import diffusion_transformer_context_gb300 as ctx
+
+    P, B, Sq, H, D = 2, 1, 32760, 12, 128
+    gen = torch.Generator().manual_seed(workloads.SEED)
+    o_host = workloads.randn((P, B, Sq, H, D), gen)
+    l_host = torch.randn((P, B, H, Sq), generator=gen) * 3 + 10
+    o, lse_p = o_host.cuda(), l_host.cuda()
+    out = torch.empty((B, Sq, H, D), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, H, Sq), dtype=torch.float32, device="cuda")
+    rows = B * Sq * H
+    nbytes = P * rows * D * 2 + P * rows * 4 + rows * D * 2 + rows * 4
+    for _ in range(args.warmup):
+        ctx.ctx_lse_merge(o, lse_p, out, lse)
+    torch.cuda.synchronize()
+    sampler = None if args.no_clocks else ClockSampler(0)
+    if sampler:
+        sampler.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        ctx.ctx_lse_merge(o, lse_p, out, lse)
+    e1.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    ms = e0.elapsed_time(e1) / args.steps
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    # e2e: parts in from pinned host memory, merged output back
+    oh, lh = o_host.pin_memory(), l_host.pin_memory()
+    outh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    e0.record()
+    for _ in range(args.steps):
+        o.copy_(oh, non_blocking=True)
+        lse_p.copy_(lh, non_blocking=True)
+        ctx.ctx_lse_merge(o, lse_p, out, lse)
+        outh.copy_(out, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    peaks, kind = load_peaks()
+    line = {"metric": "LSE merge of key-segment attention outputs, GB/s & % HBM", "value": round(gbs, 1),
+            "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "lse_merge", "P": P, "B": B, "Sq": Sq, "H": H, "D": D,
+                       "l2": "inputs_larger_than_l2"},
+            "roofline": {"bound": "hbm", "kernel": "lse_merge_kernel", "achieved": round(gbs, 1),
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                         "peak_source": f"{kind} hbm_gbs", "algorithmic_bytes_per_launch": nbytes,
+                         "traffic": None},
+            "gpu_launches": args.steps, "clocks": clocks,
+            "e2e": {"value": round(nbytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                    "h2d_bytes_per_step": oh.numel() * 2 + lh.numel() * 4,
+                    "d2h_bytes_per_step": outh.numel() * 2, "ms_per_step": round(e2e_ms, 4)}}
+    if not args.no_cpu_baseline:
+        import oracle
+        n = 4096  # rows of the sample
+        ou = workloads.as_u16(o_host[:, :, :n // H])
+        t = time.perf_counter()
+        oracle.lse_merge(ou, l_host[:, :, :, :n // H].double().numpy())
+        dt = time.perf_counter() - t
+        sample_bytes = nbytes * (n // H) / Sq
+        line["cpu_baseline"] = {"value": round(sample_bytes / dt / 1e9, 3), "unit": "GB/s", "cores": 1,
+                                "kind": "oracle", "sample": f"first {n // H} query rows of every head"}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -356,6 +438,7 @@ def main():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--unbalanced", action="store_true", help="attention without workspace: one CTA per unit")
     ap.add_argument("--eager", action="store_true", help="launch every kernel from Python instead of CUDA graphs")
+    ap.add_argument("--kernel", default=None, choices=["lse_merge"], help="time one kernel alone")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=64)
     args = ap.parse_args()
@@ -369,6 +452,10 @@ def main():
     if args.impl == "reference":
         run_reference(args, rank)
         return
+    if args.kernel == "lse_merge":
+        if rank == 0:
+            run_merge_bench(args)
+        return
 
     import torch
     import torch.distributed as dist
@@ -380,46 +467,54 @@ def main():
     K = args.steps
     attn_flops = sim.attn_flops(inp.text_len)
     ms_step = total_ms / K
-    value = whole_job_tflops(attn_flops, world, ms_step)
 
     def avg(x):
         return sum(x) / len(x)
 
-    attn_ms = avg(parts["attend"])
-    tflops = attn_flops / (attn_ms * 1e-3) / 1e12 if attn_ms > 0 else 0.0
-    peak_tf = peaks["bf16_tflops"]
     relayout_bytes = sim.pack_bytes() + sim.a2a_bytes() + sim.unpack_bytes()
     relayout_ms = avg(parts["exchange_in"])
     relayout_gbs = relayout_bytes / (relayout_ms * 1e-3) / 1e9
     reverse_ms = avg(parts["exchange_out"])
-    traffic = recorded_traffic(args.workload)
-
-    line = {
-        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": args.workload, "B": sim.wl.B, "S": sim.wl.S, "H": sim.wl.H, "D": sim.wl.D,
-                   "U": sim.wl.U, "A": sim.wl.A, "joint": sim.wl.joint, "virtual_ranks": sim.R,
-                   "attn_call": f"B'={sim.wl.U * sim.wl.B} Sq={sim.wl.S} Sk={sim.Sk} H={sim.h_l} D={sim.wl.D}",
-                   "l2": "inputs_larger_than_l2", "parallelism": f"replicas{world}",
-                   "attn_schedule": "one CTA per unit" if sim.ws is None else "persistent, key-split tail",
-                   "launch": "eager" if args.eager else "cuda graphs (one per phase)"},
-        "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel", "achieved": round(tflops, 2),
-                     "peak": peak_tf, "unit": "TFLOP/s", "frac": round(tflops / peak_tf, 4),
-                     "peak_source": f"{peak_kind} bf16_tflops (burst)",
-                     "algorithmic_flops_per_launch": attn_flops, "launch_ms": round(attn_ms, 4),
-                     "traffic": traffic},
-        "relayout": {"bound": "hbm", "what": "pack + all-to-all + unpack of all ranks",
-                     "achieved": round(relayout_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(relayout_gbs / peaks["hbm_gbs"], 4), "ms": round(relayout_ms, 4),
-                     "algorithmic_bytes": relayout_bytes,
-                     "reverse_ms": round(reverse_ms, 4), "reverse_bytes": sim.reverse_bytes()},
-        "gpu_launches": sim.launches_per_step() * K,
-        "clocks": clocks,
-        "e2e": e2e,
-    }
+    relayout = {"bound": "hbm", "kernel": "relayout_kernel (pack + all-to-all + unpack of all ranks)",
+                "achieved": round(relayout_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(relayout_gbs / peaks["hbm_gbs"], 4), "peak_source": f"{peak_kind} hbm_gbs",
+                "ms": round(relayout_ms, 4), "algorithmic_bytes": relayout_bytes,
+                "reverse_ms": round(reverse_ms, 4), "reverse_bytes": sim.reverse_bytes(), "traffic": None}
+    config = {"workload": args.workload, "B": sim.wl.B, "S": sim.wl.S, "H": sim.wl.H, "D": sim.wl.D,
+              "U": sim.wl.U, "A": sim.wl.A, "joint": sim.wl.joint, "virtual_ranks": sim.R,
+              "l2": "flushed_between_steps" if sim.l2_flushed else "inputs_larger_than_l2",
+              "parallelism": f"replicas{world}",
+              "launch": "eager" if args.eager else "cuda graphs (one per phase)"}
+    line = {"metric": METRIC, "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": config}
+    if sim.attention:
+        attn_ms = avg(parts["attend"])
+        tflops = attn_flops / (attn_ms * 1e-3) / 1e12 if attn_ms > 0 else 0.0
+        peak_tf = peaks["bf16_tflops"]
+        config["attn_call"] = f"B'={sim.wl.U * sim.wl.B} Sq={sim.wl.S} Sk={sim.Sk} H={sim.h_l} D={sim.wl.D}"
+        config["attn_schedule"] = "one CTA per unit" if sim.ws is None else "persistent, key-split tail"
+        line.update({"value": round(whole_job_tflops(attn_flops, world, ms_step), 3), "unit": "TFLOP/s",
+                     "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel", "achieved": round(tflops, 2),
+                                  "peak": peak_tf, "unit": "TFLOP/s", "frac": round(tflops / peak_tf, 4),
+                                  "peak_source": f"{peak_kind} bf16_tflops (burst)",
+                                  "algorithmic_flops_per_launch": attn_flops, "launch_ms": round(attn_ms, 4),
+                                  "traffic": recorded_traffic(args.workload)},
+                     "relayout": relayout})
+    else:
+        # layout-only workload: the metric is the pack/unpack bandwidth
+        line.update({"value": round(world * relayout_bytes / (ms_step * 1e-3) / 1e9, 1), "unit": "GB/s",
+                     "roofline": relayout})
+        if e2e is not None:
+            e2e["value"] = round(world * relayout_bytes / (e2e["ms_per_step"] * 1e-3) / 1e9, 1)
+            e2e["unit"] = "GB/s"
+    line.update({"gpu_launches": sim.launches_per_step() * K, "clocks": clocks, "e2e": e2e})
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_sample(args.workload, args.cpu_seconds)
+        cb = cpu_baseline_sample(args.workload, args.cpu_seconds)
+        if not sim.attention:
+            cb = {"value": cb["relayout_gbs"], "unit": "GB/s", "cores": cb["cores"], "kind": "oracle",
+                  "sample": cb["sample"].split("; ")[-1]}
+        line["cpu_baseline"] = cb
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

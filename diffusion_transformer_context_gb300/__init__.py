@@ -34,6 +34,7 @@ SIGNATURES = {
     "ctx_attn_lq_gkv_noalloc": (_I, [_P, _P, _P, _P, _F, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "ctx_pack_out": (_I, [_P, _P, _LL, _I, _I, _I, _I, _I, _I, _P]),
     "ctx_unpack_out": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "ctx_lse_merge": (_I, [_P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P]),
     "ctx_status_string": (ctypes.c_char_p, [_I]),
     "ctx_device_status": (_I, [_P]),
     "ctx_last_cuda_error": (_I, []),
@@ -181,6 +182,14 @@ def ctx_unpack_out(recv, y, U: int, stream=None):
     _check("ctx_unpack_out", lib().ctx_unpack_out(_ptr(recv), _ptr(y), B, S_l, h_l, D, U, _dtype(recv),
                                                   _stream(stream)))
     return y
+
+
+def ctx_lse_merge(o_parts, lse_parts, out, lse=None, stream=None):
+    """o_parts [P,B,Sq,H,D], lse_parts [P,B,H,Sq] fp32 -> out [B,Sq,H,D], lse [B,H,Sq] (optional)."""
+    P, B, Sq, H, D = o_parts.shape
+    _check("ctx_lse_merge", lib().ctx_lse_merge(_ptr(o_parts), _ptr(lse_parts), P, _ptr(out), _ptr(lse), B, Sq, H,
+                                                D, _dtype(o_parts), _stream(stream)))
+    return out
 
 
 def ctx_device_status(stream=None) -> int:

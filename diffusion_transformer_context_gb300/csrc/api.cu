@@ -415,6 +415,43 @@ long long ctx_attn_lq_gkv_workspace_size(int B, int Sq, int Sk, int H, int D)
     return bytes;
 }
 
+ctx_status ctx_lse_merge(const void *o_parts, const float *lse_parts, int P, void *out, float *lse, int B, int Sq,
+                         int H, int D, ctx_dtype dtype, void *stream)
+{
+    if (!o_parts || !lse_parts || !out || !valid_dtype(dtype))
+        return CTX_ERR_INVALID_ARG;
+    long long rows = 1;
+    if (P <= 0 || !mul_ok(rows, B) || !mul_ok(rows, Sq) || !mul_ok(rows, H) || D <= 0)
+        return CTX_ERR_INVALID_ARG;
+    long long parts = rows;
+    if (!mul_ok(parts, P) || !mul_ok(parts, D))
+        return CTX_ERR_INVALID_ARG;
+    if (D % 8 != 0 || !aligned16(o_parts) || !aligned16(out) || (reinterpret_cast<uintptr_t>(lse_parts) & 3u) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return CTX_ERR_MISALIGNED;
+    const Extent eo = extent(out, rows * D * 2), eop = extent(o_parts, parts * 2);
+    const Extent elp = extent(lse_parts, rows * P * 4);
+    const Extent el = lse ? extent(lse, rows * 4) : Extent{0, 0};
+    if (overlap(eo, eop) || overlap(eo, elp) || overlap(el, eop) || overlap(el, elp) || overlap(el, eo))
+        return CTX_ERR_ALIASING;
+    ctx_status s = check_device_ptrs({o_parts, lse_parts, out, lse});
+    if (s != CTX_OK)
+        return s;
+    ctx::LseMergeArgs a{};
+    a.o_parts = o_parts;
+    a.lse_parts = lse_parts;
+    a.P = P;
+    a.out = out;
+    a.lse = lse;
+    a.B = B;
+    a.Sq = Sq;
+    a.H = H;
+    a.D = D;
+    a.bf16 = dtype == CTX_BF16;
+    cudaError_t e = ctx::launch_lse_merge(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CTX_OK : cuda_fail(e);
+}
+
 ctx_status ctx_device_status(void *stream)
 {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));

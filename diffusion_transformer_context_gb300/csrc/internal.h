@@ -61,6 +61,18 @@ long long attention_workspace_size(int B, int Sq, int Sk, int H, int D, cudaErro
 
 cudaError_t launch_selftest_wait(unsigned long long limit_ns, cudaStream_t stream);
 
+struct LseMergeArgs {
+    const void *o_parts;     // [P, B, Sq, H, D]
+    const float *lse_parts;  // [P, B, H, Sq]
+    int P;
+    void *out;               // [B, Sq, H, D]
+    float *lse;              // NULL or [B, H, Sq]
+    int B, Sq, H, D;
+    bool bf16;
+};
+
+cudaError_t launch_lse_merge(const LseMergeArgs &a, cudaStream_t stream);
+
 // Records a CUDA error for ctx_last_cuda_error() on the calling thread.
 void record_cuda_error(cudaError_t e);
 

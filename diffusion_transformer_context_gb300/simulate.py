@@ -144,6 +144,8 @@ class SimLayer:
         for name in self.PHASES:
             if name == "exchange_out" and (not self.attention or self.wl.U == 1):
                 continue  # the identity: nothing to launch
+            if name == "attend" and not self.attention:
+                continue
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
                 getattr(self, name)()

@@ -223,6 +223,27 @@ ctx_status ctx_pack_out(const void *o, void *send, long long o_batch_stride_rows
 ctx_status ctx_unpack_out(const void *recv, void *y, int B, int S_l, int h_l,
                           int D, int U, ctx_dtype dtype, void *stream);
 
+/*
+ * ctx_lse_merge — combines attention results computed over P disjoint key
+ * segments (ring / segmented K/V; the merge interface that consumes an LSE,
+ * ChituDiffusion "Fast CP" page, Attention Planner notes). For every row:
+ *
+ *   lse[b,h,i]   = ln sum_p exp(lse_parts[p,b,h,i])
+ *   out[b,i,h,:] = sum_p exp(lse_parts[p,b,h,i] - lse[b,h,i]) * o_parts[p,b,i,h,:]
+ *
+ * Segments with lse = -inf (no valid key) contribute nothing; a row whose
+ * segments are all empty gets out = 0 and lse = -inf. The result equals
+ * attention over all keys up to the rounding of the parts.
+ *
+ * o_parts   : [P, B, Sq, H, D] device, dtype (e.g. P outputs of ctx_attn_lq_gkv).
+ * lse_parts : [P, B, H, Sq] float32 device (their LSEs).
+ * out       : [B, Sq, H, D] device, dtype.   lse : NULL or [B, H, Sq] float32.
+ * Arithmetic in fp32, out rounded to nearest even. D a multiple of 8.
+ */
+ctx_status ctx_lse_merge(const void *o_parts, const float *lse_parts, int P,
+                         void *out, float *lse, int B, int Sq, int H, int D,
+                         ctx_dtype dtype, void *stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *ctx_status_string(ctx_status status);
 

@@ -133,3 +133,13 @@ def test_product_path_has_no_oracle_or_fallback():
                 src = open(os.path.join(dirpath, fn)).read()
                 assert "import oracle" not in src and "from oracle" not in src, fn
                 assert "ctx_oracle" not in src, fn
+
+
+def test_lse_merge_validation(lib):
+    f = lib.ctx_lse_merge
+    o, l, out, lo = A0, A0 + 8 * MB, A0 + 16 * MB, A0 + 24 * MB
+    assert f(o, l, 0, out, lo, 1, 4, 2, 8, 0, None) == INVALID          # P = 0
+    assert f(o, l, 2, out, lo, 1, 4, 2, 12, 0, None) == MISALIGNED     # D % 8
+    assert f(o + 8, l, 2, out, lo, 1, 4, 2, 8, 0, None) == MISALIGNED
+    assert f(o, l, 2, o + 16, lo, 1, 4, 2, 8, 0, None) == ALIASING      # out inside the parts
+    assert f(o, l, 2, out, l, 1, 4, 2, 8, 0, None) == ALIASING          # lse over lse_parts
