@@ -74,6 +74,11 @@ def _load():
                       lib.orc_unpack_out, lib.orc_attention_rows, lib.orc_attention_probs):
                 f.restype = ctypes.c_int
             lib.orc_lse_merge.argtypes = [p, p, ctypes.c_int, ll, ll, ll, p, p]
+            lib.orc_pack_qkv_ex.argtypes = [p, p, p, p, ll, ll, ll, ll, ll, ctypes.c_int]
+            lib.orc_unpack_qkv_ex.argtypes = [p, p, p, p, ll, ll, ll, ll, ll, ctypes.c_int]
+            lib.orc_unpack_out_ex.argtypes = [p, p, ll, ll, ll, ll, ll, ll]
+            for f in (lib.orc_pack_qkv_ex, lib.orc_unpack_qkv_ex, lib.orc_unpack_out_ex):
+                f.restype = ctypes.c_int
             lib.orc_lse_merge.restype = ctypes.c_int
             lib.orc_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -138,6 +143,44 @@ def unpack_out(recv, U: int) -> np.ndarray:
     assert U2 == U
     out = np.empty((B, S_l, U * h_l, D), dtype=np.uint16)
     assert _load().orc_unpack_out(_ptr(recv), _ptr(out), B, S_l, h_l, D, U) == 0
+    return out
+
+
+LAYOUT_TQKV, LAYOUT_INTERLEAVED = 0, 1
+
+
+def pack_qkv_ex(q, k, v, U: int, layout: int = LAYOUT_TQKV) -> np.ndarray:
+    """Pack with zero-padded heads (h_l = ceil(H/U)) and a choice of staging
+    layout: 0 -> [U,3,B,S_l,h_l,D], 1 -> [U,B,S_l,h_l,3D]."""
+    q, k, v = _u16(q), _u16(k), _u16(v)
+    B, S_l, H, D = q.shape
+    h_l = -(-H // U)
+    shape = (U, 3, B, S_l, h_l, D) if layout == LAYOUT_TQKV else (U, B, S_l, h_l, 3 * D)
+    out = np.empty(shape, dtype=np.uint16)
+    assert _load().orc_pack_qkv_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, S_l, H, D, U, layout) == 0
+    return out
+
+
+def unpack_qkv_ex(recv, U: int, layout: int = LAYOUT_TQKV):
+    """Receive side for either layout -> (Q', K', V') each [B, U*S_l, h_l, D]."""
+    recv = _u16(recv)
+    if layout == LAYOUT_TQKV:
+        U2, three, B, S_l, h_l, D = recv.shape
+    else:
+        U2, B, S_l, h_l, D3 = recv.shape
+        D = D3 // 3
+    assert U2 == U
+    outs = [np.empty((B, U * S_l, h_l, D), dtype=np.uint16) for _ in range(3)]
+    assert _load().orc_unpack_qkv_ex(_ptr(recv), *(_ptr(o) for o in outs), B, S_l, h_l, D, U, layout) == 0
+    return tuple(outs)
+
+
+def unpack_out_ex(recv, U: int, H: int) -> np.ndarray:
+    """Reverse exchange receive side keeping the first H of the U*h_l heads."""
+    recv = _u16(recv)
+    U2, B, S_l, h_l, D = recv.shape
+    out = np.empty((B, S_l, H, D), dtype=np.uint16)
+    assert _load().orc_unpack_out_ex(_ptr(recv), _ptr(out), B, S_l, h_l, H, D, U) == 0
     return out
 
 

@@ -304,3 +304,75 @@ int orc_lse_merge(const uint16_t *o_parts, const double *lse_parts, int dtype, l
     }
     return 0;
 }
+
+/* Ulysses pack with the general options of the pages:
+ *  - uneven heads (vllm-omni PR #7641, "advanced_uaa" head padding): the H
+ *    heads are padded with zero heads to U*h_l, h_l = ceil(H/U), and
+ *    destination r gets padded heads [r*h_l, (r+1)*h_l);
+ *  - layout 0 = [U][3][B][S_l][h_l][D] (Q, K, V one after the other),
+ *    layout 1 = [U][B][S_l][h_l][3*D] (Q, K, V interleaved on the last
+ *    dimension, the sglang PR #33667 excerpt's staging buffer).
+ * Element (r, t, b, s, h, d) = X_t[b][s][r*h_l + h][d] if r*h_l + h < H, else 0. */
+int orc_pack_qkv_ex(const uint16_t *q, const uint16_t *k, const uint16_t *v, uint16_t *staging,
+                    long long B, long long S_l, long long H, long long D, long long U, int layout)
+{
+    if (U <= 0 || H <= 0 || (layout != 0 && layout != 1))
+        return 1;
+    long long h_l = (H + U - 1) / U;
+    const uint16_t *src[3] = {q, k, v};
+    for (long long r = 0; r < U; ++r)
+        for (long long t = 0; t < 3; ++t)
+            for (long long b = 0; b < B; ++b)
+                for (long long s = 0; s < S_l; ++s)
+                    for (long long h = 0; h < h_l; ++h)
+                        for (long long d = 0; d < D; ++d) {
+                            long long g = r * h_l + h;
+                            uint16_t val = (g < H) ? src[t][((b * S_l + s) * H + g) * D + d] : 0;
+                            long long dst = layout == 0
+                                                ? ((((r * 3 + t) * B + b) * S_l + s) * h_l + h) * D + d
+                                                : ((((r * B + b) * S_l + s) * h_l + h) * 3 + t) * D + d;
+                            staging[dst] = val;
+                        }
+    return 0;
+}
+
+/* Receive side for either staging layout: X'_t[b][r*S_l + s][h][d]. */
+int orc_unpack_qkv_ex(const uint16_t *recv, uint16_t *q, uint16_t *k, uint16_t *v, long long B,
+                      long long S_l, long long h_l, long long D, long long U, int layout)
+{
+    if (U <= 0 || (layout != 0 && layout != 1))
+        return 1;
+    uint16_t *dst[3] = {q, k, v};
+    for (long long r = 0; r < U; ++r)
+        for (long long t = 0; t < 3; ++t)
+            for (long long b = 0; b < B; ++b)
+                for (long long s = 0; s < S_l; ++s)
+                    for (long long h = 0; h < h_l; ++h)
+                        for (long long d = 0; d < D; ++d) {
+                            long long from = layout == 0
+                                                 ? ((((r * 3 + t) * B + b) * S_l + s) * h_l + h) * D + d
+                                                 : ((((r * B + b) * S_l + s) * h_l + h) * 3 + t) * D + d;
+                            dst[t][((b * (U * S_l) + (r * S_l + s)) * h_l + h) * D + d] = recv[from];
+                        }
+    return 0;
+}
+
+/* Reverse exchange receive side that drops padded heads:
+ * Y[b][s][r*h_l + h][d] = recv[r][b][s][h][d] for r*h_l + h < H. */
+int orc_unpack_out_ex(const uint16_t *recv, uint16_t *y, long long B, long long S_l, long long h_l,
+                      long long H, long long D, long long U)
+{
+    if (U <= 0 || H > U * h_l)
+        return 1;
+    for (long long r = 0; r < U; ++r)
+        for (long long b = 0; b < B; ++b)
+            for (long long s = 0; s < S_l; ++s)
+                for (long long h = 0; h < h_l; ++h) {
+                    long long g = r * h_l + h;
+                    if (g >= H)
+                        continue;
+                    for (long long d = 0; d < D; ++d)
+                        y[((b * S_l + s) * H + g) * D + d] = recv[(((r * B + b) * S_l + s) * h_l + h) * D + d];
+                }
+    return 0;
+}
