@@ -22,12 +22,16 @@ CTX_OK = 0
 STATUS_NAMES = {0: "CTX_OK", 1: "CTX_ERR_INVALID_ARG", 2: "CTX_ERR_UNSUPPORTED", 3: "CTX_ERR_MISALIGNED",
                 4: "CTX_ERR_ALIASING", 5: "CTX_ERR_CUDA", 6: "CTX_ERR_TIMEOUT"}
 CTX_BF16, CTX_FP16 = 0, 1
+CTX_LAYOUT_TQKV, CTX_LAYOUT_INTERLEAVED = 0, 1
 
 # Every symbol include/ctx.h declares, with (restype, argtypes).
 _P, _I, _LL, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_float
 SIGNATURES = {
     "ctx_pack_qkv": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "ctx_sim_all_to_all": (_I, [_P, _P, _I, _I, _LL, _P]),
+    "ctx_pack_qkv_ex": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]),
+    "ctx_unpack_qkv_ex": (_I, [_P, _P, _P, _P, _LL, _LL, _I, _I, _I, _I, _I, _I, _I, _P]),
+    "ctx_unpack_out_ex": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _P]),
     "ctx_unpack_qkv": (_I, [_P, _P, _P, _P, _LL, _LL, _I, _I, _I, _I, _I, _I, _P]),
     "ctx_attn_lq_gkv": (_I, [_P, _P, _P, _P, _F, _P, _P, _P, _LL, _I, _I, _I, _I, _I, _I, _P]),
     "ctx_attn_lq_gkv_workspace_size": (_LL, [_I, _I, _I, _I, _I]),
@@ -102,6 +106,32 @@ def ctx_pack_qkv(q, k, v, staging, U: int, stream=None):
     _check("ctx_pack_qkv", lib().ctx_pack_qkv(_ptr(q), _ptr(k), _ptr(v), _ptr(staging), B, S_l, H, D, U,
                                               _dtype(q), _stream(stream)))
     return staging
+
+
+def ctx_pack_qkv_ex(q, k, v, staging, U: int, layout: int = CTX_LAYOUT_TQKV, stream=None):
+    """q, k, v [B,S_l,H,D] (H % U allowed: zero-padded heads) -> staging in `layout`."""
+    B, S_l, H, D = q.shape
+    _check("ctx_pack_qkv_ex", lib().ctx_pack_qkv_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(staging), B, S_l, H, D, U,
+                                                    layout, _dtype(q), _stream(stream)))
+    return staging
+
+
+def ctx_unpack_qkv_ex(recv, q, k, v, U: int, B: int, S_l: int, h_l: int, D: int, layout: int = CTX_LAYOUT_TQKV,
+                      q_batch_stride_rows: int | None = None, kv_batch_stride_rows: int | None = None, stream=None):
+    """recv in `layout` -> q, k, v bases of [B, stride_rows, h_l, D] buffers."""
+    qs = U * S_l if q_batch_stride_rows is None else q_batch_stride_rows
+    ks = U * S_l if kv_batch_stride_rows is None else kv_batch_stride_rows
+    _check("ctx_unpack_qkv_ex", lib().ctx_unpack_qkv_ex(_ptr(recv), _ptr(q), _ptr(k), _ptr(v), qs, ks, B, S_l, h_l,
+                                                        D, U, layout, _dtype(recv), _stream(stream)))
+
+
+def ctx_unpack_out_ex(recv, y, U: int, stream=None):
+    """recv [U,B,S_l,h_l,D] -> y [B,S_l,H,D] keeping the first H = y.shape[2] heads."""
+    U2, B, S_l, h_l, D = recv.shape
+    H = y.shape[2]
+    _check("ctx_unpack_out_ex", lib().ctx_unpack_out_ex(_ptr(recv), _ptr(y), B, S_l, h_l, H, D, U, _dtype(recv),
+                                                        _stream(stream)))
+    return y
 
 
 def ctx_sim_all_to_all(send, recv, G: int, U: int, stream=None):

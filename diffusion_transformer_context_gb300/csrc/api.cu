@@ -336,6 +336,127 @@ ctx_status ctx_unpack_out(const void *recv, void *y, int B, int S_l, int h_l, in
     return run_relayout(RelayoutMode::UnpackOut, a, stream);
 }
 
+ctx_status ctx_pack_qkv_ex(const void *q, const void *k, const void *v, void *staging, int B, int S_l, int H, int D,
+                           int U, ctx_layout layout, ctx_dtype dtype, void *stream)
+{
+    if (!q || !k || !v || !staging || !valid_dtype(dtype) ||
+        (layout != CTX_LAYOUT_TQKV && layout != CTX_LAYOUT_INTERLEAVED))
+        return CTX_ERR_INVALID_ARG;
+    long long n = 1;
+    if (!mul_ok(n, B) || !mul_ok(n, S_l) || !mul_ok(n, H) || !mul_ok(n, D) || U <= 0)
+        return CTX_ERR_INVALID_ARG;
+    const long long h_l = (static_cast<long long>(H) + U - 1) / U;
+    long long ns = static_cast<long long>(B) * S_l;
+    if (!mul_ok(ns, h_l) || !mul_ok(ns, U) || !mul_ok(ns, 3) || !mul_ok(ns, D))
+        return CTX_ERR_INVALID_ARG;
+    if (D % 8 != 0 || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(staging))
+        return CTX_ERR_MISALIGNED;
+    const Extent st = extent(staging, ns * 2);
+    if (overlap(st, extent(q, n * 2)) || overlap(st, extent(k, n * 2)) || overlap(st, extent(v, n * 2)))
+        return CTX_ERR_ALIASING;
+    ctx_status s = check_device_ptrs({q, k, v, staging});
+    if (s != CTX_OK)
+        return s;
+    RelayoutArgs a{};
+    a.src0 = q;
+    a.src1 = k;
+    a.src2 = v;
+    a.dst0 = staging;
+    a.B = B;
+    a.S_l = S_l;
+    a.H = U * h_l;
+    a.H_real = H;
+    a.U = U;
+    a.h_l = h_l;
+    if (layout == CTX_LAYOUT_TQKV) {
+        a.run_vec = h_l * D / 8;
+        a.n_runs = 3LL * U * B * S_l;
+        return run_relayout(H % U == 0 ? RelayoutMode::PackQKV : RelayoutMode::PackQKVPad, a, stream);
+    }
+    a.run_vec = D / 8;
+    a.n_runs = static_cast<long long>(U) * B * S_l * h_l;
+    return run_relayout(RelayoutMode::PackInter, a, stream);
+}
+
+ctx_status ctx_unpack_qkv_ex(const void *recv, void *q, void *k, void *v, long long q_batch_stride_rows,
+                             long long kv_batch_stride_rows, int B, int S_l, int h_l, int D, int U, ctx_layout layout,
+                             ctx_dtype dtype, void *stream)
+{
+    if (layout == CTX_LAYOUT_TQKV)
+        return ctx_unpack_qkv(recv, q, k, v, q_batch_stride_rows, kv_batch_stride_rows, B, S_l, h_l, D, U, dtype,
+                              stream);
+    if (layout != CTX_LAYOUT_INTERLEAVED || !recv || !q || !k || !v || !valid_dtype(dtype))
+        return CTX_ERR_INVALID_ARG;
+    long long n = 1;
+    if (!mul_ok(n, B) || !mul_ok(n, S_l) || !mul_ok(n, h_l) || !mul_ok(n, D) || !mul_ok(n, U))
+        return CTX_ERR_INVALID_ARG;
+    const long long rows = static_cast<long long>(U) * S_l;
+    if (q_batch_stride_rows < rows || kv_batch_stride_rows < rows)
+        return CTX_ERR_INVALID_ARG;
+    const long long row_bytes = static_cast<long long>(h_l) * D * 2;
+    long long qspan = q_batch_stride_rows, kvspan = kv_batch_stride_rows;
+    if (!mul_ok(qspan, B) || !mul_ok(qspan, row_bytes) || !mul_ok(kvspan, B) || !mul_ok(kvspan, row_bytes))
+        return CTX_ERR_INVALID_ARG;
+    if (D % 8 != 0 || !aligned16(recv) || !aligned16(q) || !aligned16(k) || !aligned16(v))
+        return CTX_ERR_MISALIGNED;
+    const long long q_bytes = ((static_cast<long long>(B) - 1) * q_batch_stride_rows + rows) * row_bytes;
+    const long long kv_bytes = ((static_cast<long long>(B) - 1) * kv_batch_stride_rows + rows) * row_bytes;
+    const Extent r = extent(recv, 3 * n * 2);
+    const Extent eq = extent(q, q_bytes), ek = extent(k, kv_bytes), ev = extent(v, kv_bytes);
+    if (overlap(r, eq) || overlap(r, ek) || overlap(r, ev) || overlap(eq, ek) || overlap(eq, ev) ||
+        overlap(ek, ev))
+        return CTX_ERR_ALIASING;
+    ctx_status s = check_device_ptrs({recv, q, k, v});
+    if (s != CTX_OK)
+        return s;
+    RelayoutArgs a{};
+    a.src0 = recv;
+    a.dst0 = q;
+    a.dst1 = k;
+    a.dst2 = v;
+    a.B = B;
+    a.S_l = S_l;
+    a.h_l = h_l;
+    a.U = U;
+    a.q_batch_stride_rows = q_batch_stride_rows;
+    a.kv_batch_stride_rows = kv_batch_stride_rows;
+    a.run_vec = D / 8;
+    a.n_runs = static_cast<long long>(U) * B * S_l * h_l;
+    return run_relayout(RelayoutMode::UnpackInter, a, stream);
+}
+
+ctx_status ctx_unpack_out_ex(const void *recv, void *y, int B, int S_l, int h_l, int H, int D, int U, ctx_dtype dtype,
+                             void *stream)
+{
+    if (!recv || !y || !valid_dtype(dtype))
+        return CTX_ERR_INVALID_ARG;
+    long long n = 1;
+    if (!mul_ok(n, B) || !mul_ok(n, S_l) || !mul_ok(n, h_l) || !mul_ok(n, D) || !mul_ok(n, U) || H <= 0 ||
+        static_cast<long long>(H) > static_cast<long long>(U) * h_l)
+        return CTX_ERR_INVALID_ARG;
+    if (H == U * h_l)
+        return ctx_unpack_out(recv, y, B, S_l, h_l, D, U, dtype, stream);
+    if (D % 8 != 0 || !aligned16(recv) || !aligned16(y))
+        return CTX_ERR_MISALIGNED;
+    const long long y_bytes = static_cast<long long>(B) * S_l * H * D * 2;
+    if (overlap(extent(recv, n * 2), extent(y, y_bytes)))
+        return CTX_ERR_ALIASING;
+    ctx_status s = check_device_ptrs({recv, y});
+    if (s != CTX_OK)
+        return s;
+    RelayoutArgs a{};
+    a.src0 = recv;
+    a.dst0 = y;
+    a.B = B;
+    a.S_l = S_l;
+    a.h_l = h_l;
+    a.H_real = H;
+    a.U = U;
+    a.run_vec = static_cast<long long>(h_l) * D / 8;
+    a.n_runs = static_cast<long long>(U) * B * S_l;
+    return run_relayout(RelayoutMode::UnpackOutPad, a, stream);
+}
+
 ctx_status ctx_attn_lq_gkv(const void *q, const void *k, const void *v, const unsigned char *key_mask, float scale,
                            void *out, float *lse, void *workspace, long long workspace_bytes, int B, int Sq, int Sk,
                            int H, int D, ctx_dtype dtype, void *stream)

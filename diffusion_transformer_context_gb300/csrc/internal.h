@@ -20,7 +20,17 @@ int *device_status_word(cudaError_t *err);
 // Number of SMs of the current device (cached per device).
 int sm_count(cudaError_t *err);
 
-enum class RelayoutMode : int { PackQKV = 0, UnpackQKV = 1, PackOut = 2, UnpackOut = 3, AllToAll = 4 };
+enum class RelayoutMode : int {
+    PackQKV = 0,
+    UnpackQKV = 1,
+    PackOut = 2,
+    UnpackOut = 3,
+    AllToAll = 4,
+    PackQKVPad = 5,    // heads padded with zeros to U*h_l
+    UnpackOutPad = 6,  // keeps the first H of the U*h_l heads
+    PackInter = 7,     // interleaved staging [U][B][S_l][h_l][3][D] (cells of 3*D)
+    UnpackInter = 8,
+};
 
 // Every relayout step moves "runs": contiguous groups of 16-byte vectors that
 // are contiguous in both source and destination. The mode maps a run index to
@@ -36,6 +46,7 @@ struct RelayoutArgs {
     long long run_vec;  // 16-byte vectors per run
     // shape parameters (meaning depends on the mode)
     long long B, S_l, H, h_l, U, G;
+    long long H_real;                // padded modes: heads that exist (< U*h_l)
     long long q_batch_stride_rows;   // unpack: Q' batch stride; pack_out: O batch stride
     long long kv_batch_stride_rows;  // unpack: K'/V' batch stride
 };

@@ -26,11 +26,15 @@ __device__ __forceinline__ uint4 ld_stream(const uint4 *p)
 }
 
 // Source and destination of run `run` (in 16-byte vectors). rv = run length;
-// a row of H heads is U runs long (H*D/8 = U*rv).
+// a row of H heads is U runs long (H*D/8 = U*rv). `valid` is the number of
+// vectors of the run that exist in the source (padded modes): the pack
+// zero-fills the rest, the padded reverse exchange skips it.
 template <RelayoutMode M>
-__device__ __forceinline__ void map_run(const RelayoutArgs &a, long long run, const uint4 *&src, uint4 *&dst)
+__device__ __forceinline__ void map_run(const RelayoutArgs &a, long long run, const uint4 *&src, uint4 *&dst,
+                                        long long &valid)
 {
     const long long rv = a.run_vec;
+    valid = rv;
     if constexpr (M == RelayoutMode::PackQKV) {
         // run = ((r*3 + t)*B + b)*S_l + s  (destination order)
         long long s = run % a.S_l, x = run / a.S_l;
@@ -39,6 +43,18 @@ __device__ __forceinline__ void map_run(const RelayoutArgs &a, long long run, co
         long long t = x % 3, r = x / 3;
         const uint4 *base = static_cast<const uint4 *>(t == 0 ? a.src0 : (t == 1 ? a.src1 : a.src2));
         src = base + ((b * a.S_l + s) * a.U + r) * rv;
+        dst = static_cast<uint4 *>(a.dst0) + run * rv;
+    } else if constexpr (M == RelayoutMode::PackQKVPad) {
+        // as PackQKV over U*h_l padded heads; the source rows hold H_real heads
+        long long s = run % a.S_l, x = run / a.S_l;
+        long long b = x % a.B;
+        x /= a.B;
+        long long t = x % 3, r = x / 3;
+        const long long dv = rv / a.h_l;  // vectors per head
+        const long long heads = min(max(a.H_real - r * a.h_l, 0LL), a.h_l);
+        valid = heads * dv;
+        const uint4 *base = static_cast<const uint4 *>(t == 0 ? a.src0 : (t == 1 ? a.src1 : a.src2));
+        src = base + ((b * a.S_l + s) * a.H_real + r * a.h_l) * dv;
         dst = static_cast<uint4 *>(a.dst0) + run * rv;
     } else if constexpr (M == RelayoutMode::UnpackQKV) {
         // run = ((r*3 + t)*B + b)*S_l + s  (source order)
@@ -62,6 +78,15 @@ __device__ __forceinline__ void map_run(const RelayoutArgs &a, long long run, co
         long long b = x % a.B, r = x / a.B;
         src = static_cast<const uint4 *>(a.src0) + run * rv;
         dst = static_cast<uint4 *>(a.dst0) + ((b * a.S_l + s) * a.U + r) * rv;
+    } else if constexpr (M == RelayoutMode::UnpackOutPad) {
+        // as UnpackOut; destination rows hold H_real heads, pad heads are dropped
+        long long s = run % a.S_l, x = run / a.S_l;
+        long long b = x % a.B, r = x / a.B;
+        const long long dv = rv / a.h_l;
+        const long long heads = min(max(a.H_real - r * a.h_l, 0LL), a.h_l);
+        valid = heads * dv;
+        src = static_cast<const uint4 *>(a.src0) + run * rv;
+        dst = static_cast<uint4 *>(a.dst0) + ((b * a.S_l + s) * a.H_real + r * a.h_l) * dv;
     } else {
         // AllToAll: run = (g*U + r)*U + j (source order) -> recv[g][j][r]
         long long j = run % a.U, x = run / a.U;
@@ -75,6 +100,7 @@ template <RelayoutMode M, int VPL>
 __global__ void __launch_bounds__(256) relayout_kernel(RelayoutArgs a, long long n_items, int n_segs)
 {
     constexpr long long kSegVec = 32LL * VPL;
+    constexpr bool kZeroFill = (M == RelayoutMode::PackQKVPad);
     const int lane = threadIdx.x & 31;
     const long long warp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const long long n_warps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
@@ -86,21 +112,60 @@ __global__ void __launch_bounds__(256) relayout_kernel(RelayoutArgs a, long long
         }
         const uint4 *src;
         uint4 *dst;
-        map_run<M>(a, run, src, dst);
+        long long valid;
+        map_run<M>(a, run, src, dst, valid);
         const long long base = seg * kSegVec;
         const long long lim = min(a.run_vec - base, kSegVec);
+        const long long vlim = min(valid - base, kSegVec);
         uint4 buf[VPL];
 #pragma unroll
         for (int i = 0; i < VPL; ++i) {
             const long long c = lane + 32 * i;
-            if (c < lim)
+            if (c < vlim)
                 buf[i] = ld_stream(src + base + c);
+            else
+                buf[i] = make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int i = 0; i < VPL; ++i) {
             const long long c = lane + 32 * i;
-            if (c < lim)
+            if (c < vlim || (kZeroFill && c < lim))
                 dst[base + c] = buf[i];
+        }
+    }
+}
+
+// Interleaved staging layout: a cell (r, b, s, h) holds the 3*D elements
+// Q | K | V of padded head r*h_l + h; one warp moves one cell, each lane a
+// 16-byte vector of it.
+template <bool kPack>
+__global__ void __launch_bounds__(256) relayout_inter_kernel(RelayoutArgs a, long long n_cells)
+{
+    const int lane = threadIdx.x & 31;
+    const long long warp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const long long n_warps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+    const long long dv = a.run_vec;  // vectors per head (D/8)
+    for (long long cell = warp; cell < n_cells; cell += n_warps) {
+        // cell = ((r*B + b)*S_l + s)*h_l + h
+        long long h = cell % a.h_l, x = cell / a.h_l;
+        long long s = x % a.S_l;
+        x /= a.S_l;
+        long long b = x % a.B, r = x / a.B;
+        const long long g = r * a.h_l + h;
+        for (long long c = lane; c < 3 * dv; c += 32) {
+            const long long t = c / dv, cc = c - t * dv;
+            if constexpr (kPack) {
+                const uint4 *base = static_cast<const uint4 *>(t == 0 ? a.src0 : (t == 1 ? a.src1 : a.src2));
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (g < a.H_real)
+                    v = ld_stream(base + ((b * a.S_l + s) * a.H_real + g) * dv + cc);
+                static_cast<uint4 *>(a.dst0)[cell * 3 * dv + c] = v;
+            } else {
+                uint4 *base = static_cast<uint4 *>(t == 0 ? a.dst0 : (t == 1 ? a.dst1 : a.dst2));
+                const long long stride = t == 0 ? a.q_batch_stride_rows : a.kv_batch_stride_rows;
+                base[((b * stride + r * a.S_l + s) * a.h_l + h) * dv + cc] =
+                    ld_stream(static_cast<const uint4 *>(a.src0) + cell * 3 * dv + c);
+            }
         }
     }
 }
@@ -166,6 +231,24 @@ cudaError_t launch_relayout(RelayoutMode mode, const RelayoutArgs &a, cudaStream
     case RelayoutMode::PackOut: return launch_mode<RelayoutMode::PackOut>(a, stream);
     case RelayoutMode::UnpackOut: return launch_mode<RelayoutMode::UnpackOut>(a, stream);
     case RelayoutMode::AllToAll: return launch_mode<RelayoutMode::AllToAll>(a, stream);
+    case RelayoutMode::PackQKVPad: return launch_mode<RelayoutMode::PackQKVPad>(a, stream);
+    case RelayoutMode::UnpackOutPad: return launch_mode<RelayoutMode::UnpackOutPad>(a, stream);
+    case RelayoutMode::PackInter:
+    case RelayoutMode::UnpackInter: {
+        if (a.n_runs == 0)
+            return cudaSuccess;
+        cudaError_t err = cudaSuccess;
+        const int sms = sm_count(&err);
+        if (err != cudaSuccess)
+            return err;
+        const long long want = (a.n_runs + 7) / 8;
+        const unsigned grid = static_cast<unsigned>(std::max(1LL, std::min(want, 8LL * sms)));
+        if (mode == RelayoutMode::PackInter)
+            relayout_inter_kernel<true><<<grid, 256, 0, stream>>>(a, a.n_runs);
+        else
+            relayout_inter_kernel<false><<<grid, 256, 0, stream>>>(a, a.n_runs);
+        return cudaGetLastError();
+    }
     }
     return cudaErrorInvalidValue;
 }

@@ -4,10 +4,11 @@ Rank g = a*U + u (vllm-omni PR #7641: Ulysses groups are contiguous blocks of
 U ranks, AllGather-KV groups stride by U) holds input rows [g*S_l, (g+1)*S_l)
 of Q, K, V [B, S, H, D]. One step runs, through the C ABI only:
 
-  1. ctx_pack_qkv for every rank into its staging buffer;
+  1. ctx_pack_qkv_ex for every rank into its staging buffer (heads that do
+     not divide by U are zero-padded, either staging layout);
   2. ctx_sim_all_to_all inside every U group (skipped at U = 1, where the
      exchange is the identity);
-  3. ctx_unpack_qkv for every rank, writing its local Q rows into the
+  3. ctx_unpack_qkv_ex for every rank, writing its local Q rows into the
      all-ranks query buffer and its K/V rows straight into the gathered K/V
      buffer of its head group at rows [a*S/A, (a+1)*S/A): the K/V AllGather is
      this placement, no bytes are copied for it;
@@ -16,7 +17,7 @@ of Q, K, V [B, S, H, D]. One step runs, through the C ABI only:
      per u, batched over u (rows are independent, so this equals one launch
      per rank);
   5. the reverse exchange ctx_pack_out -> ctx_sim_all_to_all ->
-     ctx_unpack_out for every rank (at U = 1 the output rows already are the
+     ctx_unpack_out_ex for every rank (at U = 1 the output rows already are the
      sequence-sharded result and step 5 is the identity).
 
 Joint (text) keys and values are inputs every rank already holds; they are
@@ -29,20 +30,23 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (attn_workspace, ctx_attn_lq_gkv, ctx_pack_out, ctx_pack_qkv, ctx_sim_all_to_all, ctx_unpack_out,
-               ctx_unpack_qkv)
+from . import (CTX_LAYOUT_TQKV, attn_workspace, ctx_attn_lq_gkv, ctx_pack_out, ctx_pack_qkv_ex,
+               ctx_sim_all_to_all, ctx_unpack_out_ex, ctx_unpack_qkv_ex)
 
 
 class SimLayer:
     def __init__(self, wl, device="cuda", dtype=torch.bfloat16, attention: bool | None = None,
-                 balanced: bool = True):
+                 balanced: bool = True, layout: int = CTX_LAYOUT_TQKV):
         self.wl = wl
         self.dev = torch.device(device)
         self.dtype = dtype
+        self.layout = layout
         U, A, B, S, H, D, J = wl.U, wl.A, wl.B, wl.S, wl.H, wl.D, wl.joint
-        if S % (U * A) or H % U:
-            raise ValueError("S must divide by U*A and H by U")
-        self.R, self.S_l, self.h_l, self.Sk = U * A, S // (U * A), H // U, S + J
+        if S % (U * A):
+            raise ValueError("S must divide by U*A")
+        # heads that do not divide by U are zero-padded to U * ceil(H/U)
+        self.R, self.S_l, self.h_l, self.Sk = U * A, S // (U * A), -(-H // U), S + J
+        self.H_pad = U * self.h_l
         self.attention = wl.attention if attention is None else attention
         R, S_l, h_l, Sk = self.R, self.S_l, self.h_l, self.Sk
         kw = dict(dtype=dtype, device=self.dev)
@@ -72,10 +76,14 @@ class SimLayer:
             for t, src in enumerate((inp.q, inp.k, inp.v)):
                 self.x[g, t].copy_(inp.shard(src, g))
         if wl.joint:
-            S, h_l = wl.S, self.h_l
+            S, h_l, H = wl.S, self.h_l, wl.H
             for u in range(U):
-                self.kg[u, :, S:].copy_(inp.jk[:, :, u * h_l:(u + 1) * h_l])
-                self.vg[u, :, S:].copy_(inp.jv[:, :, u * h_l:(u + 1) * h_l])
+                lo, hi = u * h_l, min((u + 1) * h_l, H)
+                self.kg[u, :, S:].zero_()
+                self.vg[u, :, S:].zero_()
+                if hi > lo:
+                    self.kg[u, :, S:, :hi - lo].copy_(inp.jk[:, :, lo:hi])
+                    self.vg[u, :, S:, :hi - lo].copy_(inp.jv[:, :, lo:hi])
             m = inp.key_mask()
             if m is not None:
                 self.mask.copy_(torch.from_numpy(np.tile(m, (U, 1))))
@@ -90,14 +98,15 @@ class SimLayer:
         for g in range(self.R):
             a, u = divmod(g, U)
             x = self.x[g]
-            ctx_pack_qkv(x[0], x[1], x[2], self.send[a, u], U, stream=stream)
+            ctx_pack_qkv_ex(x[0], x[1], x[2], self.send[a, u], U, self.layout, stream=stream)
         if U > 1:
             ctx_sim_all_to_all(self.send, self.recv, A, U, stream=stream)
         for g in range(self.R):
             a, u = divmod(g, U)
             r0 = a * U * S_l
-            ctx_unpack_qkv(self.recv[a, u].view(U, 3, B, S_l, h_l, D), self.qg[u, :, r0:], self.kg[u, :, r0:],
-                           self.vg[u, :, r0:], U, q_batch_stride_rows=S, kv_batch_stride_rows=Sk, stream=stream)
+            ctx_unpack_qkv_ex(self.recv[a, u], self.qg[u, :, r0:], self.kg[u, :, r0:], self.vg[u, :, r0:], U, B,
+                              S_l, h_l, D, self.layout, q_batch_stride_rows=S, kv_batch_stride_rows=Sk,
+                              stream=stream)
 
     def attend(self, stream=None):
         """Step 4: local-Q / global-KV attention of every rank."""
@@ -124,7 +133,7 @@ class SimLayer:
         ctx_sim_all_to_all(self.osend, self.orecv, A, U, stream=stream)
         for g in range(self.R):
             a, u = divmod(g, U)
-            ctx_unpack_out(self.orecv[a, u].view(U, B, S_l, h_l, D), self.y[g], U, stream=stream)
+            ctx_unpack_out_ex(self.orecv[a, u].view(U, B, S_l, h_l, D), self.y[g], U, stream=stream)
 
     PHASES = ("exchange_in", "attend", "exchange_out")
 
@@ -170,7 +179,7 @@ class SimLayer:
         """Rank g's sequence-sharded attention output [B, S_l, H, D]."""
         if self.wl.U > 1:
             return self.y[g]
-        return self.out[0, :, g * self.S_l:(g + 1) * self.S_l]
+        return self.out[0, :, g * self.S_l:(g + 1) * self.S_l, :self.wl.H]
 
     def rank_q(self, g: int) -> torch.Tensor:
         a, u = divmod(g, self.wl.U)
@@ -179,22 +188,25 @@ class SimLayer:
 
     # ---------------------------------------------------------- work model
     def pack_bytes(self) -> int:
-        """Algorithmic HBM bytes (read + write) of all packs of one step."""
+        """Algorithmic HBM bytes of all packs of one step: the real heads read,
+        the padded heads written."""
         wl = self.wl
-        return 2 * 3 * self.R * wl.B * self.S_l * wl.H * wl.D * 2
+        return 3 * self.R * wl.B * self.S_l * (wl.H + self.H_pad) * wl.D * 2
 
     def unpack_bytes(self) -> int:
-        return self.pack_bytes()
+        wl = self.wl
+        return 2 * 3 * self.R * wl.B * self.S_l * self.H_pad * wl.D * 2
 
     def a2a_bytes(self) -> int:
-        return self.pack_bytes() if self.wl.U > 1 else 0
+        return self.unpack_bytes() if self.wl.U > 1 else 0
 
     def reverse_bytes(self) -> int:
         wl = self.wl
         if not self.attention or wl.U == 1:
             return 0
-        one = 2 * self.R * wl.B * self.S_l * wl.H * wl.D * 2  # one pass, read + write
-        return 3 * one  # pack_out, all-to-all, unpack_out
+        one = self.R * wl.B * self.S_l * self.H_pad * wl.D * 2
+        # pack_out and all-to-all read + write padded rows; unpack_out reads padded, writes real heads
+        return 2 * one + 2 * one + one + self.R * wl.B * self.S_l * wl.H * wl.D * 2
 
     def attn_flops(self, text_len=None, dense: bool = False) -> float:
         """4 * Sq * K_valid * D per head (QK^T and PV), summed over all ranks."""
@@ -207,4 +219,5 @@ class SimLayer:
             if not dense and wl.joint and text_len is not None:
                 kv = wl.S + int(text_len[b])
             per_b.append(kv)
-        return float(sum(4.0 * wl.U * self.h_l * wl.S * kv * wl.D for kv in per_b))
+        # useful work: the real heads (padded heads are overhead, not counted)
+        return float(sum(4.0 * wl.H * wl.S * kv * wl.D for kv in per_b))

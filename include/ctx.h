@@ -63,6 +63,12 @@ typedef enum ctx_status {
 
 typedef enum ctx_dtype { CTX_BF16 = 0, CTX_FP16 = 1 } ctx_dtype;
 
+/* Staging layouts of the Ulysses exchange (destination-major either way). */
+typedef enum ctx_layout {
+    CTX_LAYOUT_TQKV = 0,        /* [U][3][B][S_l][h_l][D]: Q, K, V one after another */
+    CTX_LAYOUT_INTERLEAVED = 1  /* [U][B][S_l][h_l][3*D]: Q|K|V per head (sglang PR #33667 excerpt) */
+} ctx_layout;
+
 /*
  * ctx_pack_qkv — Ulysses send-side relayout (sglang PR #33667, implementation
  * items 2-3 and the _usp_input_all_to_all_qkv excerpt: one kernel writes Q, K
@@ -121,6 +127,40 @@ ctx_status ctx_unpack_qkv(const void *recv, void *q, void *k, void *v,
                           long long q_batch_stride_rows,
                           long long kv_batch_stride_rows, int B, int S_l,
                           int h_l, int D, int U, ctx_dtype dtype, void *stream);
+
+/*
+ * ctx_pack_qkv_ex — ctx_pack_qkv with uneven heads and a choice of layout.
+ * Heads that do not divide by U are padded with zero heads to U*h_l,
+ * h_l = ceil(H/U) (vllm-omni PR #7641, "advanced_uaa" head padding: 14 heads
+ * at U=4 become 16, +14.3 % attention work); destination r gets padded heads
+ * [r*h_l, (r+1)*h_l). layout selects CTX_LAYOUT_TQKV ([U,3,B,S_l,h_l,D], the
+ * layout of ctx_pack_qkv) or CTX_LAYOUT_INTERLEAVED ([U,B,S_l,h_l,3D]).
+ * q, k, v: [B, S_l, H, D]. Errors as ctx_pack_qkv (H % U is allowed).
+ */
+ctx_status ctx_pack_qkv_ex(const void *q, const void *k, const void *v,
+                           void *staging, int B, int S_l, int H, int D, int U,
+                           ctx_layout layout, ctx_dtype dtype, void *stream);
+
+/*
+ * ctx_unpack_qkv_ex — ctx_unpack_qkv for either staging layout; recv is
+ * [U,3,B,S_l,h_l,D] (TQKV) or [U,B,S_l,h_l,3D] (INTERLEAVED). Outputs and
+ * strides as ctx_unpack_qkv (h_l counts padded heads).
+ */
+ctx_status ctx_unpack_qkv_ex(const void *recv, void *q, void *k, void *v,
+                             long long q_batch_stride_rows,
+                             long long kv_batch_stride_rows, int B, int S_l,
+                             int h_l, int D, int U, ctx_layout layout,
+                             ctx_dtype dtype, void *stream);
+
+/*
+ * ctx_unpack_out_ex — ctx_unpack_out that drops padded heads: keeps the first
+ * H of the U*h_l received heads (H <= U*h_l).
+ *   y[b][s][r*h_l + h][d] = recv[r][b][s][h][d]   for r*h_l + h < H
+ * recv : [U, B, S_l, h_l, D].   y : [B, S_l, H, D].
+ */
+ctx_status ctx_unpack_out_ex(const void *recv, void *y, int B, int S_l,
+                             int h_l, int H, int D, int U, ctx_dtype dtype,
+                             void *stream);
 
 /*
  * ctx_attn_lq_gkv — local-Q / global-KV attention forward (vllm-omni PR

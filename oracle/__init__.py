@@ -263,12 +263,22 @@ def attention_probs(q, k, b, h, i, mask=None, scale=None, dtype="bf16") -> np.nd
 
 # ------------------------------------------------------ composed pipeline
 
+def _pad_heads(x, H_pad):
+    B, S, H, D = x.shape
+    if H == H_pad:
+        return x
+    out = np.zeros((B, S, H_pad, D), np.uint16)
+    out[:, :, :H] = x
+    return out
+
+
 def ulysses_agkv_forward(q_shards, k_shards, v_shards, U: int, A: int,
-                         jk=None, jv=None):
+                         jk=None, jv=None, layout: int = LAYOUT_TQKV):
     """The composed U x A input side, all ranks (vllm-omni PR #7641 order):
     Ulysses all-to-all inside each U group (ranks a*U .. a*U+U-1), then the
     K/V AllGather inside each A group (ranks u, U+u, ...), then the joint
-    (text) K/V appended after the gathered image keys.
+    (text) K/V appended after the gathered image keys. Heads that do not
+    divide by U are zero-padded to U*ceil(H/U).
 
     Inputs are per-rank [B,S_l,H,D] uint16 shards indexed by g = a*U + u.
     Returns dict with, per rank g: 'q' [B,S/A,h_l,D] local-Q, and per head
@@ -276,13 +286,14 @@ def ulysses_agkv_forward(q_shards, k_shards, v_shards, U: int, A: int,
     """
     R = U * A
     assert len(q_shards) == R
-    staging = [pack_qkv(q_shards[g], k_shards[g], v_shards[g], U) for g in range(R)]
+    H = q_shards[0].shape[2]
+    staging = [pack_qkv_ex(q_shards[g], k_shards[g], v_shards[g], U, layout) for g in range(R)]
     loc = [None] * R
     for a in range(A):
         grp = [a * U + u for u in range(U)]
         recvs = all_to_all([staging[g] for g in grp])
         for u, g in enumerate(grp):
-            loc[g] = unpack_qkv(recvs[u], U)
+            loc[g] = unpack_qkv_ex(recvs[u], U, layout)
     res = {"q": [loc[g][0] for g in range(R)], "k": [], "v": []}
     for u in range(U):
         grp = [a * U + u for a in range(A)]
@@ -290,16 +301,18 @@ def ulysses_agkv_forward(q_shards, k_shards, v_shards, U: int, A: int,
         vg = all_gather([loc[g][2] for g in grp])
         if jk is not None:
             h_l = kg.shape[2]
-            kg = np.concatenate([kg, np.ascontiguousarray(jk[:, :, u * h_l:(u + 1) * h_l])], axis=1)
-            vg = np.concatenate([vg, np.ascontiguousarray(jv[:, :, u * h_l:(u + 1) * h_l])], axis=1)
+            jkp, jvp = _pad_heads(jk, U * h_l), _pad_heads(jv, U * h_l)
+            kg = np.concatenate([kg, np.ascontiguousarray(jkp[:, :, u * h_l:(u + 1) * h_l])], axis=1)
+            vg = np.concatenate([vg, np.ascontiguousarray(jvp[:, :, u * h_l:(u + 1) * h_l])], axis=1)
         res["k"].append(kg)
         res["v"].append(vg)
     return res
 
 
-def ulysses_reverse(o_ranks, U: int, A: int):
+def ulysses_reverse(o_ranks, U: int, A: int, H: int | None = None):
     """Reverse Ulysses exchange for all ranks: o_ranks[g] is rank g's output
-    [B, S/A, h_l, D]; returns per-rank [B, S_l, H, D] sequence-sharded outputs."""
+    [B, S/A, h_l, D]; returns per-rank [B, S_l, H, D] sequence-sharded
+    outputs (padded heads beyond H dropped)."""
     R = U * A
     sends = [pack_out(o_ranks[g], U) for g in range(R)]
     out = [None] * R
@@ -307,7 +320,7 @@ def ulysses_reverse(o_ranks, U: int, A: int):
         grp = [a * U + u for u in range(U)]
         recvs = all_to_all([sends[g] for g in grp])
         for u, g in enumerate(grp):
-            out[g] = unpack_out(recvs[u], U)
+            out[g] = unpack_out(recvs[u], U) if H is None else unpack_out_ex(recvs[u], U, H)
     return out
 
 

@@ -25,25 +25,25 @@ def ctx():
     return m
 
 
-def _oracle_side(orc, inp):
+def _oracle_side(orc, inp, layout=0):
     wl = inp.wl
     R = wl.ranks
     sh = [[u16(inp.shard(t, g)) for t in (inp.q, inp.k, inp.v)] for g in range(R)]
     jk = u16(inp.jk) if inp.jk is not None else None
     jv = u16(inp.jv) if inp.jv is not None else None
     return orc.ulysses_agkv_forward([s[0] for s in sh], [s[1] for s in sh], [s[2] for s in sh],
-                                    wl.U, wl.A, jk, jv)
+                                    wl.U, wl.A, jk, jv, layout)
 
 
-def _check_layer(ctx, orc, wl, n_rows=None):
+def _check_layer(ctx, orc, wl, n_rows=None, layout=0):
     from diffusion_transformer_context_gb300.simulate import SimLayer
     inp = workloads.make_inputs(wl)
-    sim = SimLayer(wl)
+    sim = SimLayer(wl, layout=layout)
     sim.load(inp)
     sim.step()
     st = ctx.ctx_device_status()
     assert st == 0, ctx.ctx_status_string(st)
-    res = _oracle_side(orc, inp)
+    res = _oracle_side(orc, inp, layout)
     U, A = wl.U, wl.A
     # layout steps: bit-exact
     for u in range(U):
@@ -83,7 +83,7 @@ def _check_layer(ctx, orc, wl, n_rows=None):
     # reverse exchange of the GPU's own output: bit-exact
     o_ranks = [u16(sim.out[u][:, a * rows_per_rank:(a + 1) * rows_per_rank])
                for a in range(A) for u in range(U)]
-    back = orc.ulysses_reverse(o_ranks, U, A)
+    back = orc.ulysses_reverse(o_ranks, U, A, wl.H)
     for g in range(wl.ranks):
         assert np.array_equal(u16(sim.rank_output(g)), back[g]), f"reverse rank {g}"
 
@@ -104,6 +104,25 @@ def test_pack_workload(ctx, orc):
 ], ids=lambda w: w.name)
 def test_composed_small(ctx, orc, wl):
     _check_layer(ctx, orc, wl)
+
+
+@pytest.mark.parametrize("wl", [
+    workloads.custom("uaa_u4_h14", B=1, S=1024, H=14, D=128, U=4, A=1),
+    workloads.custom("uaa_u4a2_h14_joint", B=2, S=512, H=14, D=64, U=4, A=2, joint=32, text_len_range=(1, 32)),
+    workloads.custom("uaa_u3_h7", B=1, S=384, H=7, D=128, U=3, A=1),
+], ids=lambda w: w.name)
+def test_uneven_heads(ctx, orc, wl):
+    """H % U != 0: heads zero-padded to U*ceil(H/U) (vllm-omni "advanced_uaa")."""
+    _check_layer(ctx, orc, wl)
+
+
+@pytest.mark.parametrize("wl", [
+    workloads.WORKLOADS["tiny"],
+    workloads.custom("inter_u4a2", B=2, S=512, H=8, D=128, U=4, A=2),
+    workloads.custom("inter_u4_h14", B=1, S=512, H=14, D=64, U=4, A=1),
+], ids=lambda w: w.name)
+def test_interleaved_staging_layout(ctx, orc, wl):
+    _check_layer(ctx, orc, wl, layout=1)
 
 
 def test_qwen_layer(ctx, orc):

@@ -133,3 +133,32 @@ def test_host_pointer_is_rejected(ctx):
     with pytest.raises(ctx.CtxError) as e:
         ctx.ctx_pack_qkv(q, q.clone().pin_memory(), q.clone().pin_memory(), st, 2)
     assert e.value.status == 1
+
+
+@pytest.mark.parametrize("layout", [0, 1])
+@pytest.mark.parametrize("B,S_l,H,D,U", [(1, 16, 14, 128, 4), (2, 5, 7, 64, 3), (1, 9, 8, 128, 4), (1, 3, 3, 8, 2)])
+def test_pack_ex_bit_exact(ctx, orc, B, S_l, H, D, U, layout):
+    gen = torch.Generator().manual_seed(71)
+    q, k, v = (_bits((B, S_l, H, D), gen) for _ in range(3))
+    h_l = -(-H // U)
+    shape = (U, 3, B, S_l, h_l, D) if layout == 0 else (U, B, S_l, h_l, 3 * D)
+    st = Guarded(shape, torch.bfloat16)
+    ctx.ctx_pack_qkv_ex(q.cuda(), k.cuda(), v.cuda(), st.t, U, layout)
+    torch.cuda.synchronize()
+    expect = orc.pack_qkv_ex(u16(q), u16(k), u16(v), U, layout)
+    assert st.intact() and np.array_equal(u16(st.t), expect)
+    outs = [Guarded((B, U * S_l, h_l, D), torch.bfloat16) for _ in range(3)]
+    ctx.ctx_unpack_qkv_ex(st.t, outs[0].t, outs[1].t, outs[2].t, U, B, S_l, h_l, D, layout)
+    torch.cuda.synchronize()
+    for o, e in zip(outs, orc.unpack_qkv_ex(expect, U, layout)):
+        assert o.intact() and np.array_equal(u16(o.t), e)
+
+
+@pytest.mark.parametrize("B,S_l,h_l,H,D,U", [(1, 16, 4, 14, 128, 4), (2, 5, 3, 7, 64, 3), (1, 4, 2, 8, 8, 4)])
+def test_unpack_out_ex_drops_pad_heads(ctx, orc, B, S_l, h_l, H, D, U):
+    gen = torch.Generator().manual_seed(72)
+    recv = _bits((U, B, S_l, h_l, D), gen)
+    y = Guarded((B, S_l, H, D), torch.bfloat16)
+    ctx.ctx_unpack_out_ex(recv.cuda(), y.t, U)
+    torch.cuda.synchronize()
+    assert y.intact() and np.array_equal(u16(y.t), orc.unpack_out_ex(u16(recv), U, H))

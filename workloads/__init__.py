@@ -95,6 +95,11 @@ WORKLOADS = {
     # Wan-14B-like 720p, U=4 x A=2: per-rank [1,9450,40,128] -> [1,37800,10,128],
     # local-Q [1,37800,10,128] vs K/V [1,75600,10,128]
     "wan14b": Workload("wan14b", B=1, S=75600, H=40, D=128, U=4, A=2),
+    # the vllm-omni PR #7641 topology comparison on 4 GPUs: 14 heads, D=128,
+    # sequence 65536; Ulysses-4 pads 14 -> 16 heads ("advanced_uaa"),
+    # Ulysses-2 x AllGather-2 divides evenly
+    "uaa14_usp4": Workload("uaa14_usp4", B=1, S=65536, H=14, D=128, U=4, A=1),
+    "uaa14_cp2usp2": Workload("uaa14_cp2usp2", B=1, S=65536, H=14, D=128, U=2, A=2),
 }
 
 
