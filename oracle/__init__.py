@@ -341,6 +341,53 @@ def lse_merge(o_parts, lse_parts, dtype="bf16"):
     return out.reshape(B, H, Sq, D).transpose(0, 2, 1, 3).copy(), lse.reshape(B, H, Sq)
 
 
+# ------------------------------------------------ packed varlen metadata
+
+def varlen_remap(cu_global, span_begin: int, span_len: int):
+    """Local query boundaries of one rank (vllm-omni PR #7641, packed query
+    metadata under AllGather-KV): every global document [cu[d], cu[d+1]) is
+    intersected with the rank's span [span_begin, span_begin + span_len); the
+    rank keeps one (possibly empty) entry per document, prefix-summed from 0."""
+    cu = [int(x) for x in cu_global]
+    out = [0]
+    lo, hi = span_begin, span_begin + span_len
+    for d in range(len(cu) - 1):
+        a, b = max(cu[d], lo), min(cu[d + 1], hi)
+        out.append(out[-1] + max(0, b - a))
+    return np.array(out, dtype=np.int32)
+
+
+def padding_remap(real: int, pad: int, span_begin: int, span_len: int):
+    """The single-document [real, pad] view of one rank: the query length
+    narrows to the rank's valid prefix (the key length stays global)."""
+    local_real = min(max(real - span_begin, 0), span_len)
+    return np.array([local_real, span_len - local_real], dtype=np.int32)
+
+
+def attention_varlen(q, k, v, cu_q, cu_k, mask=None, scale=None, dtype="bf16"):
+    """Packed varlen attention: q [Sq,H,D], k/v [Sk,H,D]; query rows of
+    document d (rows [cu_q[d], cu_q[d+1])) attend keys [cu_k[d], cu_k[d+1]).
+    mask: None or [Sk] (nonzero = attend). Returns O [Sq,H,D] (rows outside
+    every document stay NaN) and LSE [H,Sq]."""
+    Sq, H, D = q.shape
+    O = np.full((Sq, H, D), np.nan)
+    L = np.full((H, Sq), np.nan)
+    for d in range(len(cu_q) - 1):
+        q0, q1, k0, k1 = int(cu_q[d]), int(cu_q[d + 1]), int(cu_k[d]), int(cu_k[d + 1])
+        if q1 <= q0:
+            continue
+        if k1 <= k0:
+            O[q0:q1] = 0.0
+            L[:, q0:q1] = -np.inf
+            continue
+        m = None if mask is None else np.ascontiguousarray(mask[k0:k1])[None]
+        o, l = attention(np.ascontiguousarray(q[None, q0:q1]), np.ascontiguousarray(k[None, k0:k1]),
+                         np.ascontiguousarray(v[None, k0:k1]), m, scale, dtype)
+        O[q0:q1] = o[0]
+        L[:, q0:q1] = l[0]
+    return O, L
+
+
 # ------------------------------------------------------- pure-Python twins
 
 def _widen_py(x: int, dtype: str) -> float:
