@@ -39,6 +39,8 @@ SIGNATURES = {
     "ctx_pack_out": (_I, [_P, _P, _LL, _I, _I, _I, _I, _I, _I, _P]),
     "ctx_unpack_out": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "ctx_lse_merge": (_I, [_P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "ctx_varlen_remap": (_I, [_P, _I, _LL, _LL, _P, _P, _P, _P]),
+    "ctx_attn_varlen": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _F, _P, _P, _I, _I, _I, _I, _I, _P]),
     "ctx_status_string": (ctypes.c_char_p, [_I]),
     "ctx_device_status": (_I, [_P]),
     "ctx_last_cuda_error": (_I, []),
@@ -219,6 +221,29 @@ def ctx_lse_merge(o_parts, lse_parts, out, lse=None, stream=None):
     P, B, Sq, H, D = o_parts.shape
     _check("ctx_lse_merge", lib().ctx_lse_merge(_ptr(o_parts), _ptr(lse_parts), P, _ptr(out), _ptr(lse), B, Sq, H,
                                                 D, _dtype(o_parts), _stream(stream)))
+    return out
+
+
+def ctx_varlen_remap(cu_seqlens_q, span_begin: int, span_len: int, cu_seqlens_q_local, packed_padding=None,
+                     packed_padding_local=None, stream=None):
+    """int32 device tensors: [n_docs+1] global -> [n_docs+1] local boundaries of one rank."""
+    n_docs = cu_seqlens_q.numel() - 1
+    _check("ctx_varlen_remap", lib().ctx_varlen_remap(_ptr(cu_seqlens_q), n_docs, span_begin, span_len,
+                                                      _ptr(cu_seqlens_q_local), _ptr(packed_padding),
+                                                      _ptr(packed_padding_local), _stream(stream)))
+    return cu_seqlens_q_local
+
+
+def ctx_attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, out, lse=None, key_mask=None,
+                    scale: float | None = None, stream=None):
+    """q [Sq,H,D], k/v [Sk,H,D], int32 cu tensors [n_docs+1] -> out [Sq,H,D], lse [H,Sq]."""
+    Sq, H, D = q.shape
+    Sk = k.shape[0]
+    s = float("nan") if scale is None else float(scale)
+    _check("ctx_attn_varlen", lib().ctx_attn_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q),
+                                                    _ptr(cu_seqlens_k), cu_seqlens_q.numel() - 1, max_seqlen_q,
+                                                    _ptr(key_mask), s, _ptr(out), _ptr(lse), Sq, Sk, H, D,
+                                                    _dtype(q), _stream(stream)))
     return out
 
 

@@ -536,6 +536,90 @@ long long ctx_attn_lq_gkv_workspace_size(int B, int Sq, int Sk, int H, int D)
     return bytes;
 }
 
+ctx_status ctx_varlen_remap(const int *cu_seqlens_q, int n_docs, long long span_begin, long long span_len,
+                            int *cu_seqlens_q_local, const int *packed_padding, int *packed_padding_local,
+                            void *stream)
+{
+    if (!cu_seqlens_q || !cu_seqlens_q_local || n_docs <= 0 || span_begin < 0 || span_len < 0 ||
+        span_begin + span_len > 0x7fffffffLL || ((packed_padding == nullptr) != (packed_padding_local == nullptr)))
+        return CTX_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) || (reinterpret_cast<uintptr_t>(cu_seqlens_q_local) & 3u) ||
+        (reinterpret_cast<uintptr_t>(packed_padding) & 3u) || (reinterpret_cast<uintptr_t>(packed_padding_local) & 3u))
+        return CTX_ERR_MISALIGNED;
+    const long long cu_bytes = (static_cast<long long>(n_docs) + 1) * 4;
+    const Extent eg = extent(cu_seqlens_q, cu_bytes), el = extent(cu_seqlens_q_local, cu_bytes);
+    const Extent pi = packed_padding ? extent(packed_padding, 8) : Extent{0, 0};
+    const Extent po = packed_padding_local ? extent(packed_padding_local, 8) : Extent{0, 0};
+    if (overlap(eg, el) || overlap(po, eg) || overlap(po, el) || overlap(po, pi) || overlap(el, pi))
+        return CTX_ERR_ALIASING;
+    ctx_status s = check_device_ptrs({cu_seqlens_q, cu_seqlens_q_local, packed_padding, packed_padding_local});
+    if (s != CTX_OK)
+        return s;
+    cudaError_t e = ctx::launch_varlen_remap(cu_seqlens_q, n_docs, span_begin, span_len, cu_seqlens_q_local,
+                                             packed_padding, packed_padding_local, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CTX_OK : cuda_fail(e);
+}
+
+ctx_status ctx_attn_varlen(const void *q, const void *k, const void *v, const int *cu_seqlens_q,
+                           const int *cu_seqlens_k, int n_docs, int max_seqlen_q, const unsigned char *key_mask,
+                           float scale, void *out, float *lse, int Sq, int Sk, int H, int D, ctx_dtype dtype,
+                           void *stream)
+{
+    if (!q || !k || !v || !out || !cu_seqlens_q || !cu_seqlens_k || !valid_dtype(dtype) || n_docs <= 0 ||
+        max_seqlen_q <= 0)
+        return CTX_ERR_INVALID_ARG;
+    long long nq = 1, nk = 1;
+    if (!mul_ok(nq, Sq) || !mul_ok(nq, H) || !mul_ok(nq, D) || !mul_ok(nk, Sk) || !mul_ok(nk, H) || !mul_ok(nk, D))
+        return CTX_ERR_INVALID_ARG;
+    long long units = (static_cast<long long>(max_seqlen_q) + 255) / 256;
+    if (!mul_ok(units, H) || !mul_ok(units, n_docs) || units > 0x7fffffffLL)
+        return CTX_ERR_INVALID_ARG;
+    if (std::isnan(scale))
+        scale = 1.0f / std::sqrt(static_cast<float>(D));
+    if (!std::isfinite(scale) || !(scale > 0.f))
+        return CTX_ERR_INVALID_ARG;
+    if (D % 8 != 0 || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) ||
+        (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u))
+        return CTX_ERR_MISALIGNED;
+    if (D != 64 && D != 128)
+        return CTX_ERR_UNSUPPORTED;
+    const Extent eo = extent(out, nq * 2);
+    const Extent el = lse ? extent(lse, static_cast<long long>(H) * Sq * 4) : Extent{0, 0};
+    const Extent ins[] = {extent(q, nq * 2), extent(k, nk * 2), extent(v, nk * 2),
+                          key_mask ? extent(key_mask, Sk) : Extent{0, 0},
+                          extent(cu_seqlens_q, (static_cast<long long>(n_docs) + 1) * 4),
+                          extent(cu_seqlens_k, (static_cast<long long>(n_docs) + 1) * 4)};
+    for (const Extent &x : ins)
+        if (overlap(eo, x) || overlap(el, x))
+            return CTX_ERR_ALIASING;
+    if (overlap(eo, el))
+        return CTX_ERR_ALIASING;
+    ctx_status s = check_device_ptrs({q, k, v, out, lse, key_mask, cu_seqlens_q, cu_seqlens_k});
+    if (s != CTX_OK)
+        return s;
+    ctx::AttnArgs a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.mask = key_mask;
+    a.out = out;
+    a.lse = lse;
+    a.B = 1;
+    a.Sq = Sq;
+    a.Sk = Sk;
+    a.H = H;
+    a.D = D;
+    a.bf16 = dtype == CTX_BF16;
+    a.scale = scale;
+    a.cu_q = cu_seqlens_q;
+    a.cu_k = cu_seqlens_k;
+    a.n_docs = n_docs;
+    a.max_seqlen_q = max_seqlen_q;
+    cudaError_t e = ctx::launch_attention(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CTX_OK : cuda_fail(e);
+}
+
 ctx_status ctx_lse_merge(const void *o_parts, const float *lse_parts, int P, void *out, float *lse, int B, int Sq,
                          int H, int D, ctx_dtype dtype, void *stream)
 {

@@ -55,7 +55,10 @@ struct Params {
     int B, Sq, Sk, H;
     int n_qpairs;
     int n_kblocks;
-    int n_units;           // work units: (query-tile pair, head, batch)
+    const int *cu_q;       // packed varlen: [n_docs + 1] local query boundaries (device), else NULL
+    const int *cu_k;       // packed varlen: [n_docs + 1] key boundaries (device)
+    int varlen;            // 1: units are (query-tile pair, head, document)
+    int n_units;           // work units: (query-tile pair, head, batch or document)
     int grid;              // persistent CTAs
     int dp_waves;          // whole-unit waves: CTA c takes units c, c+grid, ...
     long long tail_iters;  // key blocks of the remaining units, split evenly over the grid
@@ -92,6 +95,39 @@ struct Segment {
     bool full;
 };
 
+// Geometry of one work unit: 256 query rows [q0, min(q0 + 256, q_end)) of
+// head h and batch b, against keys [k0, k0 + k_len) in key blocks of 128.
+// Packed varlen: the unit's document d gives q0 = cu_q[d] + 256*qp,
+// q_end = cu_q[d+1], keys [cu_k[d], cu_k[d+1]) (vllm-omni PR #7641: local
+// query boundaries, global key boundaries). nblk = 0 means nothing to compute.
+struct Geom {
+    int b, h, q0, q_end, k0, k_len, nblk;
+};
+
+__device__ __forceinline__ void unit_geom(const Params &p, int unit, Geom &g)
+{
+    const int qp = unit % p.n_qpairs, bh = unit / p.n_qpairs;
+    g.h = bh % p.H;
+    const int x = bh / p.H;
+    if (!p.varlen) {
+        g.b = x;
+        g.q0 = qp * (kTiles * kBM);
+        g.q_end = p.Sq;
+        g.k0 = 0;
+        g.k_len = p.Sk;
+    } else {
+        // boundaries are clamped to the tensors, so malformed ones cannot
+        // address memory outside q/out or k/v/mask
+        g.b = 0;
+        const int qs = min(max(__ldg(p.cu_q + x), 0), p.Sq);
+        g.q0 = qs + qp * (kTiles * kBM);
+        g.q_end = min(max(__ldg(p.cu_q + x + 1), qs), p.Sq);
+        g.k0 = min(max(__ldg(p.cu_k + x), 0), p.Sk);
+        g.k_len = min(max(__ldg(p.cu_k + x + 1), g.k0), p.Sk) - g.k0;
+    }
+    g.nblk = (g.q0 < g.q_end && g.k_len > 0) ? (g.k_len + kBN - 1) / kBN : 0;
+}
+
 // Segment `si` of CTA c, computed from its index alone (identical in every
 // warp role, and no iterator state lives across the key-block loops): first
 // the whole-unit waves (concurrent CTAs work on neighbouring units, so they
@@ -103,7 +139,13 @@ __device__ __forceinline__ bool segment_at(const Params &p, int c, int si, Segme
     if (si < p.dp_waves) {
         s.unit = si * p.grid + c;
         s.jb = 0;
-        s.je = p.n_kblocks;
+        if (p.varlen) {
+            Geom g;
+            unit_geom(p, s.unit, g);
+            s.je = g.nblk;  // 0: an empty unit, skipped by every role
+        } else {
+            s.je = p.n_kblocks;
+        }
         s.full = true;
         s.slot = -1;
         return true;
@@ -205,25 +247,6 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint3
     }
 }
 
-// Stores one output row (D values scaled by inv) and its LSE.
-template <int D, bool BF16>
-__device__ __forceinline__ void store_row(const Params &p, int b, int h, int qrow, const float *o, float inv,
-                                          float lse_val)
-{
-    if (qrow >= p.Sq)
-        return;
-    uint4 *orow = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) +
-                                            ((static_cast<size_t>(b) * p.Sq + qrow) * p.H + h) * D);
-#pragma unroll
-    for (int i = 0; i < D / 8; ++i)
-        orow[i] = make_uint4(ptx::pack2<BF16>(o[8 * i + 0] * inv, o[8 * i + 1] * inv),
-                             ptx::pack2<BF16>(o[8 * i + 2] * inv, o[8 * i + 3] * inv),
-                             ptx::pack2<BF16>(o[8 * i + 4] * inv, o[8 * i + 5] * inv),
-                             ptx::pack2<BF16>(o[8 * i + 6] * inv, o[8 * i + 7] * inv));
-    if (p.lse)
-        p.lse[(static_cast<size_t>(b) * p.H + h) * p.Sq + qrow] = lse_val;
-}
-
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -291,23 +314,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tma_prefetch_desc(&tmK);
             ptx::tma_prefetch_desc(&tmV);
             Segment sg;
-            int kv = 0, segi = 0;
+            int kv = 0, act = 0;  // act: segments with work so far (phase of the per-segment barriers)
             int last_k[kStages], last_v[kStages];
             for (int s = 0; s < kStages; ++s)
                 last_k[s] = last_v[s] = -1;
             bool ok = true;
-            while (ok && segment_at(p, cta, segi, sg)) {
-                const int qp = sg.unit % p.n_qpairs, bh = sg.unit / p.n_qpairs;
-                const int h = bh % p.H, b = bh / p.H;
-                const int q0 = qp * (kTiles * kBM);
-                if (segi > 0 && !(ok = wait_bar(q_empty, (segi - 1) & 1, abort_flag, p)))
+            for (int segi = 0; ok && segment_at(p, cta, segi, sg); ++segi) {
+                if (sg.je == sg.jb)
+                    continue;
+                Geom ge;
+                unit_geom(p, sg.unit, ge);
+                const int h = ge.h, b = ge.b;
+                if (act > 0 && !(ok = wait_bar(q_empty, (act - 1) & 1, abort_flag, p)))
                     break;
                 ptx::mbar_arrive_expect_tx(q_full, kTiles * L::kQBytes);
                 for (int t = 0; t < kTiles; ++t)
                     for (int pn = 0; pn < L::kPanels; ++pn)
                         ptx::tma_load_4d(&tmQ, q_full, smem + L::kQOff + t * L::kQBytes + pn * L::kQPanel, pn * 64,
-                                         h, q0 + t * kBM, b);
-                ++segi;
+                                         h, ge.q0 + t * kBM, b);
+                ++act;
                 for (int j = sg.jb; j < sg.je; ++j, ++kv) {
                     const int s = kv % kStages, u = kv / kStages;
                     if (u > 0 && !(ok = wait_bar(k_empty + s, (u - 1) & 1, abort_flag, p)))
@@ -315,20 +340,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mbar_arrive_expect_tx(k_full + s, L::kKVBytes);
                     for (int pn = 0; pn < L::kPanels; ++pn)
                         ptx::tma_load_4d(&tmK, k_full + s, smem + L::kKOff + s * L::kKVBytes + pn * L::kKVPanel,
-                                         pn * 64, h, j * kBN, b);
+                                         pn * 64, h, ge.k0 + j * kBN, b);
                     last_k[s] = u;
                     if (u > 0 && !(ok = wait_bar(v_empty + s, (u - 1) & 1, abort_flag, p)))
                         break;
                     ptx::mbar_arrive_expect_tx(v_full + s, L::kKVBytes);
                     for (int pn = 0; pn < L::kPanels; ++pn)
                         ptx::tma_load_4d(&tmV, v_full + s, smem + L::kVOff + s * L::kKVBytes + pn * L::kKVPanel,
-                                         pn * 64, h, j * kBN, b);
+                                         pn * 64, h, ge.k0 + j * kBN, b);
                     last_v[s] = u;
                 }
             }
             // Drain: every issued load has landed before the CTA can exit.
-            if (segi > 0)
-                wait_bar(q_full, (segi - 1) & 1, abort_flag, p, false);
+            if (act > 0)
+                wait_bar(q_full, (act - 1) & 1, abort_flag, p, false);
             for (int s = 0; s < kStages; ++s) {
                 if (last_k[s] >= 0)
                     wait_bar(k_full + s, last_k[s] & 1, abort_flag, p, false);
@@ -346,11 +371,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t tS0 = tmem, tS1 = tmem + kBN;
             const uint32_t tO0 = tmem + 2 * kBN, tO1 = tmem + 2 * kBN + D;
             Segment sg;
-            int kv = 0, g = 0, segi = 0;
+            int kv = 0, g = 0, act = 0;
             bool ok = true;
-            while (ok && segment_at(p, cta, segi, sg)) {
+            for (int segi = 0; ok && segment_at(p, cta, segi, sg); ++segi) {
                 const int n = sg.je - sg.jb;
-                if (!(ok = wait_bar(q_full, segi & 1, abort_flag, p)))
+                if (n == 0)
+                    continue;
+                if (!(ok = wait_bar(q_full, act & 1, abort_flag, p)))
                     break;
                 ptx::tc_fence_after();
                 for (int i = 0; i < n; ++i) {
@@ -364,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         if (!(ok = wait_bar(p_full + 0, (g + i - 1) & 1, abort_flag, p)))
                             break;
-                        if (i == 1 && segi > 0 && !(ok = wait_bar(o_empty + 0, (segi - 1) & 1, abort_flag, p)))
+                        if (i == 1 && act > 0 && !(ok = wait_bar(o_empty + 0, (act - 1) & 1, abort_flag, p)))
                             break;
                         ptx::tc_fence_after();
                         issue_pv<D, BF16>(tO0, tS0, vbase + sp * L::kKVBytes, i > 1);
@@ -374,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (i > 0) {
                         if (!(ok = wait_bar(p_full + 1, (g + i - 1) & 1, abort_flag, p)))
                             break;
-                        if (i == 1 && segi > 0 && !(ok = wait_bar(o_empty + 1, (segi - 1) & 1, abort_flag, p)))
+                        if (i == 1 && act > 0 && !(ok = wait_bar(o_empty + 1, (act - 1) & 1, abort_flag, p)))
                             break;
                         ptx::tc_fence_after();
                         issue_pv<D, BF16>(tO1, tS1, vbase + sp * L::kKVBytes, i > 1);
@@ -390,14 +417,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int lst = kv + n - 1, sl = lst % kStages, ul = lst / kStages;
                 ok = wait_bar(v_full + sl, ul & 1, abort_flag, p) &&
                      wait_bar(p_full + 0, (g + n - 1) & 1, abort_flag, p) &&
-                     (n > 1 || segi == 0 || wait_bar(o_empty + 0, (segi - 1) & 1, abort_flag, p));
+                     (n > 1 || act == 0 || wait_bar(o_empty + 0, (act - 1) & 1, abort_flag, p));
                 if (!ok)
                     break;
                 ptx::tc_fence_after();
                 issue_pv<D, BF16>(tO0, tS0, vbase + sl * L::kKVBytes, n > 1);
                 ptx::tc_commit(o_full + 0);
                 ok = wait_bar(p_full + 1, (g + n - 1) & 1, abort_flag, p) &&
-                     (n > 1 || segi == 0 || wait_bar(o_empty + 1, (segi - 1) & 1, abort_flag, p));
+                     (n > 1 || act == 0 || wait_bar(o_empty + 1, (act - 1) & 1, abort_flag, p));
                 if (!ok)
                     break;
                 ptx::tc_fence_after();
@@ -406,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tc_commit(v_empty + sl);
                 kv += n;
                 g += n;
-                ++segi;
+                ++act;
             }
             // Every MMA issued above has retired before TMEM is released.
             ptx::tc_commit(mma_done);
@@ -424,34 +451,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tS = tmem + lane_off + t * kBN;
         const uint32_t tO = tmem + lane_off + 2 * kBN + t * D;
         const float c = p.scale_log2;
-        int g = 0, segi = 0, pc = 0;
+        int g = 0, segi = 0, pc = 0, act = 0;
         bool ok = true;
-        while (ok) {
+        for (; ok; ++segi) {
             const unsigned char *mrow;
-            int n, jb;
+            int n, jb, k_len;
             {
                 Segment sg;
                 if (!segment_at(p, cta, segi, sg))
                     break;
-                const int bh = sg.unit / p.n_qpairs, b = bh / p.H;
-                mrow = p.mask ? p.mask + static_cast<size_t>(b) * p.Sk : nullptr;
+                Geom ge;
+                unit_geom(p, sg.unit, ge);
+                // the key mask is indexed by the key's global position: batch row, then k0 + offset
+                mrow = p.mask ? p.mask + static_cast<size_t>(ge.b) * p.Sk + ge.k0 : nullptr;
                 n = sg.je - sg.jb;
                 jb = sg.jb;
+                k_len = ge.k_len;
+                if (n == 0) {
+                    // query rows with no key at all (a packed document without keys): O = 0, LSE = -inf
+                    const int qrow = ge.q0 + prow;
+                    if (ge.q0 < ge.q_end && qrow < ge.q_end) {
+                        uint4 *orow = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) +
+                                                                ((static_cast<size_t>(ge.b) * p.Sq + qrow) * p.H + ge.h) * D);
+#pragma unroll
+                        for (int k = 0; k < D / 8; ++k)
+                            orow[k] = make_uint4(0u, 0u, 0u, 0u);
+                        if (p.lse)
+                            p.lse[(static_cast<size_t>(ge.b) * p.H + ge.h) * p.Sq + qrow] = -INFINITY;
+                    }
+                    continue;
+                }
             }
             float m_run = -INFINITY, l_run = 0.f;
             for (int i = 0; i < n; ++i) {
-                const int kb = (jb + i) * kBN;
+                const int kb = (jb + i) * kBN;  // key offset inside the unit's key range
                 // validity of the block's keys, one bit per key, identical in every lane
                 uint32_t vb[4];
                 if (mrow) {
 #pragma unroll
                     for (int w = 0; w < 4; ++w) {
                         const int key = kb + w * 32 + lane;
-                        const bool v = key < p.Sk && mrow[key] != 0;
+                        const bool v = key < k_len && mrow[key] != 0;
                         vb[w] = __ballot_sync(0xffffffffu, v);
                     }
                 } else {
-                    const int vn = p.Sk - kb;
+                    const int vn = k_len - kb;
 #pragma unroll
                     for (int w = 0; w < 4; ++w) {
                         const int nn = vn - 32 * w;
@@ -561,14 +605,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok)
                 break;
-            if (!(ok = wait_bar_warp(o_full + t, segi & 1, abort_flag, p)))
+            if (!(ok = wait_bar_warp(o_full + t, act & 1, abort_flag, p)))
                 break;
             ptx::tc_fence_after();
             Segment sg;
             segment_at(p, cta, opaque(segi), sg);
-            const int qp = sg.unit % p.n_qpairs, bh = sg.unit / p.n_qpairs;
-            const int h = bh % p.H, b = bh / p.H;
-            const int qrow = qp * (kTiles * kBM) + prow;
+            Geom ge;
+            unit_geom(p, sg.unit, ge);
+            const int h = ge.h, b = ge.b;
+            const int qrow = ge.q0 + prow;
+            const int q_end = ge.q_end;
             if (sg.full) {
                 const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
                 const float lse_val = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
@@ -582,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int k = 0; k < 32; ++k)
                         of[k] = __uint_as_float(o[k]);
-                    if (qrow < p.Sq) {
+                    if (qrow < q_end) {
                         uint4 *orow = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) +
                                                                 ((static_cast<size_t>(b) * p.Sq + qrow) * p.H + h) * D);
 #pragma unroll
@@ -593,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                           ptx::pack2<BF16>(of[8 * k + 6] * inv, of[8 * k + 7] * inv));
                     }
                 }
-                if (p.lse && qrow < p.Sq)
+                if (p.lse && qrow < q_end)
                     p.lse[(static_cast<size_t>(b) * p.H + h) * p.Sq + qrow] = lse_val;
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(o_empty + t);
@@ -672,7 +718,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 o[4 * k + 3] += w * v.w;
                             }
                         }
-                        if (qrow < p.Sq) {
+                        if (qrow < q_end) {
 #pragma unroll
                             for (int k = 0; k < 4; ++k)
                                 orow[c0 * 4 + k] = make_uint4(ptx::pack2<BF16>(o[8 * k + 0] * inv, o[8 * k + 1] * inv),
@@ -681,13 +727,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                               ptx::pack2<BF16>(o[8 * k + 6] * inv, o[8 * k + 7] * inv));
                         }
                     }
-                    if (p.lse && qrow < p.Sq)
+                    if (p.lse && qrow < q_end)
                         p.lse[(static_cast<size_t>(b) * p.H + h) * p.Sq + qrow] =
                             lsum > 0.f ? (M + log2f(lsum)) * kLn2 : -INFINITY;
                 }
             }
             g += n;
-            ++segi;
+            ++act;
         }
     }
 
@@ -762,6 +808,7 @@ struct Schedule {
 Schedule plan(int B, int Sq, int Sk, int H, int sms, bool split)
 {
     Schedule s{};
+    // packed varlen: B counts documents and Sq is the longest document
     const int n_qpairs = (Sq + kTiles * kBM - 1) / (kTiles * kBM);
     s.n_units = n_qpairs * H * B;
     s.n_kblocks = (Sk + kBN - 1) / kBN;
@@ -818,8 +865,11 @@ cudaError_t launch_typed(const AttnArgs &a, cudaStream_t stream)
     const int sms = sm_count(&err);
     if (err != cudaSuccess)
         return err;
-    const Schedule sc = plan(a.B, a.Sq, a.Sk, a.H, sms, a.workspace != nullptr);
-    if (a.workspace && a.workspace_bytes < ws_bytes(sc, D))
+    const bool varlen = a.cu_q != nullptr;
+    // varlen: one unit per (256 rows of the longest document, head, document), no split
+    const Schedule sc = varlen ? plan(a.n_docs, a.max_seqlen_q, a.Sk, a.H, sms, false)
+                               : plan(a.B, a.Sq, a.Sk, a.H, sms, a.workspace != nullptr);
+    if (!varlen && a.workspace && a.workspace_bytes < ws_bytes(sc, D))
         return cudaErrorInvalidValue;
     CUtensorMap mq, mk, mv;
     if ((err = make_map(&mq, a.q, a.B, a.Sq, a.H, D, BF16)) != cudaSuccess)
@@ -836,8 +886,11 @@ cudaError_t launch_typed(const AttnArgs &a, cudaStream_t stream)
     p.Sq = a.Sq;
     p.Sk = a.Sk;
     p.H = a.H;
-    p.n_qpairs = (a.Sq + kTiles * kBM - 1) / (kTiles * kBM);
+    p.n_qpairs = ((varlen ? a.max_seqlen_q : a.Sq) + kTiles * kBM - 1) / (kTiles * kBM);
     p.n_kblocks = sc.n_kblocks;
+    p.cu_q = a.cu_q;
+    p.cu_k = a.cu_k;
+    p.varlen = varlen ? 1 : 0;
     p.n_units = sc.n_units;
     p.grid = sc.grid;
     p.dp_waves = sc.dp_waves;
@@ -847,7 +900,7 @@ cudaError_t launch_typed(const AttnArgs &a, cudaStream_t stream)
     if (err != cudaSuccess)
         return err;
     p.wait_limit_ns = kDefaultWaitLimitNs;
-    if (a.workspace) {
+    if (!varlen && a.workspace) {
         uint8_t *ws = static_cast<uint8_t *>(a.workspace);
         p.counters = reinterpret_cast<int *>(ws);
         p.part_ml = reinterpret_cast<float2 *>(ws + ws_counter_bytes(sc));

@@ -63,6 +63,10 @@ struct AttnArgs {
     float scale;
     void *workspace;             // NULL: one CTA per work unit, no split
     long long workspace_bytes;
+    const int *cu_q;             // packed varlen (B = 1): local query boundaries, NULL otherwise
+    const int *cu_k;             // packed varlen: key boundaries
+    int n_docs;
+    int max_seqlen_q;
 };
 
 cudaError_t launch_attention(const AttnArgs &a, cudaStream_t stream);
@@ -83,6 +87,9 @@ struct LseMergeArgs {
 };
 
 cudaError_t launch_lse_merge(const LseMergeArgs &a, cudaStream_t stream);
+
+cudaError_t launch_varlen_remap(const int *cu_g, int n_docs, long long lo, long long len, int *cu_l,
+                                const int *pad_in, int *pad_out, cudaStream_t stream);
 
 // Records a CUDA error for ctx_last_cuda_error() on the calling thread.
 void record_cuda_error(cudaError_t e);

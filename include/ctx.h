@@ -284,6 +284,54 @@ ctx_status ctx_lse_merge(const void *o_parts, const float *lse_parts, int P,
                          void *out, float *lse, int B, int Sq, int H, int D,
                          ctx_dtype dtype, void *stream);
 
+/*
+ * ctx_varlen_remap — packed varlen query metadata of one rank (vllm-omni PR
+ * #7641, packed query metadata under AllGather-KV). Every global query
+ * document [cu[d], cu[d+1]) is intersected with the rank's span
+ * [span_begin, span_begin + span_len); the rank keeps exactly one (possibly
+ * empty) entry per document, prefix-summed from 0, so its documents still
+ * pair one to one with the global key boundaries (which stay unchanged).
+ * Example from the page: documents [0,8,12] at A = 2 give [0,6,6] on rank 0
+ * and [0,2,6] on rank 1. Computed on the device (no host synchronisation).
+ *
+ * cu_seqlens_q          : [n_docs + 1] int32 device, global query boundaries.
+ * cu_seqlens_q_local    : [n_docs + 1] int32 device, written.
+ * packed_padding        : NULL or [2] int32 device {real, pad} of a single
+ *                         padded document; packed_padding_local (both or
+ *                         neither) receives {local real, span_len - local
+ *                         real}: the query length narrows to the rank's valid
+ *                         prefix (the key length stays global).
+ */
+ctx_status ctx_varlen_remap(const int *cu_seqlens_q, int n_docs,
+                            long long span_begin, long long span_len,
+                            int *cu_seqlens_q_local, const int *packed_padding,
+                            int *packed_padding_local, void *stream);
+
+/*
+ * ctx_attn_varlen — local-Q / global-KV attention over packed documents
+ * (FlashAttention-varlen style metadata, vllm-omni PR #7641): query rows
+ * [cu_seqlens_q[d], cu_seqlens_q[d+1]) attend keys
+ * [cu_seqlens_k[d], cu_seqlens_k[d+1]) only; otherwise as ctx_attn_lq_gkv.
+ * Query rows outside every document are not written; a document with query
+ * rows but no keys gets out = 0 and lse = -inf.
+ *
+ * q            : [Sq, H, D] device (one packed sequence).
+ * k, v         : [Sk, H, D] device.
+ * cu_seqlens_q : [n_docs + 1] int32 device (local boundaries, e.g. from
+ *                ctx_varlen_remap); cu_seqlens_k : [n_docs + 1] int32 device.
+ *                Boundaries are clamped to [0, Sq] / [0, Sk] on the device.
+ * max_seqlen_q : host int >= every document's query length (rows beyond it
+ *                are not computed).
+ * key_mask     : NULL or [Sk] bytes, nonzero = attend (global key index).
+ * out          : [Sq, H, D]; lse : NULL or [H, Sq] float32.
+ */
+ctx_status ctx_attn_varlen(const void *q, const void *k, const void *v,
+                           const int *cu_seqlens_q, const int *cu_seqlens_k,
+                           int n_docs, int max_seqlen_q,
+                           const unsigned char *key_mask, float scale,
+                           void *out, float *lse, int Sq, int Sk, int H, int D,
+                           ctx_dtype dtype, void *stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *ctx_status_string(ctx_status status);
 

@@ -143,3 +143,19 @@ def test_lse_merge_validation(lib):
     assert f(o + 8, l, 2, out, lo, 1, 4, 2, 8, 0, None) == MISALIGNED
     assert f(o, l, 2, o + 16, lo, 1, 4, 2, 8, 0, None) == ALIASING      # out inside the parts
     assert f(o, l, 2, out, l, 1, 4, 2, 8, 0, None) == ALIASING          # lse over lse_parts
+
+
+def test_varlen_validation(lib):
+    f = lib.ctx_attn_varlen
+    q, k, v, cq, ck, o, l = A0, A0 + MB, A0 + 2 * MB, A0 + 3 * MB, A0 + 3 * MB + 256, A0 + 4 * MB, A0 + 5 * MB
+    nan = float("nan")
+    assert f(q, k, v, cq, ck, 0, 16, None, nan, o, l, 16, 16, 2, 128, 0, None) == INVALID   # no documents
+    assert f(q, k, v, cq, ck, 2, 0, None, nan, o, l, 16, 16, 2, 128, 0, None) == INVALID   # max_seqlen_q
+    assert f(q, k, v, cq, ck, 2, 16, None, nan, o, l, 16, 16, 2, 96, 0, None) == UNSUPPORTED
+    assert f(q, k, v, cq + 2, ck, 2, 16, None, nan, o, l, 16, 16, 2, 128, 0, None) == MISALIGNED
+    assert f(q, k, v, cq, ck, 2, 16, None, nan, cq, l, 16, 16, 2, 128, 0, None) == ALIASING
+    r = lib.ctx_varlen_remap
+    assert r(cq, 0, 0, 8, ck, None, None, None) == INVALID
+    assert r(cq, 2, -1, 8, ck, None, None, None) == INVALID
+    assert r(cq, 2, 0, 8, cq + 4, None, None, None) == ALIASING
+    assert r(cq, 2, 0, 8, ck, A0 + 6 * MB, None, None) == INVALID      # padding in without out
