@@ -35,6 +35,7 @@ SIGNATURES = {
     "ctx_unpack_qkv": (_I, [_P, _P, _P, _P, _LL, _LL, _I, _I, _I, _I, _I, _I, _P]),
     "ctx_attn_lq_gkv": (_I, [_P, _P, _P, _P, _F, _P, _P, _P, _LL, _I, _I, _I, _I, _I, _I, _P]),
     "ctx_attn_lq_gkv_workspace_size": (_LL, [_I, _I, _I, _I, _I]),
+    "ctx_attn_lq_gkv_pack_out": (_I, [_P, _P, _P, _P, _F, _P, _P, _P, _LL, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
     "ctx_attn_lq_gkv_noalloc": (_I, [_P, _P, _P, _P, _F, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "ctx_pack_out": (_I, [_P, _P, _LL, _I, _I, _I, _I, _I, _I, _P]),
     "ctx_unpack_out": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P]),
@@ -169,6 +170,20 @@ def ctx_attn_lq_gkv(q, k, v, out, lse=None, key_mask=None, scale: float | None =
                                                     _ptr(lse), _ptr(workspace), wb, B, Sq, Sk, H, D, _dtype(q),
                                                     _stream(stream)))
     return out
+
+
+def ctx_attn_lq_gkv_pack_out(q, k, v, send, U: int, B_rank: int, S_l: int, lse=None, key_mask=None,
+                             scale: float | None = None, workspace=None, stream=None):
+    """Attention whose output goes straight into the reverse exchange's send
+    layout: q [B,Sq,H,D] (B = U'*B_rank, Sq = A*U*S_l), send [A,U',U,B_rank,S_l,H,D]."""
+    B, Sq, H, D = q.shape
+    Sk = k.shape[1]
+    s = float("nan") if scale is None else float(scale)
+    wb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("ctx_attn_lq_gkv_pack_out", lib().ctx_attn_lq_gkv_pack_out(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(key_mask), s, _ptr(send), _ptr(lse), _ptr(workspace), wb, B, Sq, Sk, H, D,
+        U, B_rank, S_l, _dtype(q), _stream(stream)))
+    return send
 
 
 def ctx_attn_lq_gkv_workspace_size(B: int, Sq: int, Sk: int, H: int, D: int) -> int:

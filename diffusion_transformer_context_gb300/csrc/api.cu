@@ -457,9 +457,10 @@ ctx_status ctx_unpack_out_ex(const void *recv, void *y, int B, int S_l, int h_l,
     return run_relayout(RelayoutMode::UnpackOutPad, a, stream);
 }
 
-ctx_status ctx_attn_lq_gkv(const void *q, const void *k, const void *v, const unsigned char *key_mask, float scale,
-                           void *out, float *lse, void *workspace, long long workspace_bytes, int B, int Sq, int Sk,
-                           int H, int D, ctx_dtype dtype, void *stream)
+static ctx_status attn_common(const void *q, const void *k, const void *v, const unsigned char *key_mask,
+                              float scale, void *out, float *lse, void *workspace, long long workspace_bytes, int B,
+                              int Sq, int Sk, int H, int D, ctx_dtype dtype, void *stream, int blk_s, int blk_u,
+                              int blk_b)
 {
     if (!q || !k || !v || !out || !valid_dtype(dtype))
         return CTX_ERR_INVALID_ARG;
@@ -518,8 +519,32 @@ ctx_status ctx_attn_lq_gkv(const void *q, const void *k, const void *v, const un
     a.scale = scale;
     a.workspace = workspace;
     a.workspace_bytes = workspace_bytes;
+    a.blk_s = blk_s;
+    a.blk_u = blk_u;
+    a.blk_b = blk_b;
     cudaError_t e = ctx::launch_attention(a, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? CTX_OK : cuda_fail(e);
+}
+
+ctx_status ctx_attn_lq_gkv(const void *q, const void *k, const void *v, const unsigned char *key_mask, float scale,
+                           void *out, float *lse, void *workspace, long long workspace_bytes, int B, int Sq, int Sk,
+                           int H, int D, ctx_dtype dtype, void *stream)
+{
+    return attn_common(q, k, v, key_mask, scale, out, lse, workspace, workspace_bytes, B, Sq, Sk, H, D, dtype, stream,
+                       0, 0, 0);
+}
+
+ctx_status ctx_attn_lq_gkv_pack_out(const void *q, const void *k, const void *v, const unsigned char *key_mask,
+                                    float scale, void *send, float *lse, void *workspace, long long workspace_bytes,
+                                    int B, int Sq, int Sk, int H, int D, int U, int B_rank, int S_l, ctx_dtype dtype,
+                                    void *stream)
+{
+    // the send layout must cover the output exactly: Sq = A*U*S_l rows, B = U'*B_rank with U' <= U
+    if (U <= 0 || B_rank <= 0 || S_l <= 0 || Sq <= 0 || B <= 0 || Sq % (static_cast<long long>(U) * S_l) != 0 ||
+        B % B_rank != 0 || B / B_rank > U)
+        return CTX_ERR_INVALID_ARG;
+    return attn_common(q, k, v, key_mask, scale, send, lse, workspace, workspace_bytes, B, Sq, Sk, H, D, dtype,
+                       stream, S_l, U, B_rank);
 }
 
 long long ctx_attn_lq_gkv_workspace_size(int B, int Sq, int Sk, int H, int D)

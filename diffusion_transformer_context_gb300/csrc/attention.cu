@@ -58,6 +58,7 @@ struct Params {
     const int *cu_q;       // packed varlen: [n_docs + 1] local query boundaries (device), else NULL
     const int *cu_k;       // packed varlen: [n_docs + 1] key boundaries (device)
     int varlen;            // 1: units are (query-tile pair, head, document)
+    int blk_s, blk_u, blk_b;  // > 0: out is the reverse exchange's send buffer (see out_row)
     int n_units;           // work units: (query-tile pair, head, batch or document)
     int grid;              // persistent CTAs
     int dp_waves;          // whole-unit waves: CTA c takes units c, c+grid, ...
@@ -126,6 +127,28 @@ __device__ __forceinline__ void unit_geom(const Params &p, int unit, Geom &g)
         g.k_len = min(max(__ldg(p.cu_k + x + 1), g.k0), p.Sk) - g.k0;
     }
     g.nblk = (g.q0 < g.q_end && g.k_len > 0) ? (g.k_len + kBN - 1) / kBN : 0;
+}
+
+// First element of output row (b, qrow, h). Plain layout: [B, Sq, H, D].
+// Reverse-exchange layout (blk_s > 0, the send-side relayout of the output
+// exchange fused into the epilogue): query row q = (a*blk_u + r)*blk_s + s
+// of batch b = u*blk_b + b' goes to the send buffer of rank (a, u),
+// destination r: [a][u][r][b'][s] — for one rank's call (a = u = 0) that is
+// [U][B][S_l], the layout ctx_pack_out writes.
+template <int D>
+__device__ __forceinline__ uint4 *out_row(const Params &p, int b, int h, int qrow)
+{
+    size_t row;
+    if (p.blk_s > 0) {
+        const int qb = qrow / p.blk_s, s = qrow - qb * p.blk_s;
+        const int a = qb / p.blk_u, r = qb - a * p.blk_u;
+        const int u = b / p.blk_b, bb = b - u * p.blk_b;
+        row = ((static_cast<size_t>(a) * p.blk_u + u) * p.blk_u + r) * p.blk_b * p.blk_s +
+              static_cast<size_t>(bb) * p.blk_s + s;
+    } else {
+        row = static_cast<size_t>(b) * p.Sq + qrow;
+    }
+    return reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) + (row * p.H + h) * D);
 }
 
 // Segment `si` of CTA c, computed from its index alone (identical in every
@@ -471,8 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // query rows with no key at all (a packed document without keys): O = 0, LSE = -inf
                     const int qrow = ge.q0 + prow;
                     if (ge.q0 < ge.q_end && qrow < ge.q_end) {
-                        uint4 *orow = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) +
-                                                                ((static_cast<size_t>(ge.b) * p.Sq + qrow) * p.H + ge.h) * D);
+                        uint4 *orow = out_row<D>(p, ge.b, ge.h, qrow);
 #pragma unroll
                         for (int k = 0; k < D / 8; ++k)
                             orow[k] = make_uint4(0u, 0u, 0u, 0u);
@@ -629,8 +651,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int k = 0; k < 32; ++k)
                         of[k] = __uint_as_float(o[k]);
                     if (qrow < q_end) {
-                        uint4 *orow = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) +
-                                                                ((static_cast<size_t>(b) * p.Sq + qrow) * p.H + h) * D);
+                        uint4 *orow = out_row<D>(p, b, h, qrow);
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
                             orow[c0 * 4 + k] = make_uint4(ptx::pack2<BF16>(of[8 * k + 0] * inv, of[8 * k + 1] * inv),
@@ -696,8 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         lsum += (ml.x == -INFINITY) ? 0.f : ptx::ex2_approx(ml.x - M) * ml.y;
                     }
                     const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
-                    uint4 *orow = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) +
-                                                            ((static_cast<size_t>(b) * p.Sq + qrow) * p.H + h) * D);
+                    uint4 *orow = out_row<D>(p, b, h, qrow);
 #pragma unroll 1
                     for (int c0 = 0; c0 < D / 32; ++c0) {
                         float o[32];
@@ -891,6 +911,9 @@ cudaError_t launch_typed(const AttnArgs &a, cudaStream_t stream)
     p.cu_q = a.cu_q;
     p.cu_k = a.cu_k;
     p.varlen = varlen ? 1 : 0;
+    p.blk_s = a.blk_s;
+    p.blk_u = a.blk_u;
+    p.blk_b = a.blk_b;
     p.n_units = sc.n_units;
     p.grid = sc.grid;
     p.dp_waves = sc.dp_waves;

@@ -67,6 +67,7 @@ struct AttnArgs {
     const int *cu_k;             // packed varlen: key boundaries
     int n_docs;
     int max_seqlen_q;
+    int blk_s, blk_u, blk_b;     // > 0: write out in the reverse exchange's send layout
 };
 
 cudaError_t launch_attention(const AttnArgs &a, cudaStream_t stream);

@@ -16,7 +16,9 @@ of Q, K, V [B, S, H, D]. One step runs, through the C ABI only:
      gathered K/V, so their local-Q slices stack into one [S, h_l] query set
      per u, batched over u (rows are independent, so this equals one launch
      per rank);
-  5. the reverse exchange ctx_pack_out -> ctx_sim_all_to_all ->
+  5. the reverse exchange ctx_pack_out (fused into the attention epilogue
+     by default: ctx_attn_lq_gkv_pack_out writes the send buffers) ->
+     ctx_sim_all_to_all ->
      ctx_unpack_out_ex for every rank (at U = 1 the output rows already are the
      sequence-sharded result and step 5 is the identity).
 
@@ -30,17 +32,19 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (CTX_LAYOUT_TQKV, attn_workspace, ctx_attn_lq_gkv, ctx_pack_out, ctx_pack_qkv_ex,
-               ctx_sim_all_to_all, ctx_unpack_out_ex, ctx_unpack_qkv_ex)
+from . import (CTX_LAYOUT_TQKV, attn_workspace, ctx_attn_lq_gkv, ctx_attn_lq_gkv_pack_out, ctx_pack_out,
+               ctx_pack_qkv_ex, ctx_sim_all_to_all, ctx_unpack_out_ex, ctx_unpack_qkv_ex)
 
 
 class SimLayer:
     def __init__(self, wl, device="cuda", dtype=torch.bfloat16, attention: bool | None = None,
-                 balanced: bool = True, layout: int = CTX_LAYOUT_TQKV):
+                 balanced: bool = True, layout: int = CTX_LAYOUT_TQKV, fuse_reverse: bool = True):
         self.wl = wl
         self.dev = torch.device(device)
         self.dtype = dtype
         self.layout = layout
+        # U > 1: the attention epilogue writes the reverse exchange's send buffers directly
+        self.fuse_reverse = fuse_reverse and wl.U > 1
         U, A, B, S, H, D, J = wl.U, wl.A, wl.B, wl.S, wl.H, wl.D, wl.joint
         if S % (U * A):
             raise ValueError("S must divide by U*A")
@@ -115,9 +119,13 @@ class SimLayer:
         wl = self.wl
         U, B, S, D = wl.U, wl.B, wl.S, wl.D
         h_l, Sk = self.h_l, self.Sk
-        ctx_attn_lq_gkv(self.qg.view(U * B, S, h_l, D), self.kg.view(U * B, Sk, h_l, D),
-                        self.vg.view(U * B, Sk, h_l, D), self.out.view(U * B, S, h_l, D), self.lse,
-                        key_mask=self.mask, workspace=self.ws, stream=stream)
+        args = (self.qg.view(U * B, S, h_l, D), self.kg.view(U * B, Sk, h_l, D), self.vg.view(U * B, Sk, h_l, D))
+        if self.fuse_reverse:
+            ctx_attn_lq_gkv_pack_out(*args, self.osend, U, B, self.S_l, lse=self.lse, key_mask=self.mask,
+                                     workspace=self.ws, stream=stream)
+        else:
+            ctx_attn_lq_gkv(*args, self.out.view(U * B, S, h_l, D), self.lse, key_mask=self.mask,
+                            workspace=self.ws, stream=stream)
 
     def exchange_out(self, stream=None):
         """Step 5: the reverse exchange (identity at U = 1)."""
@@ -126,10 +134,11 @@ class SimLayer:
         S_l, h_l = self.S_l, self.h_l
         if not self.attention or U == 1:
             return
-        for g in range(self.R):
-            a, u = divmod(g, U)
-            ctx_pack_out(self.out[u, :, a * U * S_l:], self.osend[a, u].view(U, B, S_l, h_l, D), U,
-                         o_batch_stride_rows=S, stream=stream)
+        if not self.fuse_reverse:
+            for g in range(self.R):
+                a, u = divmod(g, U)
+                ctx_pack_out(self.out[u, :, a * U * S_l:], self.osend[a, u].view(U, B, S_l, h_l, D), U,
+                             o_batch_stride_rows=S, stream=stream)
         ctx_sim_all_to_all(self.osend, self.orecv, A, U, stream=stream)
         for g in range(self.R):
             a, u = divmod(g, U)
@@ -171,7 +180,9 @@ class SimLayer:
         U, R = self.wl.U, self.R
         n = 2 * R + (1 if U > 1 else 0)
         if self.attention:
-            n += 1 + ((2 * R + 1) if U > 1 else 0)
+            n += 1
+            if U > 1:
+                n += (R + 1) if self.fuse_reverse else (2 * R + 1)
         return n
 
     # ---------------------------------------------------------- results
@@ -205,8 +216,10 @@ class SimLayer:
         if not self.attention or wl.U == 1:
             return 0
         one = self.R * wl.B * self.S_l * self.H_pad * wl.D * 2
-        # pack_out and all-to-all read + write padded rows; unpack_out reads padded, writes real heads
-        return 2 * one + 2 * one + one + self.R * wl.B * self.S_l * wl.H * wl.D * 2
+        # pack_out (unless fused into the attention epilogue) and the all-to-all read + write
+        # padded rows; unpack_out reads padded, writes real heads
+        pack_out = 0 if self.fuse_reverse else 2 * one
+        return pack_out + 2 * one + one + self.R * wl.B * self.S_l * wl.H * wl.D * 2
 
     def attn_flops(self, text_len=None, dense: bool = False) -> float:
         """4 * Sq * K_valid * D per head (QK^T and PV), summed over all ranks."""

@@ -205,6 +205,29 @@ ctx_status ctx_attn_lq_gkv(const void *q, const void *k, const void *v,
                            int H, int D, ctx_dtype dtype, void *stream);
 
 /*
+ * ctx_attn_lq_gkv_pack_out — ctx_attn_lq_gkv whose epilogue writes the output
+ * directly in the send layout of the reverse Ulysses exchange (the output of
+ * ctx_pack_out), saving one read and one write of O (the page's reverse
+ * all-to-all after local-Q / global-KV attention; fusing it into the
+ * epilogue is this library's choice).
+ *
+ * One rank: q is its local query [B_rank, U*S_l, h_l, D] (B = B_rank); send
+ * is [U, B_rank, S_l, h_l, D]: send[r][b][s] = O[b][r*S_l + s].
+ * Several ranks stacked as the simulation does (rank (a, u) holds query rows
+ * [a*U*S_l, (a+1)*U*S_l) of batch block u, B = U'*B_rank, Sq = A*U*S_l):
+ * send is [A][U'][U][B_rank][S_l][h_l][D], rank (a, u)'s send buffer at
+ * [a][u]. lse keeps the plain [B, H, Sq] layout.
+ * Errors: as ctx_attn_lq_gkv; INVALID_ARG unless Sq % (U*S_l) == 0,
+ * B % B_rank == 0 and B / B_rank <= U.
+ */
+ctx_status ctx_attn_lq_gkv_pack_out(const void *q, const void *k, const void *v,
+                                    const unsigned char *key_mask, float scale,
+                                    void *send, float *lse, void *workspace,
+                                    long long workspace_bytes, int B, int Sq,
+                                    int Sk, int H, int D, int U, int B_rank,
+                                    int S_l, ctx_dtype dtype, void *stream);
+
+/*
  * ctx_attn_lq_gkv_workspace_size — bytes of workspace ctx_attn_lq_gkv needs
  * for its balanced schedule on the current device (it depends on the SM
  * count). Returns -1 for invalid sizes or when no device can be queried.

@@ -159,3 +159,16 @@ def test_varlen_validation(lib):
     assert r(cq, 2, -1, 8, ck, None, None, None) == INVALID
     assert r(cq, 2, 0, 8, cq + 4, None, None, None) == ALIASING
     assert r(cq, 2, 0, 8, ck, A0 + 6 * MB, None, None) == INVALID      # padding in without out
+
+
+def test_pack_out_fused_validation(lib):
+    f = lib.ctx_attn_lq_gkv_pack_out
+    q, k, v, o = A0, A0 + MB, A0 + 2 * MB, A0 + 3 * MB
+    nan = float("nan")
+    # Sq = 30 not a multiple of U*S_l = 4*8
+    assert f(q, k, v, None, nan, o, None, None, 0, 1, 30, 16, 2, 128, 4, 1, 8, 0, None) == INVALID
+    # B = 3 not a multiple of B_rank = 2
+    assert f(q, k, v, None, nan, o, None, None, 0, 3, 32, 16, 2, 128, 4, 2, 8, 0, None) == INVALID
+    # more batch blocks (B / B_rank = 5) than destinations U = 4
+    assert f(q, k, v, None, nan, o, None, None, 0, 5, 32, 16, 2, 128, 4, 1, 8, 0, None) == INVALID
+    assert f(q, k, v, None, nan, o, None, None, 0, 1, 32, 16, 2, 96, 4, 1, 8, 0, None) == UNSUPPORTED

@@ -224,6 +224,31 @@ def test_balanced_schedule_matches_per_unit(ctx, B, Sq, Sk, H):
     assert float((l1 - l2).abs().max()) <= 1e-5
 
 
+@pytest.mark.parametrize("B_rank,U,S_l,A,split", [(2, 4, 300, 1, False), (1, 2, 512, 2, True), (2, 2, 96, 3, True)])
+def test_pack_out_fused_epilogue_equals_attention_then_pack_out(ctx, B_rank, U, S_l, A, split):
+    """ctx_attn_lq_gkv_pack_out == ctx_attn_lq_gkv followed by ctx_pack_out,
+    bit for bit, for one rank (A = 1, one batch block) and for stacked ranks."""
+    gen = torch.Generator().manual_seed(17)
+    H, D, Sk = 2, 128, 777
+    Ub = U if A > 1 else 1          # batch blocks (head groups) stacked in the call
+    B, Sq = Ub * B_rank, A * U * S_l
+    q, k, v = (workloads.randn(s, gen).cuda() for s in ((B, Sq, H, D), (B, Sk, H, D), (B, Sk, H, D)))
+    ws = ctx.attn_workspace(B, Sq, Sk, H, D) if split else None
+    out = torch.empty_like(q)
+    lse1 = torch.empty((B, H, Sq), device="cuda")
+    ctx.ctx_attn_lq_gkv(q, k, v, out, lse1, workspace=ws)
+    send_ref = torch.empty((A, Ub, U, B_rank, S_l, H, D), dtype=q.dtype, device="cuda")
+    ov = out.view(Ub, B_rank, Sq, H, D)
+    for a in range(A):
+        for u in range(Ub):
+            ctx.ctx_pack_out(ov[u, :, a * U * S_l:], send_ref[a, u], U, o_batch_stride_rows=Sq)
+    send = torch.full_like(send_ref, float("nan"))
+    lse2 = torch.empty_like(lse1)
+    ctx.ctx_attn_lq_gkv_pack_out(q, k, v, send, U, B_rank, S_l, lse=lse2, workspace=ws)
+    assert ctx.ctx_device_status() == 0
+    assert torch.equal(send, send_ref) and torch.equal(lse1, lse2)
+
+
 # ---------------------------------------------------------------- failure path
 
 def test_bounded_wait_times_out_and_context_survives(ctx, orc):

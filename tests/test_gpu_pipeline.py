@@ -38,7 +38,7 @@ def _oracle_side(orc, inp, layout=0):
 def _check_layer(ctx, orc, wl, n_rows=None, layout=0):
     from diffusion_transformer_context_gb300.simulate import SimLayer
     inp = workloads.make_inputs(wl)
-    sim = SimLayer(wl, layout=layout)
+    sim = SimLayer(wl, layout=layout, fuse_reverse=False)
     sim.load(inp)
     sim.step()
     st = ctx.ctx_device_status()
@@ -86,6 +86,15 @@ def _check_layer(ctx, orc, wl, n_rows=None, layout=0):
     back = orc.ulysses_reverse(o_ranks, U, A, wl.H)
     for g in range(wl.ranks):
         assert np.array_equal(u16(sim.rank_output(g)), back[g]), f"reverse rank {g}"
+    if U > 1:
+        # the send-side relayout fused into the attention epilogue gives the same bits
+        fused = SimLayer(wl, layout=layout, fuse_reverse=True)
+        fused.load(inp)
+        fused.step()
+        assert ctx.ctx_device_status() == 0
+        assert torch.equal(fused.lse, sim.lse)
+        for g in range(wl.ranks):
+            assert torch.equal(fused.rank_output(g), sim.rank_output(g)), f"fused reverse rank {g}"
 
 
 def test_tiny(ctx, orc):
