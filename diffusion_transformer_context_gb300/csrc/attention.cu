@@ -10,8 +10,8 @@
 //   * warp 0 issues TMA loads: both Q tiles once, then K and V blocks of 128
 //     keys into a two-stage ring (128-byte swizzled tiles, mbarrier
 //     complete_tx accounting);
-//   * warp 1 allocates 512 TMEM columns and one elected lane issues every
-//     tcgen05.mma: S_t = Q_t K^T (A and B from shared memory, K-major) into
+//   * warp 1 allocates 512 TMEM columns and runs the MMA loop as a whole warp
+//     (warp-uniform descriptors), one elected lane issuing every tcgen05.mma: S_t = Q_t K^T (A and B from shared memory, K-major) into
 //     TMEM columns [128t, 128t+128), and O_t += P_t V with P_t read from TMEM
 //     (it overwrites S_t as 16-bit pairs) and V from shared memory (MN-major)
 //     into columns [256 + Dt, 256 + D(t+1));
@@ -386,7 +386,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issue
-        if (lane == 0) {
+        // The whole warp runs this loop (warp-uniform values, warp-wide waits);
+        // one elected lane issues each MMA and commit.
+        {
             const uint32_t qa0 = ptx::smem_u32(smem + L::kQOff);
             const uint32_t qa1 = qa0 + L::kQBytes;
             const uint32_t kbase = ptx::smem_u32(smem + L::kKOff);
@@ -400,21 +402,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int n = sg.je - sg.jb;
                 if (n == 0)
                     continue;
-                if (!(ok = wait_bar(q_full, act & 1, abort_flag, p)))
+                if (!(ok = wait_bar_warp(q_full, act & 1, abort_flag, p)))
                     break;
                 ptx::tc_fence_after();
                 for (int i = 0; i < n; ++i) {
                     const int cur = kv + i, s = cur % kStages, u = cur / kStages;
-                    if (!(ok = wait_bar(k_full + s, u & 1, abort_flag, p)))
+                    if (!(ok = wait_bar_warp(k_full + s, u & 1, abort_flag, p)))
                         break;
                     ptx::tc_fence_after();
                     const int prv = cur - 1, sp = (cur + kStages - 1) % kStages, up = prv / kStages;
                     if (i > 0) {
-                        if (!(ok = wait_bar(v_full + sp, up & 1, abort_flag, p)))
+                        if (!(ok = wait_bar_warp(v_full + sp, up & 1, abort_flag, p)))
                             break;
-                        if (!(ok = wait_bar(p_full + 0, (g + i - 1) & 1, abort_flag, p)))
+                        if (!(ok = wait_bar_warp(p_full + 0, (g + i - 1) & 1, abort_flag, p)))
                             break;
-                        if (i == 1 && act > 0 && !(ok = wait_bar(o_empty + 0, (act - 1) & 1, abort_flag, p)))
+                        if (i == 1 && act > 0 && !(ok = wait_bar_warp(o_empty + 0, (act - 1) & 1, abort_flag, p)))
                             break;
                         ptx::tc_fence_after();
                         issue_pv<D, BF16>(tO0, tS0, vbase + sp * L::kKVBytes, i > 1);
@@ -422,9 +424,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     issue_qk<D, BF16>(tS0, qa0, kbase + s * L::kKVBytes);
                     ptx::tc_commit(s_full + 0);
                     if (i > 0) {
-                        if (!(ok = wait_bar(p_full + 1, (g + i - 1) & 1, abort_flag, p)))
+                        if (!(ok = wait_bar_warp(p_full + 1, (g + i - 1) & 1, abort_flag, p)))
                             break;
-                        if (i == 1 && act > 0 && !(ok = wait_bar(o_empty + 1, (act - 1) & 1, abort_flag, p)))
+                        if (i == 1 && act > 0 && !(ok = wait_bar_warp(o_empty + 1, (act - 1) & 1, abort_flag, p)))
                             break;
                         ptx::tc_fence_after();
                         issue_pv<D, BF16>(tO1, tS1, vbase + sp * L::kKVBytes, i > 1);
@@ -438,16 +440,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 ptx::tc_commit(q_empty);  // the segment's QK^T products are all issued
                 const int lst = kv + n - 1, sl = lst % kStages, ul = lst / kStages;
-                ok = wait_bar(v_full + sl, ul & 1, abort_flag, p) &&
-                     wait_bar(p_full + 0, (g + n - 1) & 1, abort_flag, p) &&
-                     (n > 1 || act == 0 || wait_bar(o_empty + 0, (act - 1) & 1, abort_flag, p));
+                ok = wait_bar_warp(v_full + sl, ul & 1, abort_flag, p) &&
+                     wait_bar_warp(p_full + 0, (g + n - 1) & 1, abort_flag, p) &&
+                     (n > 1 || act == 0 || wait_bar_warp(o_empty + 0, (act - 1) & 1, abort_flag, p));
                 if (!ok)
                     break;
                 ptx::tc_fence_after();
                 issue_pv<D, BF16>(tO0, tS0, vbase + sl * L::kKVBytes, n > 1);
                 ptx::tc_commit(o_full + 0);
-                ok = wait_bar(p_full + 1, (g + n - 1) & 1, abort_flag, p) &&
-                     (n > 1 || act == 0 || wait_bar(o_empty + 1, (act - 1) & 1, abort_flag, p));
+                ok = wait_bar_warp(p_full + 1, (g + n - 1) & 1, abort_flag, p) &&
+                     (n > 1 || act == 0 || wait_bar_warp(o_empty + 1, (act - 1) & 1, abort_flag, p));
                 if (!ok)
                     break;
                 ptx::tc_fence_after();
@@ -461,8 +463,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Every MMA issued above has retired before TMEM is released.
             ptx::tc_commit(mma_done);
             wait_bar(mma_done, 0, abort_flag, p, false);
+            __syncwarp();
         }
-        __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax
         const int t = (warp - 2) >> 2;  // query tile
