@@ -9,8 +9,9 @@ Default workload: the Wan-like 480p AllGather-KV CP8 layer (local-Q
 `value` is the attention FLOPs of the step divided by the device time of the
 whole step (inputs resident in HBM); `roofline` is the attention kernel alone
 (CUDA events on its stream); `relayout` reports the pack/unpack GB/s;
-`e2e` repeats the step through the same public API with the inputs copied
-from pinned host memory and the output read back inside the timed region.
+`e2e` repeats the step through the same public API with every step's inputs
+copied from pinned host memory and its output read back inside the timed
+region (copies pipelined on their own streams against the compute).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle on a bounded sample
@@ -214,31 +215,91 @@ def run_gpu(args, rank, world, local_rank):
     # ---------------------------------------------------------- e2e (host buffers)
     e2e = None
     if not args.no_e2e:
-        host_x = torch.empty(sim.x.shape, dtype=sim.x.dtype).pin_memory()
-        host_x.copy_(sim.x.cpu())
-        result = sim.y if (sim.attention and wl.U > 1) else sim.out
-        host_y = torch.empty(result.shape, dtype=result.dtype).pin_memory()
-        for _ in range(max(1, args.warmup)):
-            sim.x.copy_(host_x, non_blocking=True)
-            plain_step()
-            host_y.copy_(result, non_blocking=True)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        barrier()
-        e0.record(stream)
-        for _ in range(args.steps):
-            sim.x.copy_(host_x, non_blocking=True)
-            plain_step()
-            host_y.copy_(result, non_blocking=True)
-        e1.record(stream)
-        barrier()
-        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
-        flops = sim.attn_flops(inp.text_len)
-        e2e = {"value": round(whole_job_tflops(flops * args.steps, world, e2e_ms), 3), "unit": "TFLOP/s",
-               "h2d_bytes_per_step": host_x.numel() * host_x.element_size(),
-               "d2h_bytes_per_step": host_y.numel() * host_y.element_size(),
-               "ms_per_step": round(e2e_ms / args.steps, 4)}
+        e2e = run_e2e(sim, inp, args, world, dev, run_phase, barrier)
     sim.l2_flushed = flush
     return sim, inp, total_ms, parts, clocks, e2e
+
+
+def run_e2e(sim, inp, args, world, dev, run_phase, barrier):
+    """The same steps with every step's inputs copied in from pinned host
+    memory and its result copied back, all inside the timed region.
+
+    Three streams pipeline the copies the way a serving loop would: the
+    host->device copy of step i+1 runs on its own stream as soon as step i's
+    exchange has read the input buffer (during step i's attention), and the
+    device->host copy of step i runs on a third stream while step i+1
+    computes. Where the result buffer is written again early in the next
+    step (the attention output at U = 1), it is first snapshotted on the
+    device (one D2D copy per step, inside the timed region) so the read-back
+    never races the next step's kernels."""
+    import torch
+
+    cs = torch.cuda.current_stream(dev)
+    hs, ds = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    host_x = torch.empty(sim.x.shape, dtype=sim.x.dtype).pin_memory()
+    host_x.copy_(sim.x.cpu())
+    # the step's result and the phase of the next step that rewrites it
+    if not sim.attention:
+        results, rewrite = [sim.qg, sim.kg, sim.vg], "exchange_in"   # the unpacked Q/K/V
+    elif sim.wl.U > 1:
+        results, rewrite = [sim.y], "exchange_out"                   # after the reverse exchange
+    else:
+        results, rewrite = [sim.out], "attend"
+    host_y = [torch.empty(r.shape, dtype=r.dtype).pin_memory() for r in results]
+    # the attention output is rewritten by the next step's attention, which starts
+    # right after the next exchange: read it back from a snapshot instead
+    stage = [torch.empty_like(r) for r in results] if rewrite == "attend" else None
+
+    def ev():
+        return torch.cuda.Event()
+
+    def steps(n):
+        in_free, out_free = None, None
+        for _ in range(n):
+            h2d_done, x_read, out_ready, d2h_done = ev(), ev(), ev(), ev()
+            with torch.cuda.stream(hs):
+                if in_free is not None:
+                    hs.wait_event(in_free)   # the previous exchange has read x
+                sim.x.copy_(host_x, non_blocking=True)
+                h2d_done.record(hs)
+            cs.wait_event(h2d_done)
+            for name in sim.PHASES:
+                if name == rewrite and stage is None and out_free is not None:
+                    cs.wait_event(out_free)  # the previous read-back has left the result buffer
+                run_phase(name)
+                if name == "exchange_in":
+                    x_read.record(cs)
+            src = results
+            if stage is not None:
+                if out_free is not None:
+                    cs.wait_event(out_free)  # the previous read-back has left the snapshot
+                for d, r in zip(stage, results):
+                    d.copy_(r, non_blocking=True)
+                src = stage
+            out_ready.record(cs)
+            with torch.cuda.stream(ds):
+                ds.wait_event(out_ready)
+                for h, r in zip(host_y, src):
+                    h.copy_(r, non_blocking=True)
+                d2h_done.record(ds)
+            in_free, out_free = x_read, d2h_done
+        cs.wait_event(out_free)  # the last read-back is inside the timed region
+
+    steps(max(1, args.warmup))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(cs)
+    hs.wait_event(e0)
+    steps(args.steps)
+    e1.record(cs)
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    flops = sim.attn_flops(inp.text_len)
+    return {"value": round(whole_job_tflops(flops * args.steps, world, e2e_ms), 3), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": host_x.numel() * host_x.element_size(),
+            "d2h_bytes_per_step": sum(h.numel() * h.element_size() for h in host_y),
+            "ms_per_step": round(e2e_ms / args.steps, 4),
+            "pipeline": "H2D / compute / D2H on three streams" + (", D2D snapshot of the output" if stage is not None else "")}
 
 
 def cpu_baseline_sample(wl_name: str, seconds: float, seed: int = 1234):
