@@ -47,27 +47,36 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_sha1() -> str:
+def kernel_source_sha1(files=("attention.cu", "ptx.cuh")) -> str:
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "diffusion_transformer_context_gb300", "csrc")
-    for fn in ("attention.cu", "ptx.cuh"):
+    for fn in files:
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
 
 
-def recorded_traffic(workload: str):
-    """DRAM bytes per attention launch from the committed ncu summary, or None
-    if the kernel source changed since the counters were taken."""
-    path = os.path.join(ROOT, "profiles", "attn_traffic.json")
+TRAFFIC_RECORDS = {
+    # roofline object -> (committed ncu summary, kernel sources it was taken on)
+    "attention": ("attn_traffic.json", ("attention.cu", "ptx.cuh")),
+    "relayout": ("relayout_traffic.json", ("relayout.cu",)),
+}
+
+
+def recorded_traffic(workload: str, kind: str = "attention"):
+    """DRAM bytes per launch (attention) or per step (relayout: all its
+    launches) from the committed ncu summary, or None if the kernel source
+    changed since the counters were taken."""
+    fname, files = TRAFFIC_RECORDS[kind]
+    path = os.path.join(ROOT, "profiles", fname)
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
     entry = d.get(workload)
-    if not entry or entry.get("source_sha1") != kernel_source_sha1():
+    if not entry or entry.get("source_sha1") != kernel_source_sha1(files):
         return None
-    return entry.get("bytes_per_launch")
+    return entry.get("bytes_per_launch", entry.get("bytes_per_step"))
 
 
 # ------------------------------------------------------------------ clocks
@@ -540,7 +549,8 @@ def main():
                 "achieved": round(relayout_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(relayout_gbs / peaks["hbm_gbs"], 4), "peak_source": f"{peak_kind} hbm_gbs",
                 "ms": round(relayout_ms, 4), "algorithmic_bytes": relayout_bytes,
-                "reverse_ms": round(reverse_ms, 4), "reverse_bytes": sim.reverse_bytes(), "traffic": None}
+                "reverse_ms": round(reverse_ms, 4), "reverse_bytes": sim.reverse_bytes(),
+                "traffic": recorded_traffic(args.workload, "relayout")}
     config = {"workload": args.workload, "B": sim.wl.B, "S": sim.wl.S, "H": sim.wl.H, "D": sim.wl.D,
               "U": sim.wl.U, "A": sim.wl.A, "joint": sim.wl.joint, "virtual_ranks": sim.R,
               "l2": "flushed_between_steps" if sim.l2_flushed else "inputs_larger_than_l2",
