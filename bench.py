@@ -303,12 +303,15 @@ def run_e2e(sim, inp, args, world, dev, run_phase, barrier):
     e1.record(cs)
     barrier()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    # after the timed region: the host copy of the last step's result equals the device result
+    verified = all(torch.equal(h.to(dev), r) for h, r in zip(host_y, results))
     flops = sim.attn_flops(inp.text_len)
     return {"value": round(whole_job_tflops(flops * args.steps, world, e2e_ms), 3), "unit": "TFLOP/s",
             "h2d_bytes_per_step": host_x.numel() * host_x.element_size(),
             "d2h_bytes_per_step": sum(h.numel() * h.element_size() for h in host_y),
             "ms_per_step": round(e2e_ms / args.steps, 4),
-            "pipeline": "H2D / compute / D2H on three streams" + (", D2D snapshot of the output" if stage is not None else "")}
+            "pipeline": "H2D / compute / D2H on three streams" + (", D2D snapshot of the output" if stage is not None else ""),
+            "readback_verified": verified}
 
 
 def cpu_baseline_sample(wl_name: str, seconds: float, seed: int = 1234):

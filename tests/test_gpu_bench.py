@@ -1,0 +1,56 @@
+"""bench.py's output contract on a GPU: one JSON line with the metric, the
+roofline and relayout objects, the pipelined end-to-end leg (whose host copy
+of the result must equal the device result) and the launch count."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def run_bench(*args):
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], cwd=ROOT, capture_output=True,
+                         text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [line for line in out.stdout.splitlines() if line.startswith("{")]
+    assert len(lines) == 1, out.stdout
+    return json.loads(lines[0])
+
+
+@pytest.mark.gpu
+def test_attention_workload_line():
+    d = run_bench("--workload", "tiny", "--steps", "3", "--warmup", "3", "--no-cpu-baseline", "--no-clocks")
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "dtype", "data", "config", "roofline", "relayout", "gpu_launches", "e2e"):
+        assert key in d, key
+    assert d["unit"] == "TFLOP/s" and d["value"] > 0
+    assert d["steps"] == 3 and d["n_gpus"] == 1 and d["scaling"] == "weak"
+    r = d["roofline"]
+    assert r["bound"] == "tensor" and r["achieved"] > 0 and r["peak"] > 0
+    assert r["frac"] == pytest.approx(r["achieved"] / r["peak"], abs=1e-4)  # rounded to 4 places
+    assert d["gpu_launches"] > 0
+    e = d["e2e"]
+    assert e["readback_verified"] is True
+    assert e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0 and e["value"] > 0
+
+
+@pytest.mark.gpu
+def test_layout_workload_line():
+    d = run_bench("--workload", "pack", "--steps", "3", "--warmup", "3", "--no-cpu-baseline", "--no-clocks")
+    assert d["unit"] == "GB/s" and d["value"] > 0
+    assert d["roofline"]["bound"] == "hbm"
+    assert d["config"]["l2"] == "flushed_between_steps"
+    assert d["e2e"]["readback_verified"] is True
+    assert d["e2e"]["unit"] == "GB/s"
+
+
+@pytest.mark.gpu
+def test_attention_output_snapshot_path():
+    # U = 1: the attention output is read back from a device snapshot
+    d = run_bench("--workload", "wan480", "--steps", "3", "--warmup", "3", "--no-cpu-baseline", "--no-clocks")
+    assert "snapshot" in d["e2e"]["pipeline"]
+    assert d["e2e"]["readback_verified"] is True
+    assert d["roofline"]["algorithmic_flops_per_launch"] == pytest.approx(4.0 * 12 * 32760 * 32760 * 128)
