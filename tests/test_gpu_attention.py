@@ -208,8 +208,10 @@ def test_balanced_schedule_matches_per_unit(ctx, B, Sq, Sk, H):
     """The key-split schedule (units cut between SMs, merged by log-sum-exp)
     agrees with one CTA per unit to fp32 rounding of the merge: same bf16
     output up to one ulp, LSE to 1e-5. Shapes: one rank of the Wan-like 480p
-    layer (192 units on the SMs: every unit split), a single unit split over
-    many SMs, and uneven wave remainders."""
+    layer (192 units: one whole wave, the 40 left over each cut into ~4
+    pieces), a single unit split over many SMs, and uneven wave remainders
+    where the last whole wave is split too (fewer than 32 key blocks per SM
+    in the leftover units alone)."""
     gen = torch.Generator().manual_seed(21)
     q, k, v = (workloads.randn(s, gen).cuda() for s in ((B, Sq, H, 128), (B, Sk, H, 128), (B, Sk, H, 128)))
     o1, l1 = torch.empty_like(q), torch.empty((B, H, Sq), device="cuda")
