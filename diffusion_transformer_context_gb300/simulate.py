@@ -22,6 +22,12 @@ of Q, K, V [B, S, H, D]. One step runs, through the C ABI only:
      ctx_unpack_out_ex for every rank (at U = 1 the output rows already are the
      sequence-sharded result and step 5 is the identity).
 
+The per-rank layout launches of a step (every rank's pack, every rank's
+unpack) are issued on parallel streams, forked from and joined back into the
+caller's stream: on a real deployment every rank runs its own on its own GPU
+at the same time, and on one GPU the concurrent launches share the SMs
+instead of queueing one behind the other.
+
 Joint (text) keys and values are inputs every rank already holds; they are
 written once, head-sliced, after the S image rows of each gathered K/V buffer
 (the "re-attach" of the same page), and the merged key mask [B, S + joint]
@@ -71,6 +77,23 @@ class SimLayer:
             self.osend = torch.empty((A, U, U, ochunk), **kw)
             self.orecv = torch.empty_like(self.osend)
             self.y = torch.empty((R, B, S_l, H, D), **kw)
+        # one stream per simulated rank (at most 8), for the per-rank layout launches
+        self.lanes = [torch.cuda.Stream(self.dev) for _ in range(min(R, 8))]
+
+    def _per_rank(self, stream, launch):
+        """Runs launch(g, s) for every rank g on the rank streams, forked from
+        and joined back into `stream` (default: the current stream)."""
+        base = stream if stream is not None else torch.cuda.current_stream(self.dev)
+        fork = torch.cuda.Event()
+        fork.record(base)
+        for lane in self.lanes:
+            lane.wait_event(fork)
+        for g in range(self.R):
+            launch(g, self.lanes[g % len(self.lanes)])
+        for lane in self.lanes:
+            done = torch.cuda.Event()
+            done.record(lane)
+            base.wait_event(done)
 
     # ---------------------------------------------------------- inputs
     def load(self, inp, pinned: bool = False):
@@ -99,18 +122,22 @@ class SimLayer:
         wl = self.wl
         U, A, B, S, D = wl.U, wl.A, wl.B, wl.S, wl.D
         S_l, h_l, Sk = self.S_l, self.h_l, self.Sk
-        for g in range(self.R):
+
+        def pack(g, s):
             a, u = divmod(g, U)
             x = self.x[g]
-            ctx_pack_qkv_ex(x[0], x[1], x[2], self.send[a, u], U, self.layout, stream=stream)
-        if U > 1:
-            ctx_sim_all_to_all(self.send, self.recv, A, U, stream=stream)
-        for g in range(self.R):
+            ctx_pack_qkv_ex(x[0], x[1], x[2], self.send[a, u], U, self.layout, stream=s)
+
+        def unpack(g, s):
             a, u = divmod(g, U)
             r0 = a * U * S_l
             ctx_unpack_qkv_ex(self.recv[a, u], self.qg[u, :, r0:], self.kg[u, :, r0:], self.vg[u, :, r0:], U, B,
-                              S_l, h_l, D, self.layout, q_batch_stride_rows=S, kv_batch_stride_rows=Sk,
-                              stream=stream)
+                              S_l, h_l, D, self.layout, q_batch_stride_rows=S, kv_batch_stride_rows=Sk, stream=s)
+
+        self._per_rank(stream, pack)
+        if U > 1:
+            ctx_sim_all_to_all(self.send, self.recv, A, U, stream=stream)
+        self._per_rank(stream, unpack)
 
     def attend(self, stream=None):
         """Step 4: local-Q / global-KV attention of every rank."""
@@ -134,15 +161,19 @@ class SimLayer:
         S_l, h_l = self.S_l, self.h_l
         if not self.attention or U == 1:
             return
-        if not self.fuse_reverse:
-            for g in range(self.R):
-                a, u = divmod(g, U)
-                ctx_pack_out(self.out[u, :, a * U * S_l:], self.osend[a, u].view(U, B, S_l, h_l, D), U,
-                             o_batch_stride_rows=S, stream=stream)
-        ctx_sim_all_to_all(self.osend, self.orecv, A, U, stream=stream)
-        for g in range(self.R):
+        def pack_out(g, s):
             a, u = divmod(g, U)
-            ctx_unpack_out_ex(self.orecv[a, u].view(U, B, S_l, h_l, D), self.y[g], U, stream=stream)
+            ctx_pack_out(self.out[u, :, a * U * S_l:], self.osend[a, u].view(U, B, S_l, h_l, D), U,
+                         o_batch_stride_rows=S, stream=s)
+
+        def unpack_out(g, s):
+            a, u = divmod(g, U)
+            ctx_unpack_out_ex(self.orecv[a, u].view(U, B, S_l, h_l, D), self.y[g], U, stream=s)
+
+        if not self.fuse_reverse:
+            self._per_rank(stream, pack_out)
+        ctx_sim_all_to_all(self.osend, self.orecv, A, U, stream=stream)
+        self._per_rank(stream, unpack_out)
 
     PHASES = ("exchange_in", "attend", "exchange_out")
 
