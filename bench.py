@@ -385,8 +385,11 @@ def run_reference(args, rank):
     oracle.build()
     wl = workloads.WORKLOADS[args.workload]
     inp = workloads.make_inputs(wl)
-    h_l = wl.h_l
     u16 = workloads.as_u16
+    if not wl.attention:
+        run_reference_layout(args, wl, inp)
+        return
+    h_l = wl.h_l
     q, k, v = u16(inp.q[:, :, :h_l]), u16(inp.k[:, :, :h_l]), u16(inp.v[:, :, :h_l])
     mask = None
     if wl.joint:
@@ -424,6 +427,40 @@ def run_reference(args, rank):
                              "sample": f"{n_rows} random query rows of {args.workload} per step, all keys"},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_reference_layout(args, wl, inp):
+    """--impl reference on a layout-only workload: the oracle's pack and unpack
+    of one rank per step, in GB/s of algorithmic read + write bytes."""
+    import oracle
+    import workloads
+
+    u16 = workloads.as_u16
+    shards = [[u16(inp.shard(t, g)) for t in (inp.q, inp.k, inp.v)] for g in range(wl.U * wl.A)]
+
+    def one_step(g):
+        t = time.perf_counter()
+        st = oracle.pack_qkv(*shards[g], wl.U)
+        oracle.unpack_qkv(st, wl.U)
+        return 2 * 2 * st.nbytes, time.perf_counter() - t
+
+    for i in range(args.warmup):
+        one_step(i % len(shards))
+    nb = dt = 0.0
+    for i in range(args.steps):
+        b, t = one_step(i % len(shards))
+        nb += b
+        dt += t
+    value = nb / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * dt / args.steps, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "u16 (bit copy)", "data": "synthetic",
+            "config": {"workload": args.workload, "sample": "pack + unpack of one rank per step"},
+            "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": "pack + unpack of one rank per step"},
+            "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
