@@ -261,3 +261,32 @@ def test_bounded_wait_times_out_and_context_survives(ctx, orc):
     q, k, v = (workloads.randn(s, gen) for s in ((1, 64, 1, 128), (1, 64, 1, 128), (1, 64, 1, 128)))
     O, L = _run(ctx, q, k, v)
     _check_full(orc, q, k, v, O, L)
+
+
+def test_beyond_2pow31_elements(ctx, orc):
+    """Q and O of more than 2^31 elements (64-bit output, LSE and TMA row
+    arithmetic): Q [1, 524365, 32, 128] (ragged last tile) against 130 keys.
+    Q is a seeded [1, 4096, 32, 128] block repeated along the rows on the
+    device, so the oracle computes any sampled row from the block."""
+    B, Sq, Sk, H, D, blk = 1, (1 << 19) + 77, 130, 32, 128, 4096
+    assert B * Sq * H * D > 2 ** 31
+    gen = torch.Generator().manual_seed(31)
+    q_blk, k, v = (workloads.randn(s, gen) for s in ((B, blk, H, D), (B, Sk, H, D), (B, Sk, H, D)))
+    reps = -(-Sq // blk)
+    q = q_blk.cuda().repeat(1, reps, 1, 1)[:, :Sq].contiguous()
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, Sq), dtype=torch.float32, device="cuda")
+    ctx.ctx_attn_lq_gkv(q, k.cuda(), v.cuda(), out, lse, workspace=ctx.attn_workspace(B, Sq, Sk, H, D))
+    assert ctx.ctx_device_status() == 0
+    rows_i = np.concatenate([workloads.sample_rows(Sq, 256), np.arange(Sq - 80, Sq)])
+    rng = np.random.default_rng(31)
+    bhi = np.stack([np.zeros(rows_i.size, np.int64), rng.integers(0, H, rows_i.size), rows_i], axis=1)
+    src = bhi.copy()
+    src[:, 2] %= blk  # row i of q is row i % blk of the block
+    eo, el = orc.attention_rows(u16(q_blk), u16(k), u16(v), src)
+    got_o = np.stack([out[0, i, h].float().cpu().numpy() for _, h, i in bhi])
+    got_l = np.array([float(lse[0, h, i]) for _, h, i in bhi])
+    err = np.abs(got_o - eo)
+    assert err.max() <= O_MAX, err.max()
+    assert err.mean() <= O_MEAN, err.mean()
+    assert np.abs(got_l - el).max() <= LSE_TOL

@@ -162,3 +162,33 @@ def test_unpack_out_ex_drops_pad_heads(ctx, orc, B, S_l, h_l, H, D, U):
     ctx.ctx_unpack_out_ex(recv.cuda(), y.t, U)
     torch.cuda.synchronize()
     assert y.intact() and np.array_equal(u16(y.t), orc.unpack_out_ex(u16(recv), U, H))
+
+
+def test_beyond_2pow31_elements(ctx, orc):
+    """Pack and unpack of tensors with more than 2^31 elements each (64-bit
+    run and vector indices): per-rank Q/K/V [1, 65541, 256, 128], U = 8
+    (staging 12.9 GB). Each input is a seeded [1, 512, 256, 128] block
+    repeated along the rows on the device; sampled rows (always the last ones)
+    are compared bit for bit with the oracle applied to the same rows."""
+    B, S_l, H, D, U, blk = 1, (1 << 16) + 5, 256, 128, 8, 512
+    h_l = H // U
+    assert B * S_l * H * D > 2 ** 31
+    gen = torch.Generator().manual_seed(32)
+    blocks = [_bits((B, blk, H, D), gen) for _ in range(3)]
+    reps = -(-S_l // blk)
+    q, k, v = (b.cuda().repeat(1, reps, 1, 1)[:, :S_l].contiguous() for b in blocks)
+    st = torch.empty((U, 3, B, S_l, h_l, D), dtype=torch.bfloat16, device="cuda")
+    ctx.ctx_pack_qkv(q, k, v, st, U)
+    del q, k, v
+    outs = [torch.empty((B, U * S_l, h_l, D), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    ctx.ctx_unpack_qkv(st, *outs, U)
+    torch.cuda.synchronize()
+    rows = np.concatenate([workloads.sample_rows(S_l, 64), np.arange(S_l - 8, S_l)])
+    for s in rows:
+        src = [u16(b[:, s % blk:s % blk + 1]) for b in blocks]
+        exp_st = orc.pack_qkv(*src, U)                      # [U, 3, B, 1, h_l, D]
+        assert np.array_equal(u16(st[:, :, :, s:s + 1]), exp_st), s
+        exp_un = orc.unpack_qkv(exp_st, U)                  # 3 x [B, U, h_l, D]: row r <- source r
+        for t in range(3):
+            got = u16(outs[t][:, s::S_l][:, :U])
+            assert np.array_equal(got, exp_un[t]), (s, t)
