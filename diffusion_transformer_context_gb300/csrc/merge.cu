@@ -8,6 +8,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cuda_fp16.h>
+#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -53,15 +54,15 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const uint4 *__restrict_
         uint4 ov[kUnr][PT];
 #pragma unroll
         for (int u = 0; u < kUnr; ++u) {
-            // rows are walked in LSE order: lrow = (b*H + h)*Sq + i of [B, H, Sq], so the
-            // LSE loads of neighbouring lane groups are contiguous; the output row is
-            // r = (b*Sq + i)*H + h of [B, Sq, H, D]
+            // rows are walked in output order r = (b*Sq + i)*H + h of [B, Sq, H, D], so a
+            // warp's rows are one contiguous stretch of every part (the bulk of the bytes);
+            // the LSE of a row sits at lrow = (b*H + h)*Sq + i of [B, H, Sq] (small, L2-resident)
             const long long l0 = r0 + static_cast<long long>(u) * kGroups + grp;
-            lrow[u] = l0 < rows ? l0 : rows - 1;  // clamp: loads stay in bounds
-            const long long bh = lrow[u] / Sq, i = lrow[u] - bh * Sq;
-            const long long b = bh / H, h = bh - b * H;
-            r[u] = l0 < rows ? (b * Sq + i) * H + h : rows;
-            const long long rr = (b * Sq + i) * H + h;
+            const long long rr = l0 < rows ? l0 : rows - 1;  // clamp: loads stay in bounds
+            const long long bi = rr / H, h = rr - bi * H;
+            const long long b = bi / Sq, i = bi - b * Sq;
+            lrow[u] = (b * H + h) * Sq + i;
+            r[u] = l0 < rows ? rr : rows;
 #pragma unroll
             for (int p = 0; p < PT; ++p) {
                 lv[u][p] = __ldg(lse_parts + p * rows + lrow[u]);
@@ -151,21 +152,47 @@ __global__ void __launch_bounds__(256) lse_merge_generic(const uint4 *__restrict
     }
 }
 
+// Blocks of `kernel` (256 threads) that fit on one SM at once, cached per
+// kernel and device: the grid is sized to what is resident together, so the
+// grid-stride loop shares the rows evenly instead of running a partial last
+// wave of blocks.
+template <typename K>
+int resident_blocks(K kernel, int dev)
+{
+    static int cache[64] = {0};
+    static std::mutex mu;
+    std::lock_guard<std::mutex> g(mu);
+    if (dev >= 0 && dev < 64 && cache[dev] > 0)
+        return cache[dev];
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, 256, 0) != cudaSuccess || n < 1)
+        n = 1;
+    if (dev >= 0 && dev < 64)
+        cache[dev] = n;
+    return n;
+}
+
 template <bool BF16>
 cudaError_t launch_typed_merge(const LseMergeArgs &a, int sms, cudaStream_t stream)
 {
+    int dev = 0;
+    cudaError_t derr = cudaGetDevice(&dev);
+    if (derr != cudaSuccess)
+        return derr;
     const long long rows = static_cast<long long>(a.B) * a.Sq * a.H;
     const int dv = a.D / 8;
     const uint4 *op = static_cast<const uint4 *>(a.o_parts);
     uint4 *out = static_cast<uint4 *>(a.out);
-    const long long cap = static_cast<long long>(sms) * 8;
-    auto grid_for = [&](long long rows_per_block) {
+    auto grid_for = [&](long long rows_per_block, int per_sm) {
+        const long long cap = static_cast<long long>(sms) * per_sm;
         return static_cast<unsigned>(std::max(1LL, std::min(cap, (rows + rows_per_block - 1) / rows_per_block)));
     };
     bool done = false;
 #define CTX_MERGE_CASE(DVV, PP)                                                                              \
     if (!done && dv == DVV && a.P == PP) {                                                                   \
-        lse_merge_kernel<BF16, DVV, PP><<<grid_for(8LL * (32 / DVV) * 4), 256, 0, stream>>>(                \
+        lse_merge_kernel<BF16, DVV, PP><<<grid_for(8LL * (32 / DVV) * 4,                                     \
+                                                    resident_blocks(lse_merge_kernel<BF16, DVV, PP>, dev)),   \
+                                          256, 0, stream>>>(                                                  \
             op, a.lse_parts, out, a.lse, rows, a.Sq, a.H);                                                   \
         done = true;                                                                                         \
     }
@@ -175,7 +202,8 @@ cudaError_t launch_typed_merge(const LseMergeArgs &a, int sms, cudaStream_t stre
 #undef CTX_MERGE_DV
 #undef CTX_MERGE_CASE
     if (!done)
-        lse_merge_generic<BF16><<<grid_for(256 / std::max(1, dv)), 256, 0, stream>>>(op, a.lse_parts, a.P, out,
+        lse_merge_generic<BF16><<<grid_for(256 / std::max(1, dv), resident_blocks(lse_merge_generic<BF16>, dev)),
+                                  256, 0, stream>>>(op, a.lse_parts, a.P, out,
                                                                                      a.lse, rows, a.Sq, a.H, dv);
     return cudaGetLastError();
 }
