@@ -522,7 +522,8 @@ def run_merge_bench(args):
             "gpu_launches": args.steps, "clocks": clocks,
             "e2e": {"value": round(nbytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                     "h2d_bytes_per_step": oh.numel() * 2 + lh.numel() * 4,
-                    "d2h_bytes_per_step": outh.numel() * 2, "ms_per_step": round(e2e_ms, 4)}}
+                    "d2h_bytes_per_step": outh.numel() * 2, "ms_per_step": round(e2e_ms, 4),
+                    "pipeline": "copies and compute one after another"}}
     if not args.no_cpu_baseline:
         import oracle
         n = 4096  # rows of the sample
@@ -533,6 +534,113 @@ def run_merge_bench(args):
         sample_bytes = nbytes * (n // H) / Sq
         line["cpu_baseline"] = {"value": round(sample_bytes / dt / 1e9, 3), "unit": "GB/s", "cores": 1,
                                 "kind": "oracle", "sample": f"first {n // H} query rows of every head"}
+    print(json.dumps(line), flush=True)
+
+
+VARLEN_DOCS = (12288, 8192, 6144, 4096, 2048)  # tokens per packed document (sum 32768)
+
+
+def run_varlen_bench(args):
+    """--kernel varlen: packed variable-length documents under AllGather-KV.
+    One packed sequence of 32768 tokens holds five documents (VARLEN_DOCS),
+    12 heads, D = 128, over A = 8 ranks: every rank remaps the global query
+    boundaries to its span of 4096 rows (ctx_varlen_remap, on the device) and
+    attends the whole documents' keys (ctx_attn_varlen); the eight ranks'
+    launches go out on parallel streams. Work: sum over documents of
+    4 * len^2 * H * D FLOP per step."""
+    import numpy as np
+    import torch
+
+    import workloads
+    import diffusion_transformer_context_gb300 as ctx
+
+    S, H, D, A = sum(VARLEN_DOCS), 12, 128, 8
+    S_l = S // A
+    gen = torch.Generator().manual_seed(workloads.SEED)
+    q_h, k_h, v_h = (workloads.randn((S, H, D), gen) for _ in range(3))
+    q, k, v = q_h.cuda(), k_h.cuda(), v_h.cuda()
+    bounds = np.concatenate([[0], np.cumsum(VARLEN_DOCS)]).astype(np.int32)
+    cu = torch.from_numpy(bounds).cuda()
+    n_docs = len(VARLEN_DOCS)
+    cu_loc = [torch.empty(n_docs + 1, dtype=torch.int32, device="cuda") for _ in range(A)]
+    out = torch.empty((A, S_l, H, D), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((A, H, S_l), dtype=torch.float32, device="cuda")
+    lanes = [torch.cuda.Stream() for _ in range(A)]
+    flops = float(sum(4.0 * n * n * H * D for n in VARLEN_DOCS))
+
+    def step():
+        base = torch.cuda.current_stream()
+        fork = torch.cuda.Event()
+        fork.record(base)
+        for r, s in enumerate(lanes):
+            s.wait_event(fork)
+            ctx.ctx_varlen_remap(cu, r * S_l, S_l, cu_loc[r], stream=s)
+            ctx.ctx_attn_varlen(q[r * S_l:(r + 1) * S_l], k, v, cu_loc[r], cu, S_l, out[r], lse[r], stream=s)
+            done = torch.cuda.Event()
+            done.record(s)
+            base.wait_event(done)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = ctx.ctx_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status: {ctx.ctx_status_string(st)}")
+    sampler = None if args.no_clocks else ClockSampler(0)
+    if sampler:
+        sampler.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    ms = e0.elapsed_time(e1) / args.steps
+    tflops = flops / (ms * 1e-3) / 1e12
+    # e2e: the packed Q/K/V in from pinned host memory, every rank's output back
+    qh, kh, vh = (t.pin_memory() for t in (q_h, k_h, v_h))
+    outh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    e0.record()
+    for _ in range(args.steps):
+        q.copy_(qh, non_blocking=True)
+        k.copy_(kh, non_blocking=True)
+        v.copy_(vh, non_blocking=True)
+        step()
+        outh.copy_(out, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    peaks, kind = load_peaks()
+    line = {"metric": METRIC, "value": round(tflops, 3), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "varlen", "documents": list(VARLEN_DOCS), "S": S, "H": H, "D": D, "A": A,
+                       "l2": "inputs_larger_than_l2", "launch": "8 ranks on parallel streams"},
+            "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel (varlen)", "achieved": round(tflops, 2),
+                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": round(tflops / peaks["bf16_tflops"], 4),
+                         "peak_source": f"{kind} bf16_tflops (burst)", "algorithmic_flops_per_step": flops,
+                         "traffic": None},
+            "gpu_launches": 2 * A * args.steps, "clocks": clocks,
+            "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": 3 * qh.numel() * 2, "d2h_bytes_per_step": outh.numel() * 2,
+                    "ms_per_step": round(e2e_ms, 4), "pipeline": "copies and compute one after another"}}
+    if not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        d0 = VARLEN_DOCS[0]
+        u16 = workloads.as_u16
+        qd, kd, vd = (u16(t[:d0].unsqueeze(0)) for t in (q_h, k_h, v_h))
+        rng = np.random.default_rng(workloads.SEED)
+        n = 512
+        bhi = np.stack([np.zeros(n, np.int64), rng.integers(0, H, n), rng.integers(0, d0, n)], axis=1)
+        t = time.perf_counter()
+        oracle.attention_rows(qd, kd, vd, bhi)
+        dt = time.perf_counter() - t
+        line["cpu_baseline"] = {"value": round(4.0 * d0 * D * n / dt / 1e12, 6), "unit": "TFLOP/s",
+                                "cores": oracle.num_threads(), "kind": "oracle",
+                                "sample": f"{n} random query rows of the {d0}-token document, all its keys"}
     print(json.dumps(line), flush=True)
 
 
@@ -548,7 +656,7 @@ def main():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--unbalanced", action="store_true", help="attention without workspace: one CTA per unit")
     ap.add_argument("--eager", action="store_true", help="launch every kernel from Python instead of CUDA graphs")
-    ap.add_argument("--kernel", default=None, choices=["lse_merge"], help="time one kernel alone")
+    ap.add_argument("--kernel", default=None, choices=["lse_merge", "varlen"], help="time one kernel alone")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=64)
     args = ap.parse_args()
@@ -565,6 +673,10 @@ def main():
     if args.kernel == "lse_merge":
         if rank == 0:
             run_merge_bench(args)
+        return
+    if args.kernel == "varlen":
+        if rank == 0:
+            run_varlen_bench(args)
         return
 
     import torch
