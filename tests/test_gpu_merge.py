@@ -19,7 +19,8 @@ def ctx():
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
-@pytest.mark.parametrize("P,B,Sq,H,D", [(2, 1, 300, 3, 128), (5, 2, 17, 1, 64), (1, 1, 8, 2, 8), (3, 1, 4095, 12, 128)])
+@pytest.mark.parametrize("P,B,Sq,H,D", [(2, 1, 300, 3, 128), (5, 2, 17, 1, 64), (1, 1, 8, 2, 8), (3, 1, 4095, 12, 128),
+                                       (4, 2, 100, 5, 128), (2, 3, 33, 7, 64)])
 def test_merge_matches_oracle(ctx, orc, P, B, Sq, H, D, dtype):
     gen = torch.Generator().manual_seed(51)
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float16

@@ -85,8 +85,8 @@ def _check(O, L, eO, eL):
     assert np.abs(L[fin] - eL[fin]).max() <= LSE_TOL
 
 
-@pytest.mark.parametrize("D", [128, 64])
-def test_varlen_attention_against_oracle(ctx, orc, D):
+@pytest.mark.parametrize("D,dtype", [(128, "bf16"), (64, "bf16"), (128, "fp16")])
+def test_varlen_attention_against_oracle(ctx, orc, D, dtype):
     gen = torch.Generator().manual_seed(91)
     H = 3
     q_lens = [300, 0, 17, 513, 128, 1]
@@ -94,9 +94,9 @@ def test_varlen_attention_against_oracle(ctx, orc, D):
     cu_q = np.concatenate([[0], np.cumsum(q_lens)]).tolist()
     cu_k = np.concatenate([[0], np.cumsum(k_lens)]).tolist()
     Sq, Sk = cu_q[-1] + 40, cu_k[-1] + 3           # padding rows / keys after the documents
-    q, k, v = (workloads.randn(s, gen) for s in ((Sq, H, D), (Sk, H, D), (Sk, H, D)))
+    q, k, v = (workloads.randn(s, gen, dtype) for s in ((Sq, H, D), (Sk, H, D), (Sk, H, D)))
     O, L = _run_varlen(ctx, q, k, v, cu_q, cu_k, max(q_lens))
-    eO, eL = orc.attention_varlen(u16(q), u16(k), u16(v), cu_q, cu_k)
+    eO, eL = orc.attention_varlen(u16(q), u16(k), u16(v), cu_q, cu_k, dtype=dtype)
     _check(O, L, eO, eL)
 
 
