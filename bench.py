@@ -567,6 +567,9 @@ def run_varlen_bench(args):
     lse = torch.empty((A, H, S_l), dtype=torch.float32, device="cuda")
     lanes = [torch.cuda.Stream() for _ in range(A)]
     flops = float(sum(4.0 * n * n * H * D for n in VARLEN_DOCS))
+    # the eight simulated ranks share the GPU concurrently, so each call runs one CTA per
+    # unit; one rank alone (as on its own GPU) is also timed with the balanced schedule
+    ws0 = ctx.varlen_workspace(n_docs, S_l, H, D)
 
     def step():
         base = torch.cuda.current_stream()
@@ -598,6 +601,25 @@ def run_varlen_bench(args):
     clocks = sampler.stop() if sampler else None
     ms = e0.elapsed_time(e1) / args.steps
     tflops = flops / (ms * 1e-3) / 1e12
+
+    # one rank alone (a deployment runs one rank per GPU): rank 0, balanced and one CTA per unit
+    def one_rank(ws):
+        ctx.ctx_varlen_remap(cu, 0, S_l, cu_loc[0])
+        for _ in range(3):
+            ctx.ctx_attn_varlen(q[:S_l], k, v, cu_loc[0], cu, S_l, out[0], lse[0], workspace=ws)
+        e0.record()
+        for _ in range(args.steps):
+            ctx.ctx_attn_varlen(q[:S_l], k, v, cu_loc[0], cu, S_l, out[0], lse[0], workspace=ws)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / args.steps
+
+    lens0 = np.clip(np.minimum(bounds[1:], S_l) - bounds[:-1], 0, None)
+    flops0 = float(sum(4.0 * int(lq) * int(n) * H * D for lq, n in zip(lens0, VARLEN_DOCS)))
+    ms_bal, ms_unit = one_rank(ws0), one_rank(None)
+    one_rank_line = {"rank": 0, "flops": flops0,
+                     "balanced_tflops": round(flops0 / (ms_bal * 1e-3) / 1e12, 1),
+                     "one_cta_per_unit_tflops": round(flops0 / (ms_unit * 1e-3) / 1e12, 1)}
     # e2e: the packed Q/K/V in from pinned host memory, every rank's output back
     qh, kh, vh = (t.pin_memory() for t in (q_h, k_h, v_h))
     outh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -616,7 +638,9 @@ def run_varlen_bench(args):
             "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": "varlen", "documents": list(VARLEN_DOCS), "S": S, "H": H, "D": D, "A": A,
-                       "l2": "inputs_larger_than_l2", "launch": "8 ranks on parallel streams"},
+                       "l2": "inputs_larger_than_l2", "launch": "8 ranks on parallel streams",
+                       "attn_schedule": "one CTA per unit (8 concurrent ranks)"},
+            "one_rank": one_rank_line,
             "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel (varlen)", "achieved": round(tflops, 2),
                          "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": round(tflops / peaks["bf16_tflops"], 4),

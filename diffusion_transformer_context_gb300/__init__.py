@@ -41,7 +41,8 @@ SIGNATURES = {
     "ctx_unpack_out": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "ctx_lse_merge": (_I, [_P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P]),
     "ctx_varlen_remap": (_I, [_P, _I, _LL, _LL, _P, _P, _P, _P]),
-    "ctx_attn_varlen": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _F, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "ctx_attn_varlen": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _F, _P, _P, _P, _LL, _I, _I, _I, _I, _I, _P]),
+    "ctx_attn_varlen_workspace_size": (_LL, [_I, _I, _I, _I]),
     "ctx_status_string": (ctypes.c_char_p, [_I]),
     "ctx_device_status": (_I, [_P]),
     "ctx_last_cuda_error": (_I, []),
@@ -250,16 +251,31 @@ def ctx_varlen_remap(cu_seqlens_q, span_begin: int, span_len: int, cu_seqlens_q_
 
 
 def ctx_attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, out, lse=None, key_mask=None,
-                    scale: float | None = None, stream=None):
-    """q [Sq,H,D], k/v [Sk,H,D], int32 cu tensors [n_docs+1] -> out [Sq,H,D], lse [H,Sq]."""
+                    scale: float | None = None, workspace=None, stream=None):
+    """q [Sq,H,D], k/v [Sk,H,D], int32 cu tensors [n_docs+1] -> out [Sq,H,D], lse [H,Sq]; `workspace`: a
+    zero-filled uint8 device tensor of ctx_attn_varlen_workspace_size(...) bytes for the balanced schedule."""
     Sq, H, D = q.shape
     Sk = k.shape[0]
     s = float("nan") if scale is None else float(scale)
+    wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check("ctx_attn_varlen", lib().ctx_attn_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q),
                                                     _ptr(cu_seqlens_k), cu_seqlens_q.numel() - 1, max_seqlen_q,
-                                                    _ptr(key_mask), s, _ptr(out), _ptr(lse), Sq, Sk, H, D,
-                                                    _dtype(q), _stream(stream)))
+                                                    _ptr(key_mask), s, _ptr(out), _ptr(lse), _ptr(workspace), wsb,
+                                                    Sq, Sk, H, D, _dtype(q), _stream(stream)))
     return out
+
+
+def ctx_attn_varlen_workspace_size(n_docs: int, max_seqlen_q: int, H: int, D: int) -> int:
+    n = lib().ctx_attn_varlen_workspace_size(n_docs, max_seqlen_q, H, D)
+    if n < 0:
+        raise CtxError("ctx_attn_varlen_workspace_size", 1)
+    return n
+
+
+def varlen_workspace(n_docs: int, max_seqlen_q: int, H: int, D: int, device="cuda"):
+    """A zero-filled workspace tensor of the size the balanced varlen schedule needs."""
+    n = ctx_attn_varlen_workspace_size(n_docs, max_seqlen_q, H, D)
+    return torch.zeros(max(n, 256), dtype=torch.uint8, device=device)
 
 
 def ctx_device_status(stream=None) -> int:

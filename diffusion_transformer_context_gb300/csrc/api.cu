@@ -587,8 +587,8 @@ ctx_status ctx_varlen_remap(const int *cu_seqlens_q, int n_docs, long long span_
 
 ctx_status ctx_attn_varlen(const void *q, const void *k, const void *v, const int *cu_seqlens_q,
                            const int *cu_seqlens_k, int n_docs, int max_seqlen_q, const unsigned char *key_mask,
-                           float scale, void *out, float *lse, int Sq, int Sk, int H, int D, ctx_dtype dtype,
-                           void *stream)
+                           float scale, void *out, float *lse, void *workspace, long long workspace_bytes, int Sq,
+                           int Sk, int H, int D, ctx_dtype dtype, void *stream)
 {
     if (!q || !k || !v || !out || !cu_seqlens_q || !cu_seqlens_k || !valid_dtype(dtype) || n_docs <= 0 ||
         max_seqlen_q <= 0)
@@ -603,26 +603,37 @@ ctx_status ctx_attn_varlen(const void *q, const void *k, const void *v, const in
         scale = 1.0f / std::sqrt(static_cast<float>(D));
     if (!std::isfinite(scale) || !(scale > 0.f))
         return CTX_ERR_INVALID_ARG;
+    if (workspace && workspace_bytes <= 0)
+        return CTX_ERR_INVALID_ARG;
     if (D % 8 != 0 || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
         (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) ||
-        (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u))
+        (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return CTX_ERR_MISALIGNED;
     if (D != 64 && D != 128)
         return CTX_ERR_UNSUPPORTED;
     const Extent eo = extent(out, nq * 2);
     const Extent el = lse ? extent(lse, static_cast<long long>(H) * Sq * 4) : Extent{0, 0};
+    const Extent ew = workspace ? extent(workspace, workspace_bytes) : Extent{0, 0};
     const Extent ins[] = {extent(q, nq * 2), extent(k, nk * 2), extent(v, nk * 2),
                           key_mask ? extent(key_mask, Sk) : Extent{0, 0},
                           extent(cu_seqlens_q, (static_cast<long long>(n_docs) + 1) * 4),
                           extent(cu_seqlens_k, (static_cast<long long>(n_docs) + 1) * 4)};
     for (const Extent &x : ins)
-        if (overlap(eo, x) || overlap(el, x))
+        if (overlap(eo, x) || overlap(el, x) || overlap(ew, x))
             return CTX_ERR_ALIASING;
-    if (overlap(eo, el))
+    if (overlap(eo, el) || overlap(ew, eo) || overlap(ew, el))
         return CTX_ERR_ALIASING;
-    ctx_status s = check_device_ptrs({q, k, v, out, lse, key_mask, cu_seqlens_q, cu_seqlens_k});
+    ctx_status s = check_device_ptrs({q, k, v, out, lse, key_mask, cu_seqlens_q, cu_seqlens_k, workspace});
     if (s != CTX_OK)
         return s;
+    if (workspace) {
+        cudaError_t e = cudaSuccess;
+        const long long need = ctx::varlen_workspace_size(n_docs, max_seqlen_q, H, D, &e);
+        if (e != cudaSuccess)
+            return cuda_fail(e);
+        if (workspace_bytes < need)
+            return CTX_ERR_INVALID_ARG;
+    }
     ctx::AttnArgs a{};
     a.q = q;
     a.k = k;
@@ -641,8 +652,25 @@ ctx_status ctx_attn_varlen(const void *q, const void *k, const void *v, const in
     a.cu_k = cu_seqlens_k;
     a.n_docs = n_docs;
     a.max_seqlen_q = max_seqlen_q;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
     cudaError_t e = ctx::launch_attention(a, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? CTX_OK : cuda_fail(e);
+}
+
+long long ctx_attn_varlen_workspace_size(int n_docs, int max_seqlen_q, int H, int D)
+{
+    long long units = (static_cast<long long>(max_seqlen_q) + 255) / 256;
+    if (n_docs <= 0 || max_seqlen_q <= 0 || !mul_ok(units, H) || !mul_ok(units, n_docs) ||
+        units > 0x7fffffffLL || (D != 64 && D != 128))
+        return -1;
+    cudaError_t e = cudaSuccess;
+    const long long bytes = ctx::varlen_workspace_size(n_docs, max_seqlen_q, H, D, &e);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    return bytes;
 }
 
 ctx_status ctx_lse_merge(const void *o_parts, const float *lse_parts, int P, void *out, float *lse, int B, int Sq,

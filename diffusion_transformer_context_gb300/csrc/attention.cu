@@ -58,6 +58,9 @@ struct Params {
     const int *cu_q;       // packed varlen: [n_docs + 1] local query boundaries (device), else NULL
     const int *cu_k;       // packed varlen: [n_docs + 1] key boundaries (device)
     int varlen;            // 1: units are (query-tile pair, head, document)
+    int n_docs;            // packed varlen: documents
+    const long long *var_prefix;  // packed varlen, balanced: [n_docs + 1] first key-block iteration of
+                                  // every document (written on the device before the launch), else NULL
     int blk_s, blk_u, blk_b;  // > 0: out is the reverse exchange's send buffer (see out_row)
     int n_units;           // work units: (query-tile pair, head, batch or document)
     int grid;              // persistent CTAs
@@ -90,10 +93,13 @@ struct Layout {
     static constexpr int kAlloc = kBytes + 1024;    // room to align the base to 1024 B
 };
 
-// One contiguous run of key blocks [jb, je) of one work unit.
+// One contiguous run of key blocks [jb, je) of one work unit. first: the
+// unit's first iteration in the split order; nb: the unit's key blocks.
 struct Segment {
     int unit, jb, je, slot;
     bool full;
+    long long first;
+    int nb;
 };
 
 // Geometry of one work unit: 256 query rows [q0, min(q0 + 256, q_end)) of
@@ -157,8 +163,79 @@ __device__ __forceinline__ uint4 *out_row(const Params &p, int b, int h, int qro
 // share the same heads' K/V in L2), then an even share of the remaining
 // units' key blocks, cut at unit boundaries (so every SM finishes at the same
 // time; units cut between CTAs are merged by log-sum-exp).
+__device__ __forceinline__ long long tail_start(const Params &p, long long total, int c)
+{
+    return static_cast<long long>(c) * total / p.grid;
+}
+
+// CTA whose tail range holds tail iteration `it`.
+__device__ __forceinline__ int tail_cta_of(const Params &p, long long total, long long it)
+{
+    return static_cast<int>(((it + 1) * p.grid + total - 1) / total) - 1;
+}
+
+// Iterations shared by the split schedule: the tail of the dense schedule,
+// or every key block of every document in the balanced varlen schedule.
+__device__ __forceinline__ long long split_total(const Params &p)
+{
+    return p.var_prefix ? __ldg(p.var_prefix + p.n_docs) : p.tail_iters;
+}
+
+// Balanced packed varlen: the unit holding split iteration y (documents in
+// order, then heads, then query-tile pairs, then key blocks; empty units hold
+// no iteration), its first iteration and its key blocks. The per-document
+// counts follow unit_geom exactly.
+__device__ __forceinline__ void var_unit_at(const Params &p, long long y, int &unit, long long &ustart, int &nb)
+{
+    int lo = 0, hi = p.n_docs - 1;
+    while (lo < hi) {  // the last document whose first iteration is <= y (skips empty ones)
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(p.var_prefix + mid) <= y)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const int d = lo;
+    const int qs = min(max(__ldg(p.cu_q + d), 0), p.Sq);
+    const int q_len = min(max(__ldg(p.cu_q + d + 1), qs), p.Sq) - qs;
+    const int k0 = min(max(__ldg(p.cu_k + d), 0), p.Sk);
+    const int k_len = min(max(__ldg(p.cu_k + d + 1), k0), p.Sk) - k0;
+    nb = (k_len + kBN - 1) / kBN;
+    const int nqp = min((q_len + kTiles * kBM - 1) / (kTiles * kBM), p.n_qpairs);
+    const long long off = y - __ldg(p.var_prefix + d);
+    const long long per_h = static_cast<long long>(nqp) * nb;
+    const int h = static_cast<int>(off / per_h);
+    const long long r = off - h * per_h;
+    const int qp = static_cast<int>(r / nb), blk = static_cast<int>(r - static_cast<long long>(qp) * nb);
+    unit = qp + p.n_qpairs * (h + p.H * d);
+    ustart = y - blk;
+}
+
 __device__ __forceinline__ bool segment_at(const Params &p, int c, int si, Segment &s)
 {
+    if (p.var_prefix) {
+        // balanced packed varlen: CTA c takes split iterations [x0, x1), cut at unit ends
+        const long long total = split_total(p);
+        const long long x0 = tail_start(p, total, c), x1 = tail_start(p, total, c + 1);
+        long long y = x0, ustart = 0;
+        int unit = 0, nb = 0;
+        for (int j = 0;; ++j) {
+            if (y >= x1)
+                return false;
+            var_unit_at(p, y, unit, ustart, nb);
+            if (j == si)
+                break;
+            y = ustart + nb;
+        }
+        s.unit = unit;
+        s.jb = static_cast<int>(y - ustart);
+        s.je = static_cast<int>(min(static_cast<long long>(nb), x1 - ustart));
+        s.full = (s.jb == 0 && s.je == nb);
+        s.slot = (si == 0) ? 2 * c : 2 * c + 1;
+        s.first = ustart;
+        s.nb = nb;
+        return true;
+    }
     if (si < p.dp_waves) {
         s.unit = si * p.grid + c;
         s.jb = 0;
@@ -171,6 +248,8 @@ __device__ __forceinline__ bool segment_at(const Params &p, int c, int si, Segme
         }
         s.full = true;
         s.slot = -1;
+        s.first = 0;
+        s.nb = s.je;
         return true;
     }
     const long long nb = p.n_kblocks;
@@ -188,6 +267,8 @@ __device__ __forceinline__ bool segment_at(const Params &p, int c, int si, Segme
     s.je = s.jb + static_cast<int>(end - start);
     s.full = (s.jb == 0 && s.je == p.n_kblocks);
     s.slot = (k == 0) ? 2 * c : 2 * c + 1;
+    s.first = u * nb;
+    s.nb = p.n_kblocks;
     return true;
 }
 
@@ -197,17 +278,6 @@ __device__ __forceinline__ int opaque(int i)
 {
     asm volatile("" : "+r"(i));
     return i;
-}
-
-__device__ __forceinline__ long long tail_start(const Params &p, int c)
-{
-    return static_cast<long long>(c) * p.tail_iters / p.grid;
-}
-
-// CTA whose tail range holds tail iteration `it`.
-__device__ __forceinline__ int tail_cta_of(const Params &p, long long it)
-{
-    return static_cast<int>(((it + 1) * p.grid + p.tail_iters - 1) / p.tail_iters) - 1;
 }
 
 // Bounded wait on an mbarrier phase. honor_abort: give up as soon as another
@@ -686,9 +756,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::mbar_arrive(o_empty + t);
                 __threadfence();
                 ptx::mbar_arrive(seg_done + t);
-                const long long ut = sg.unit - static_cast<long long>(p.dp_waves) * p.grid;
-                const long long first = ut * p.n_kblocks;
-                const int c_lo = tail_cta_of(p, first), c_hi = tail_cta_of(p, first + p.n_kblocks - 1);
+                const long long total = split_total(p);
+                const long long first = sg.first;  // the unit's first iteration in the split order
+                const int c_lo = tail_cta_of(p, total, first), c_hi = tail_cta_of(p, total, first + sg.nb - 1);
                 if (tile_leader) {
                     int last = 0;
                     if (wait_bar(seg_done + t, pc & 1, abort_flag, p)) {
@@ -709,12 +779,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // Last segment of this unit to finish: combine every segment by log-sum-exp.
                     float M = -INFINITY;
                     for (int cc = c_lo; cc <= c_hi; ++cc) {
-                        const int sl = (tail_start(p, cc) >= first) ? 2 * cc : 2 * cc + 1;
+                        const int sl = (tail_start(p, total, cc) >= first) ? 2 * cc : 2 * cc + 1;
                         M = fmaxf(M, __ldcg(p.part_ml + static_cast<size_t>(sl) * (kTiles * kBM) + prow).x);
                     }
                     float lsum = 0.f;
                     for (int cc = c_lo; cc <= c_hi; ++cc) {
-                        const int sl = (tail_start(p, cc) >= first) ? 2 * cc : 2 * cc + 1;
+                        const int sl = (tail_start(p, total, cc) >= first) ? 2 * cc : 2 * cc + 1;
                         const float2 ml = __ldcg(p.part_ml + static_cast<size_t>(sl) * (kTiles * kBM) + prow);
                         lsum += (ml.x == -INFINITY) ? 0.f : ptx::ex2_approx(ml.x - M) * ml.y;
                     }
@@ -727,7 +797,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int k = 0; k < 32; ++k)
                             o[k] = 0.f;
                         for (int cc = c_lo; cc <= c_hi; ++cc) {
-                            const int sl = (tail_start(p, cc) >= first) ? 2 * cc : 2 * cc + 1;
+                            const int sl = (tail_start(p, total, cc) >= first) ? 2 * cc : 2 * cc + 1;
                             const float2 ml = __ldcg(p.part_ml + static_cast<size_t>(sl) * (kTiles * kBM) + prow);
                             const float w = (ml.x == -INFINITY) ? 0.f : ptx::ex2_approx(ml.x - M);
                             const float4 *src = p.part_o + (static_cast<size_t>(sl) * (D / 4) + c0 * 8) * (kTiles * kBM) + prow;
@@ -860,6 +930,27 @@ Schedule plan(int B, int Sq, int Sk, int H, int sms, bool split)
     return s;
 }
 
+// Packed varlen: one unit per (query-tile pair of the longest document, head,
+// document). Without a split every unit gets a CTA; with one, a persistent grid
+// of one CTA per SM shares every key block of every unit evenly (the totals are
+// known only on the device; the plan kernel writes them).
+Schedule plan_varlen(int n_docs, int max_seqlen_q, int H, int sms, bool split)
+{
+    Schedule s{};
+    const int n_qpairs = (max_seqlen_q + kTiles * kBM - 1) / (kTiles * kBM);
+    s.n_units = n_qpairs * H * n_docs;
+    s.n_kblocks = 0;  // per document
+    s.grid = split ? sms : s.n_units;
+    s.dp_waves = split ? 0 : 1;
+    s.tail_iters = 0;
+    return s;
+}
+
+long long ws_prefix_bytes(int n_docs)
+{
+    return ((static_cast<long long>(n_docs) + 1) * 8 + 255) / 256 * 256;
+}
+
 long long ws_counter_bytes(const Schedule &s)
 {
     return (static_cast<long long>(s.n_units) * kTiles * 4 + 255) / 256 * 256;
@@ -900,10 +991,12 @@ cudaError_t launch_typed(const AttnArgs &a, cudaStream_t stream)
     if (err != cudaSuccess)
         return err;
     const bool varlen = a.cu_q != nullptr;
-    // varlen: one unit per (256 rows of the longest document, head, document), no split
-    const Schedule sc = varlen ? plan(a.n_docs, a.max_seqlen_q, a.Sk, a.H, sms, false)
+    // varlen: units are (256 rows of the longest document, head, document); without a
+    // workspace one CTA per unit, with one every SM takes an equal share of all key blocks
+    const bool vsplit = varlen && a.workspace != nullptr;
+    const Schedule sc = varlen ? plan_varlen(a.n_docs, a.max_seqlen_q, a.H, sms, vsplit)
                                : plan(a.B, a.Sq, a.Sk, a.H, sms, a.workspace != nullptr);
-    if (!varlen && a.workspace && a.workspace_bytes < ws_bytes(sc, D))
+    if (a.workspace && a.workspace_bytes < ws_bytes(sc, D) + (vsplit ? ws_prefix_bytes(a.n_docs) : 0))
         return cudaErrorInvalidValue;
     CUtensorMap mq, mk, mv;
     if ((err = make_map(&mq, a.q, a.B, a.Sq, a.H, D, BF16)) != cudaSuccess)
@@ -937,17 +1030,34 @@ cudaError_t launch_typed(const AttnArgs &a, cudaStream_t stream)
     if (err != cudaSuccess)
         return err;
     p.wait_limit_ns = kDefaultWaitLimitNs;
-    if (!varlen && a.workspace) {
+    p.n_docs = varlen ? a.n_docs : 0;
+    if (a.workspace) {
         uint8_t *ws = static_cast<uint8_t *>(a.workspace);
         p.counters = reinterpret_cast<int *>(ws);
         p.part_ml = reinterpret_cast<float2 *>(ws + ws_counter_bytes(sc));
         p.part_o = reinterpret_cast<float4 *>(ws + ws_counter_bytes(sc) + ws_ml_bytes(sc));
+    }
+    if (vsplit) {
+        long long *prefix = reinterpret_cast<long long *>(static_cast<uint8_t *>(a.workspace) + ws_bytes(sc, D));
+        if ((err = launch_varlen_plan(a.cu_q, a.cu_k, a.n_docs, a.Sq, a.Sk, a.H, p.n_qpairs, prefix, a.out, a.lse, D,
+                                      stream)) != cudaSuccess)
+            return err;
+        p.var_prefix = prefix;
     }
     attn_fwd_kernel<D, BF16><<<static_cast<unsigned>(sc.grid), kThreads, L::kAlloc, stream>>>(mq, mk, mv, p);
     return cudaGetLastError();
 }
 
 }  // namespace
+
+long long varlen_workspace_size(int n_docs, int max_seqlen_q, int H, int D, cudaError_t *err)
+{
+    const int sms = sm_count(err);
+    if (*err != cudaSuccess)
+        return -1;
+    const Schedule sc = plan_varlen(n_docs, max_seqlen_q, H, sms, true);
+    return ws_bytes(sc, D) + ws_prefix_bytes(n_docs);
+}
 
 long long attention_workspace_size(int B, int Sq, int Sk, int H, int D, cudaError_t *err)
 {

@@ -92,6 +92,14 @@ cudaError_t launch_lse_merge(const LseMergeArgs &a, cudaStream_t stream);
 cudaError_t launch_varlen_remap(const int *cu_g, int n_docs, long long lo, long long len, int *cu_l,
                                 const int *pad_in, int *pad_out, cudaStream_t stream);
 
+// Balanced packed varlen: per-document first split iteration into prefix[0..n_docs]
+// and out = 0 / lse = -inf for query rows of documents without keys.
+cudaError_t launch_varlen_plan(const int *cu_q, const int *cu_k, int n_docs, int Sq, int Sk, int H, int n_qpairs,
+                               long long *prefix, void *out, float *lse, int D, cudaStream_t stream);
+
+// Bytes of workspace the balanced packed-varlen attention needs on the current device.
+long long varlen_workspace_size(int n_docs, int max_seqlen_q, int H, int D, cudaError_t *err);
+
 // Records a CUDA error for ctx_last_cuda_error() on the calling thread.
 void record_cuda_error(cudaError_t e);
 

@@ -347,13 +347,34 @@ ctx_status ctx_varlen_remap(const int *cu_seqlens_q, int n_docs,
  *                are not computed).
  * key_mask     : NULL or [Sk] bytes, nonzero = attend (global key index).
  * out          : [Sq, H, D]; lse : NULL or [H, Sq] float32.
+ * workspace, workspace_bytes :
+ *                NULL / 0: one CTA per (256 query rows, head, document) unit.
+ *                Otherwise device memory of at least
+ *                ctx_attn_varlen_workspace_size(n_docs, max_seqlen_q, H, D)
+ *                bytes, 256-byte aligned, zero-filled before its first use: a
+ *                small plan kernel counts every document's key blocks on the
+ *                device, then a persistent grid (one CTA per SM) gives every SM
+ *                an equal share of all key blocks, cutting units between SMs
+ *                and merging the pieces by log-sum-exp (as ctx_attn_lq_gkv's
+ *                balanced schedule). A successful call leaves the arrival
+ *                counters zeroed; after CTX_ERR_TIMEOUT the workspace must be
+ *                re-zeroed. Calls that may run concurrently must not share one.
  */
 ctx_status ctx_attn_varlen(const void *q, const void *k, const void *v,
                            const int *cu_seqlens_q, const int *cu_seqlens_k,
                            int n_docs, int max_seqlen_q,
                            const unsigned char *key_mask, float scale,
-                           void *out, float *lse, int Sq, int Sk, int H, int D,
-                           ctx_dtype dtype, void *stream);
+                           void *out, float *lse, void *workspace,
+                           long long workspace_bytes, int Sq, int Sk, int H,
+                           int D, ctx_dtype dtype, void *stream);
+
+/*
+ * ctx_attn_varlen_workspace_size — bytes of workspace ctx_attn_varlen needs
+ * for its balanced schedule on the current device (it depends on the SM
+ * count, the number of documents and the longest document's query length).
+ * Returns -1 for invalid sizes or when no device can be queried.
+ */
+long long ctx_attn_varlen_workspace_size(int n_docs, int max_seqlen_q, int H, int D);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *ctx_status_string(ctx_status status);

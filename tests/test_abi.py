@@ -149,11 +149,17 @@ def test_varlen_validation(lib):
     f = lib.ctx_attn_varlen
     q, k, v, cq, ck, o, l = A0, A0 + MB, A0 + 2 * MB, A0 + 3 * MB, A0 + 3 * MB + 256, A0 + 4 * MB, A0 + 5 * MB
     nan = float("nan")
-    assert f(q, k, v, cq, ck, 0, 16, None, nan, o, l, 16, 16, 2, 128, 0, None) == INVALID   # no documents
-    assert f(q, k, v, cq, ck, 2, 0, None, nan, o, l, 16, 16, 2, 128, 0, None) == INVALID   # max_seqlen_q
-    assert f(q, k, v, cq, ck, 2, 16, None, nan, o, l, 16, 16, 2, 96, 0, None) == UNSUPPORTED
-    assert f(q, k, v, cq + 2, ck, 2, 16, None, nan, o, l, 16, 16, 2, 128, 0, None) == MISALIGNED
-    assert f(q, k, v, cq, ck, 2, 16, None, nan, cq, l, 16, 16, 2, 128, 0, None) == ALIASING
+    assert f(q, k, v, cq, ck, 0, 16, None, nan, o, l, None, 0, 16, 16, 2, 128, 0, None) == INVALID   # no documents
+    assert f(q, k, v, cq, ck, 2, 0, None, nan, o, l, None, 0, 16, 16, 2, 128, 0, None) == INVALID   # max_seqlen_q
+    assert f(q, k, v, cq, ck, 2, 16, None, nan, o, l, None, 0, 16, 16, 2, 96, 0, None) == UNSUPPORTED
+    assert f(q, k, v, cq + 2, ck, 2, 16, None, nan, o, l, None, 0, 16, 16, 2, 128, 0, None) == MISALIGNED
+    assert f(q, k, v, cq, ck, 2, 16, None, nan, cq, l, None, 0, 16, 16, 2, 128, 0, None) == ALIASING
+    ws = A0 + 8 * MB
+    assert f(q, k, v, cq, ck, 2, 16, None, nan, o, l, ws, 0, 16, 16, 2, 128, 0, None) == INVALID    # no size
+    assert f(q, k, v, cq, ck, 2, 16, None, nan, o, l, ws + 16, MB, 16, 16, 2, 128, 0, None) == MISALIGNED
+    assert f(q, k, v, cq, ck, 2, 16, None, nan, o, l, o, MB, 16, 16, 2, 128, 0, None) == ALIASING   # over out
+    assert lib.ctx_attn_varlen_workspace_size(0, 16, 2, 128) == -1
+    assert lib.ctx_attn_varlen_workspace_size(2, 16, 2, 96) == -1
     r = lib.ctx_varlen_remap
     assert r(cq, 0, 0, 8, ck, None, None, None) == INVALID
     assert r(cq, 2, -1, 8, ck, None, None, None) == INVALID

@@ -146,3 +146,114 @@ def test_allgather_shard_path_equals_unsplit(ctx, orc, A):
     assert torch.equal(torch.cat(lparts, dim=1), full_l)
     eO, eL = orc.attention_varlen(u16(q.cpu()), u16(k.cpu()), u16(v.cpu()), cu, cu)
     _check(full.float().cpu().numpy(), full_l.cpu().numpy(), eO, eL)
+
+
+def _varlen_pair(ctx, q, k, v, cu_q, cu_k, max_q, mask=None):
+    """The same packed varlen call with one CTA per unit and with the balanced
+    (key-split) schedule; the balanced one runs twice on one workspace."""
+    Sq, H, D = q.shape
+    cq = torch.tensor(cu_q, dtype=torch.int32, device="cuda")
+    ck = torch.tensor(cu_k, dtype=torch.int32, device="cuda")
+    m = None if mask is None else torch.from_numpy(mask).cuda()
+    o1 = torch.full((Sq, H, D), float("nan"), dtype=q.dtype, device="cuda")
+    l1 = torch.full((H, Sq), float("nan"), device="cuda")
+    ctx.ctx_attn_varlen(q, k, v, cq, ck, max_q, o1, l1, key_mask=m)
+    ws = ctx.varlen_workspace(len(cu_q) - 1, max_q, H, D)
+    outs = []
+    for _ in range(2):  # a second call on the same workspace: counters were left at zero
+        o2 = Guarded((Sq, H, D), q.dtype)
+        l2 = Guarded((H, Sq), torch.float32)
+        ctx.ctx_attn_varlen(q, k, v, cq, ck, max_q, o2.t, l2.t, key_mask=m, workspace=ws)
+        assert ctx.ctx_device_status() == 0
+        assert o2.intact() and l2.intact()
+        outs.append((o2.t, l2.t))
+    n_units = ((max_q + 255) // 256) * H * (len(cu_q) - 1)
+    assert int(ws[:n_units * 2 * 4].count_nonzero()) == 0
+    return (o1, l1), outs
+
+
+def _same_up_to_merge(a, b):
+    """One CTA per unit vs the split schedule: rows not written stay NaN in
+    both; written rows agree to fp32 rounding of the log-sum-exp merge."""
+    (o1, l1), (o2, l2) = a, b
+    assert torch.equal(torch.isnan(o1), torch.isnan(o2))
+    w = ~torch.isnan(o1)
+    d = (o1.float()[w] - o2.float()[w]).abs()
+    if d.numel():
+        assert float(d.max()) <= 2.0 ** -7 * max(1.0, float(o1.float()[w].abs().max()))
+    lw = ~torch.isnan(l1)
+    assert torch.equal(lw, ~torch.isnan(l2))
+    fin = torch.isfinite(l1) & lw
+    assert torch.equal(fin, torch.isfinite(l2) & lw)
+    if fin.any():
+        assert float((l1[fin] - l2[fin]).abs().max()) <= 1e-5
+
+
+@pytest.mark.parametrize("D,dtype", [(128, "bf16"), (64, "bf16"), (128, "fp16")])
+def test_balanced_varlen_matches_per_unit_and_oracle(ctx, orc, D, dtype):
+    """Documents of uneven lengths, an empty one, one without keys, one
+    without queries, padding rows after the last document."""
+    gen = torch.Generator().manual_seed(94)
+    H = 3
+    q_lens = [1300, 0, 17, 513, 128, 1, 40, 600]
+    k_lens = [2000, 50, 0, 1000, 129, 5, 0, 333]
+    cu_q = np.concatenate([[0], np.cumsum(q_lens)]).tolist()
+    cu_k = np.concatenate([[0], np.cumsum(k_lens)]).tolist()
+    Sq, Sk = cu_q[-1] + 40, cu_k[-1] + 3
+    q, k, v = (workloads.randn(s, gen, dtype).cuda() for s in ((Sq, H, D), (Sk, H, D), (Sk, H, D)))
+    a, outs = _varlen_pair(ctx, q, k, v, cu_q, cu_k, max(q_lens))
+    for b in outs:
+        _same_up_to_merge(a, b)
+    eO, eL = orc.attention_varlen(u16(q.cpu()), u16(k.cpu()), u16(v.cpu()), cu_q, cu_k, dtype=dtype)
+    _check(outs[0][0].float().cpu().numpy(), outs[0][1].cpu().numpy(), eO, eL)
+
+
+def test_balanced_varlen_with_mask_and_many_documents(ctx, orc):
+    gen = torch.Generator().manual_seed(95)
+    H, D = 2, 128
+    rng = np.random.default_rng(95)
+    lens = rng.integers(0, 700, 300).tolist()           # 300 documents, some empty
+    cu = np.concatenate([[0], np.cumsum(lens)]).tolist()
+    S = cu[-1]
+    q, k, v = (workloads.randn((S, H, D), gen).cuda() for _ in range(3))
+    mask = (rng.random(S) > 0.1).astype(np.uint8)
+    a, outs = _varlen_pair(ctx, q, k, v, cu, cu, max(lens), mask)
+    for b in outs:
+        _same_up_to_merge(a, b)
+    rows = workloads.sample_rows(S, 256)
+    eO, eL = orc.attention_varlen(u16(q.cpu()), u16(k.cpu()), u16(v.cpu()), cu, cu, mask)
+    got = outs[0][0].float().cpu().numpy()
+    err = np.abs(got[rows] - eO[rows])
+    assert err.max() <= O_MAX and err.mean() <= O_MEAN
+
+
+@pytest.mark.parametrize("A", [4, 8])
+def test_balanced_varlen_shard_path(ctx, orc, A):
+    """One rank of an AllGather-KV group at a time, balanced: concatenated
+    outputs equal the unsplit packed attention up to the merge rounding."""
+    gen = torch.Generator().manual_seed(96)
+    H, D = 4, 128
+    lens = [12288, 8192, 6144, 4096, 2048]
+    cu = np.concatenate([[0], np.cumsum(lens)]).tolist()
+    S = cu[-1]
+    q, k, v = (workloads.randn((S, H, D), gen).cuda() for _ in range(3))
+    cu_g = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    full = torch.empty_like(q)
+    full_l = torch.empty((H, S), device="cuda")
+    ctx.ctx_attn_varlen(q, k, v, cu_g, cu_g, max(lens), full, full_l)
+    span = S // A
+    ws = ctx.varlen_workspace(len(lens), span, H, D)
+    parts, lparts = [], []
+    for r in range(A):
+        loc = torch.empty_like(cu_g)
+        ctx.ctx_varlen_remap(cu_g, r * span, span, loc)
+        qr = q[r * span:(r + 1) * span].contiguous()
+        o = torch.empty_like(qr)
+        l = torch.empty((H, span), device="cuda")
+        ctx.ctx_attn_varlen(qr, k, v, loc, cu_g, span, o, l, workspace=ws)
+        parts.append(o)
+        lparts.append(l)
+    assert ctx.ctx_device_status() == 0
+    d = (torch.cat(parts).float() - full.float()).abs()
+    assert float(d.max()) <= 2.0 ** -7 * max(1.0, float(full.float().abs().max()))
+    assert float((torch.cat(lparts, dim=1) - full_l).abs().max()) <= 1e-5
