@@ -11,7 +11,8 @@
 //     keys into a two-stage ring (128-byte swizzled tiles, mbarrier
 //     complete_tx accounting);
 //   * warp 1 allocates 512 TMEM columns and runs the MMA loop as a whole warp
-//     (warp-uniform descriptors), one elected lane issuing every tcgen05.mma: S_t = Q_t K^T (A and B from shared memory, K-major) into
+//     (warp-uniform descriptors), one elected lane issuing every tcgen05.mma:
+//     S_t = Q_t K^T (A and B from shared memory, K-major) into
 //     TMEM columns [128t, 128t+128), and O_t += P_t V with P_t read from TMEM
 //     (it overwrites S_t as 16-bit pairs) and V from shared memory (MN-major)
 //     into columns [256 + Dt, 256 + D(t+1));
@@ -24,7 +25,11 @@
 //   * O is rescaled only when a row maximum grows by more than 2^8 (a stale
 //     maximum keeps every probability <= 2^8, exact after the final division),
 //     which the public FlashAttention-4 write-up calls conditional rescaling;
-//   * epilogue: O / l rounded to the input type, LSE = ln2 * (m + log2 l).
+//   * epilogue: O / l rounded to the input type, LSE = ln2 * (m + log2 l);
+//   * schedules: one CTA per work unit, or (given a workspace) a persistent
+//     grid of one CTA per SM that cuts units' key ranges between SMs and
+//     merges the pieces by log-sum-exp; for packed varlen documents the
+//     split iteration space is planned on the device (varlen.cu).
 // Every wait is bounded (%globaltimer); on expiry the kernel records a
 // timeout in the device status word, drains its own TMA loads and MMAs, frees
 // TMEM and returns.
