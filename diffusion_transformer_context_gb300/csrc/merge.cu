@@ -36,14 +36,19 @@ __device__ __forceinline__ void widen8(const uint4 &v, float *f)
 // every group merges kUnr rows per iteration. All PT segment LSEs and all PT
 // 16-byte chunks of those rows are loaded before any of them is used, so a
 // lane keeps PT*kUnr loads in flight and an iteration waits for one DRAM
-// round trip. Row indices are decomposed once per row.
-template <bool BF16, int DV, int PT>
-__global__ void __launch_bounds__(256) lse_merge_kernel(const uint4 *__restrict__ o_parts,
+// round trip. Row indices are decomposed once per row, in 32-bit arithmetic
+// when every row index fits (I32); with 64 registers a thread, four blocks
+// stay resident on an SM (three for four segments).
+__host__ __device__ constexpr int merge_unroll(int pt) { return pt <= 2 ? 4 : 2; }
+__host__ __device__ constexpr int merge_min_blocks(int pt) { return pt <= 3 ? 4 : 3; }
+
+template <bool BF16, int DV, int PT, bool I32>
+__global__ void __launch_bounds__(256, merge_min_blocks(PT)) lse_merge_kernel(const uint4 *__restrict__ o_parts,
                                                         const float *__restrict__ lse_parts, uint4 *out,
                                                         float *lse_out, long long rows, int Sq, int H)
 {
     constexpr int kGroups = 32 / DV;
-    constexpr int kUnr = 4;
+    constexpr int kUnr = merge_unroll(PT);
     const int lane = threadIdx.x & 31;
     const int grp = lane / DV, c = lane % DV;
     const long long warp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -59,9 +64,16 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const uint4 *__restrict_
             // the LSE of a row sits at lrow = (b*H + h)*Sq + i of [B, H, Sq] (small, L2-resident)
             const long long l0 = r0 + static_cast<long long>(u) * kGroups + grp;
             const long long rr = l0 < rows ? l0 : rows - 1;  // clamp: loads stay in bounds
-            const long long bi = rr / H, h = rr - bi * H;
-            const long long b = bi / Sq, i = bi - b * Sq;
-            lrow[u] = (b * H + h) * Sq + i;
+            if constexpr (I32) {
+                const unsigned r32 = static_cast<unsigned>(rr), hu = static_cast<unsigned>(H);
+                const unsigned bi = r32 / hu, h = r32 - bi * hu;
+                const unsigned b = bi / static_cast<unsigned>(Sq), i = bi - b * static_cast<unsigned>(Sq);
+                lrow[u] = static_cast<long long>((b * hu + h) * static_cast<unsigned>(Sq) + i);
+            } else {
+                const long long bi = rr / H, h = rr - bi * H;
+                const long long b = bi / Sq, i = bi - b * Sq;
+                lrow[u] = (b * H + h) * Sq + i;
+            }
             r[u] = l0 < rows ? rr : rows;
 #pragma unroll
             for (int p = 0; p < PT; ++p) {
@@ -188,19 +200,22 @@ cudaError_t launch_typed_merge(const LseMergeArgs &a, int sms, cudaStream_t stre
         return static_cast<unsigned>(std::max(1LL, std::min(cap, (rows + rows_per_block - 1) / rows_per_block)));
     };
     bool done = false;
-#define CTX_MERGE_CASE(DVV, PP)                                                                              \
-    if (!done && dv == DVV && a.P == PP) {                                                                   \
-        lse_merge_kernel<BF16, DVV, PP><<<grid_for(8LL * (32 / DVV) * 4,                                     \
-                                                    resident_blocks(lse_merge_kernel<BF16, DVV, PP>, dev)),   \
-                                          256, 0, stream>>>(                                                  \
+    const bool i32 = rows <= 0x7fffffffLL;  // every row index, and (b*H + h)*Sq + i, fits in 32 bits
+#define CTX_MERGE_CASE_I(DVV, PP, I)                                                                         \
+    if (!done && dv == DVV && a.P == PP && i32 == I) {                                                      \
+        lse_merge_kernel<BF16, DVV, PP, I><<<grid_for(8LL * (32 / DVV) * merge_unroll(PP),                   \
+                                                       resident_blocks(lse_merge_kernel<BF16, DVV, PP, I>, dev)), \
+                                             256, 0, stream>>>(                                               \
             op, a.lse_parts, out, a.lse, rows, a.Sq, a.H);                                                   \
         done = true;                                                                                         \
     }
+#define CTX_MERGE_CASE(DVV, PP) CTX_MERGE_CASE_I(DVV, PP, true) CTX_MERGE_CASE_I(DVV, PP, false)
 #define CTX_MERGE_DV(DVV) CTX_MERGE_CASE(DVV, 1) CTX_MERGE_CASE(DVV, 2) CTX_MERGE_CASE(DVV, 3) CTX_MERGE_CASE(DVV, 4)
     CTX_MERGE_DV(8)
     CTX_MERGE_DV(16)
 #undef CTX_MERGE_DV
 #undef CTX_MERGE_CASE
+#undef CTX_MERGE_CASE_I
     if (!done)
         lse_merge_generic<BF16><<<grid_for(256 / std::max(1, dv), resident_blocks(lse_merge_generic<BF16>, dev)),
                                   256, 0, stream>>>(op, a.lse_parts, a.P, out,
