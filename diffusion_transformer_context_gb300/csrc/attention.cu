@@ -94,8 +94,13 @@ struct Layout {
     // s_full[T], p_full[T], o_full[T], o_empty[T], seg_done[T], merge_go[T], mma_done
     static constexpr int kNumBars = 2 + 4 * kStages + 6 * kTiles + 1;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-    static constexpr int kBytes = kMiscOff + 32;
+    // per softmax warp: its 32 rows x 64 output columns, staged so that the
+    // output rows leave as whole 128-byte lines
+    static constexpr int kEpiWarpBytes = 32 * 128;
+    static constexpr int kEpiOff = (kMiscOff + 32 + 127) / 128 * 128;
+    static constexpr int kBytes = kEpiOff + 2 * 4 * kEpiWarpBytes;
     static constexpr int kAlloc = kBytes + 1024;    // room to align the base to 1024 B
+    static_assert(kAlloc <= 227 * 1024, "shared memory per CTA");
 };
 
 // One contiguous run of key blocks [jb, je) of one work unit. first: the
@@ -160,6 +165,40 @@ __device__ __forceinline__ uint4 *out_row(const Params &p, int b, int h, int qro
         row = static_cast<size_t>(b) * p.Sq + qrow;
     }
     return reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) + (row * p.H + h) * D);
+}
+
+// Output staging of one softmax warp (32 rows x 64 columns, 4 KB): row =
+// lane, 16-byte chunk j of the row at j ^ (row & 7), so that both the row-wise
+// writes and the line-wise reads hit 8 distinct bank groups per quarter warp.
+// stage32: this thread's columns [32*qq, 32*qq + 32) of the half, times
+// `scale`, rounded to the output type.
+template <bool BF16>
+__device__ __forceinline__ void stage32(uint4 *stg, int lane, int qq, const float *v, float scale)
+{
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int j = 4 * qq + k;
+        stg[lane * 8 + (j ^ (lane & 7))] = make_uint4(ptx::pack2<BF16>(v[8 * k + 0] * scale, v[8 * k + 1] * scale),
+                                                      ptx::pack2<BF16>(v[8 * k + 2] * scale, v[8 * k + 3] * scale),
+                                                      ptx::pack2<BF16>(v[8 * k + 4] * scale, v[8 * k + 5] * scale),
+                                                      ptx::pack2<BF16>(v[8 * k + 6] * scale, v[8 * k + 7] * scale));
+    }
+}
+
+// The warp's staged half rows to global memory, four whole 128-byte row
+// pieces per store instruction. orow: this lane's output row (0: the row does
+// not exist); col16: the half's first 16-byte column. Warp-wide.
+__device__ __forceinline__ void store_staged(const uint4 *stg, int lane, unsigned long long orow, int col16)
+{
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = 4 * i + (lane >> 3), cc = lane & 7;
+        uint4 *const dst = reinterpret_cast<uint4 *>(__shfl_sync(0xffffffffu, orow, r));
+        if (dst)
+            dst[col16 + cc] = stg[r * 8 + (cc ^ (r & 7))];
+    }
+    __syncwarp();
 }
 
 // Segment `si` of CTA c, computed from its index alone (identical in every
@@ -717,30 +756,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (sg.full) {
                 const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
                 const float lse_val = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+                // Each thread converts its own row into the warp's staging
+                // area; the warp then stores 4 rows x 128 bytes per
+                // instruction instead of 32 scattered 16-byte pieces.
+                const unsigned long long orow =
+                    qrow < q_end ? reinterpret_cast<unsigned long long>(out_row<D>(p, b, h, qrow)) : 0ull;
+                uint4 *const stg = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(bars) +
+                                                             (L::kEpiOff - L::kBarOff) + (warp - 2) * L::kEpiWarpBytes);
 #pragma unroll
-                for (int c0 = 0; c0 < D / 32; ++c0) {
-                    uint32_t o[32];
-                    ptx::tmem_ld32(tO + c0 * 32, o);
-                    ptx::tmem_ld_wait();
-                    ptx::reg_fence32(o);
-                    float of[32];
+                for (int hf = 0; hf < D / 64; ++hf) {
 #pragma unroll
-                    for (int k = 0; k < 32; ++k)
-                        of[k] = __uint_as_float(o[k]);
-                    if (qrow < q_end) {
-                        uint4 *orow = out_row<D>(p, b, h, qrow);
+                    for (int qq = 0; qq < 2; ++qq) {
+                        uint32_t o[32];
+                        ptx::tmem_ld32(tO + hf * 64 + qq * 32, o);
+                        ptx::tmem_ld_wait();
+                        ptx::reg_fence32(o);
+                        if (hf == D / 64 - 1 && qq == 1) {
+                            ptx::tc_fence_before();
+                            ptx::mbar_arrive(o_empty + t);  // O is in registers: the next PV may start
+                        }
+                        float of[32];
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            orow[c0 * 4 + k] = make_uint4(ptx::pack2<BF16>(of[8 * k + 0] * inv, of[8 * k + 1] * inv),
-                                                          ptx::pack2<BF16>(of[8 * k + 2] * inv, of[8 * k + 3] * inv),
-                                                          ptx::pack2<BF16>(of[8 * k + 4] * inv, of[8 * k + 5] * inv),
-                                                          ptx::pack2<BF16>(of[8 * k + 6] * inv, of[8 * k + 7] * inv));
+                        for (int k = 0; k < 32; ++k)
+                            of[k] = __uint_as_float(o[k]);
+                        stage32<BF16>(stg, lane, qq, of, inv);
                     }
+                    store_staged(stg, lane, orow, hf * 8);
                 }
                 if (p.lse && qrow < q_end)
                     p.lse[(static_cast<size_t>(b) * p.H + h) * p.Sq + qrow] = lse_val;
-                ptx::tc_fence_before();
-                ptx::mbar_arrive(o_empty + t);
             } else {
                 // Partial segment: unnormalised O and (m, l) go to this CTA's slot.
                 float4 *po = p.part_o + static_cast<size_t>(sg.slot) * (D / 4) * (kTiles * kBM) + prow;
