@@ -45,13 +45,14 @@ namespace ctx {
 namespace {
 
 constexpr int kBM = 128;      // query rows per tile (= TMEM lanes)
-constexpr int kBN = 128;      // keys per block
+constexpr int kBN = kAttnKeyBlock;  // keys per block (128)
 constexpr int kTiles = 2;     // query tiles per CTA
 constexpr int kStages = 2;    // depth of the K ring and of the V ring
 constexpr int kThreads = 320; // 10 warps
 constexpr int kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLn2 = 0.693147180559945309f;
+static_assert(kTiles * kBM == kAttnUnitRows, "work unit rows");
 
 struct Params {
     const unsigned char *mask;

@@ -14,6 +14,12 @@ constexpr int kStatusTimeout = 6;
 // Bound for every device-side wait (nanoseconds of %globaltimer).
 constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;
 
+// Attention work geometry shared by the kernel and the packed-varlen planner:
+// a work unit is kAttnUnitRows query rows (two 128-row tiles) of one head,
+// walked over its keys in blocks of kAttnKeyBlock.
+constexpr int kAttnUnitRows = 256;
+constexpr int kAttnKeyBlock = 128;
+
 // Address of the current device's status word (set up once per device).
 int *device_status_word(cudaError_t *err);
 

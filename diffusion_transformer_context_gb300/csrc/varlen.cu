@@ -99,8 +99,8 @@ __global__ void __launch_bounds__(kRemapThreads) varlen_plan_kernel(const int *c
             const int q_len = min(max(cu_q[d + 1], qs), Sq) - qs;
             const int k0 = min(max(cu_k[d], 0), Sk);
             const int k_len = min(max(cu_k[d + 1], k0), Sk) - k0;
-            const long long nqp = min((q_len + 255) / 256, n_qpairs);
-            v = static_cast<long long>(H) * nqp * ((k_len + 127) / 128);
+            const long long nqp = min((q_len + kAttnUnitRows - 1) / kAttnUnitRows, n_qpairs);
+            v = static_cast<long long>(H) * nqp * ((k_len + kAttnKeyBlock - 1) / kAttnKeyBlock);
         }
         for (int o = 1; o < 32; o <<= 1) {
             const long long x = __shfl_up_sync(0xffffffffu, v, o);
@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(kRemapThreads) varlen_plan_kernel(const int *c
     // first n_qpairs tile pairs) get out = 0, lse = -inf
     for (int d = 0; d < n_docs; ++d) {
         const int qs = min(max(cu_q[d], 0), Sq);
-        const int qe = min(min(max(cu_q[d + 1], qs), Sq), qs + n_qpairs * 256);
+        const int qe = min(min(max(cu_q[d + 1], qs), Sq), qs + n_qpairs * kAttnUnitRows);
         const int k0 = min(max(cu_k[d], 0), Sk);
         const int k_len = min(max(cu_k[d + 1], k0), Sk) - k0;
         if (k_len > 0 || qe <= qs)
