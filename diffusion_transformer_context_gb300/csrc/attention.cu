@@ -16,7 +16,9 @@
 //     TMEM columns [128t, 128t+128), and O_t += P_t V with P_t read from TMEM
 //     (it overwrites S_t as 16-bit pairs) and V from shared memory (MN-major)
 //     into columns [256 + Dt, 256 + D(t+1));
-//   * warps 2-5 and 6-9 are the softmax of tile 0 and tile 1: each thread
+//   * warps 4-7 and 8-11 are the softmax of tile 0 and tile 1 (warps 2-3
+//     only hand their registers over: the first warpgroup runs with 104
+//     registers per thread, the softmax warpgroups with 200): each thread
 //     owns one query row (its TMEM lane), reads its 128 scores with
 //     tcgen05.ld, does the online softmax in the log2 domain with exp2, writes
 //     P back with tcgen05.st and signals the MMA warp. The MMA warp issues
@@ -48,9 +50,17 @@ constexpr int kBM = 128;      // query rows per tile (= TMEM lanes)
 constexpr int kBN = kAttnKeyBlock;  // keys per block (128)
 constexpr int kTiles = 2;     // query tiles per CTA
 constexpr int kStages = 2;    // depth of the K ring and of the V ring
-constexpr int kThreads = 320; // 10 warps
+constexpr int kThreads = 384; // 12 warps: TMA, MMA, two idle, 4 + 4 softmax
+// Registers: the kernel is launched with kRegsLaunch per thread (the compiler's
+// figure for 384 threads, checked on the host before the first launch); the
+// first warpgroup (TMA, MMA) gives registers up to the two softmax warpgroups.
+constexpr int kRegsLaunch = 168;
+constexpr int kRegsControl = 104;
+constexpr int kRegsSoftmax = 200;
+static_assert(kRegsControl * 128 + kRegsSoftmax * 256 == kRegsLaunch * kThreads, "register split");
 constexpr int kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;
+constexpr float kFastSumLimit = 32768.0f;  // 2^15: largest block sum accepted against a stale maximum
 constexpr float kLn2 = 0.693147180559945309f;
 static_assert(kTiles * kBM == kAttnUnitRows, "work unit rows");
 
@@ -447,6 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
+        ptx::setmaxnreg_dec<kRegsControl>();
         if (lane == 0) {
             ptx::tma_prefetch_desc(&tmQ);
             ptx::tma_prefetch_desc(&tmK);
@@ -501,6 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issue
+        ptx::setmaxnreg_dec<kRegsControl>();
         // The whole warp runs this loop (warp-uniform values, warp-wide waits);
         // one elected lane issues each MMA and commit.
         {
@@ -580,13 +592,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             wait_bar(mma_done, 0, abort_flag, p, false);
             __syncwarp();
         }
+    } else if (warp < 4) {
+        ptx::setmaxnreg_dec<kRegsControl>();  // warps 2-3: registers only
     } else {
         // ------------------------------------------------------------ softmax
-        const int t = (warp - 2) >> 2;  // query tile
+        ptx::setmaxnreg_inc<kRegsSoftmax>();
+        const int t = (warp - 4) >> 2;  // query tile
         const int quad = warp & 3;      // TMEM lane quadrant this warp may access
         const int row = quad * 32 + lane;
         const int prow = t * kBM + row;  // row inside the unit's 256 query rows
-        const bool tile_leader = ((warp - 2) & 3) == 0 && lane == 0;
+        const bool tile_leader = ((warp - 4) & 3) == 0 && lane == 0;
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t tS = tmem + lane_off + t * kBN;
         const uint32_t tO = tmem + lane_off + 2 * kBN + t * D;
@@ -646,98 +661,153 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!(ok = wait_bar_warp(s_full + t, (g + i) & 1, abort_flag, p)))
                     break;
                 ptx::tc_fence_after();
-                float mx;
-                {
-                    uint32_t sr[kBN];
-                    ptx::tmem_ld32(tS + 0, sr + 0);
-                    ptx::tmem_ld32(tS + 32, sr + 32);
-                    ptx::tmem_ld32(tS + 64, sr + 64);
-                    ptx::tmem_ld32(tS + 96, sr + 96);
-                    ptx::tmem_ld_wait();
-                    ptx::reg_fence32(sr + 0);
-                    ptx::reg_fence32(sr + 32);
-                    ptx::reg_fence32(sr + 64);
-                    ptx::reg_fence32(sr + 96);
-                    float s[kBN];
+                // After a segment's first block the exps are taken against the
+                // running maximum without computing the block maximum first;
+                // the block's probability sum shows whether that was safe.
+                // Every p is at most the sum, so a sum <= 2^15 keeps every p
+                // (and the 16-bit P) in range; a larger sum (a maximum that
+                // grew by about 2^8 or more) sends the block through the exact
+                // path below: block maximum, conditional rescale of O, exps.
+                // S is still intact then: the fast path stores P only after
+                // the check.
+                bool fast = i > 0 && __all_sync(0xffffffffu, m_run != -INFINITY);
+                float l_blk = 0.f;
+                if (fast) {
+                    const uint64_t c2 = ptx::f2_pack(c, c), nm2 = ptx::f2_pack(-m_run, -m_run);
+                    uint64_t sum2[4] = {0, 0, 0, 0};
+                    uint32_t pk[kBN / 2];
+                    {
+                        uint32_t sh[kBN];
+                        ptx::tmem_ld32(tS + 0, sh + 0);
+                        ptx::tmem_ld32(tS + 32, sh + 32);
+                        ptx::tmem_ld32(tS + 64, sh + 64);
+                        ptx::tmem_ld32(tS + 96, sh + 96);
+                        ptx::tmem_ld_wait();
+                        ptx::reg_fence32(sh + 0);
+                        ptx::reg_fence32(sh + 32);
+                        ptx::reg_fence32(sh + 64);
+                        ptx::reg_fence32(sh + 96);
+                        if (!all_valid) {
 #pragma unroll
-                    for (int k = 0; k < kBN; ++k)
-                        s[k] = __uint_as_float(sr[k]);
-                    if (!all_valid) {
+                            for (int k = 0; k < kBN; ++k)
+                                if (!((vb[k >> 5] >> (k & 31)) & 1u))
+                                    sh[k] = __float_as_uint(-INFINITY);
+                        }
+#pragma unroll
+                        for (int k = 0; k < kBN / 2; ++k) {
+                            const uint64_t arg = ptx::f2_fma(
+                                ptx::f2_pack(__uint_as_float(sh[2 * k]), __uint_as_float(sh[2 * k + 1])), c2, nm2);
+                            const float p0 = ptx::ex2_approx(ptx::f2_lo(arg));
+                            const float p1 = ptx::ex2_approx(ptx::f2_hi(arg));
+                            sum2[k & 3] = ptx::f2_add(sum2[k & 3], ptx::f2_pack(p0, p1));
+                            pk[k] = ptx::pack2<BF16>(p0, p1);
+                        }
+                    }
+                    const uint64_t sum01 = ptx::f2_add(sum2[0], sum2[1]), sum23 = ptx::f2_add(sum2[2], sum2[3]);
+                    const uint64_t tot = ptx::f2_add(sum01, sum23);
+                    l_blk = ptx::f2_lo(tot) + ptx::f2_hi(tot);
+                    if (__any_sync(0xffffffffu, !(l_blk <= kFastSumLimit))) {
+                        fast = false;
+                    } else {
+                        ptx::tmem_st32(tS, pk);
+                        ptx::tmem_st32(tS + 32, pk + 32);
+                    }
+                }
+                if (!fast) {
+                    float mx;
+                    {
+                        uint32_t sr[kBN];
+                        ptx::tmem_ld32(tS + 0, sr + 0);
+                        ptx::tmem_ld32(tS + 32, sr + 32);
+                        ptx::tmem_ld32(tS + 64, sr + 64);
+                        ptx::tmem_ld32(tS + 96, sr + 96);
+                        ptx::tmem_ld_wait();
+                        ptx::reg_fence32(sr + 0);
+                        ptx::reg_fence32(sr + 32);
+                        ptx::reg_fence32(sr + 64);
+                        ptx::reg_fence32(sr + 96);
+                        float s[kBN];
 #pragma unroll
                         for (int k = 0; k < kBN; ++k)
-                            if (!((vb[k >> 5] >> (k & 31)) & 1u))
-                                s[k] = -INFINITY;
-                    }
-                    float acc[8];
+                            s[k] = __uint_as_float(sr[k]);
+                        if (!all_valid) {
 #pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        acc[k] = s[k];
-#pragma unroll
-                    for (int k = 8; k < kBN; k += 16) {
-#pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            acc[q] = ptx::max3(acc[q], s[k + q], s[k + 8 + q]);
-                    }
-                    mx = ptx::max3(ptx::max3(acc[0], acc[1], acc[2]), ptx::max3(acc[3], acc[4], acc[5]),
-                                   fmaxf(acc[6], acc[7]));
-                }
-                const float m_new = fmaxf(m_run, mx * c);
-                if (i == 0) {
-                    m_run = m_new;
-                } else {
-                    const bool need = m_new > m_run + kRescaleLog2;
-                    if (__any_sync(0xffffffffu, need)) {
-                        const float alpha = need ? ptx::ex2_approx(m_run - m_new) : 1.0f;
-                        if (need) {
-                            l_run *= alpha;
-                            m_run = m_new;
+                            for (int k = 0; k < kBN; ++k)
+                                if (!((vb[k >> 5] >> (k & 31)) & 1u))
+                                    s[k] = -INFINITY;
                         }
+                        float acc[8];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            acc[k] = s[k];
+#pragma unroll
+                        for (int k = 8; k < kBN; k += 16) {
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                acc[q] = ptx::max3(acc[q], s[k + q], s[k + 8 + q]);
+                        }
+                        mx = ptx::max3(ptx::max3(acc[0], acc[1], acc[2]), ptx::max3(acc[3], acc[4], acc[5]),
+                                       fmaxf(acc[6], acc[7]));
+                    }
+                    const float m_new = fmaxf(m_run, mx * c);
+                    if (i == 0) {
+                        m_run = m_new;
+                    } else {
+                        const bool need = m_new > m_run + kRescaleLog2;
+                        if (__any_sync(0xffffffffu, need)) {
+                            const float alpha = need ? ptx::ex2_approx(m_run - m_new) : 1.0f;
+                            if (need) {
+                                l_run *= alpha;
+                                m_run = m_new;
+                            }
 #pragma unroll 1
-                        for (int c0 = 0; c0 < D / 16; ++c0) {
-                            uint32_t o[16];
-                            ptx::tmem_ld16(tO + c0 * 16, o);
-                            ptx::tmem_ld_wait();
-                            ptx::reg_fence16(o);
+                            for (int c0 = 0; c0 < D / 16; ++c0) {
+                                uint32_t o[16];
+                                ptx::tmem_ld16(tO + c0 * 16, o);
+                                ptx::tmem_ld_wait();
+                                ptx::reg_fence16(o);
 #pragma unroll
-                            for (int k = 0; k < 16; ++k)
-                                o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-                            ptx::tmem_st16(tO + c0 * 16, o);
+                                for (int k = 0; k < 16; ++k)
+                                    o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                                ptx::tmem_st16(tO + c0 * 16, o);
+                            }
+                            ptx::tmem_st_wait();
                         }
-                        ptx::tmem_st_wait();
                     }
+                    const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
+                    const uint64_t c2 = ptx::f2_pack(c, c), nm2 = ptx::f2_pack(neg_m, neg_m);
+                    uint64_t sum2[4] = {0, 0, 0, 0};
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t sh[64];
+                        ptx::tmem_ld32(tS + 64 * half, sh);
+                        ptx::tmem_ld32(tS + 64 * half + 32, sh + 32);
+                        ptx::tmem_ld_wait();
+                        ptx::reg_fence32(sh);
+                        ptx::reg_fence32(sh + 32);
+                        if (!all_valid) {
+#pragma unroll
+                            for (int k = 0; k < 64; ++k)
+                                if (!((vb[2 * half + (k >> 5)] >> (k & 31)) & 1u))
+                                    sh[k] = __float_as_uint(-INFINITY);
+                        }
+                        uint32_t pk[32];
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) {
+                            const uint64_t arg = ptx::f2_fma(
+                                ptx::f2_pack(__uint_as_float(sh[2 * k]), __uint_as_float(sh[2 * k + 1])), c2, nm2);
+                            const float p0 = ptx::ex2_approx(ptx::f2_lo(arg));
+                            const float p1 = ptx::ex2_approx(ptx::f2_hi(arg));
+                            sum2[k & 3] = ptx::f2_add(sum2[k & 3], ptx::f2_pack(p0, p1));
+                            pk[k] = ptx::pack2<BF16>(p0, p1);
+                        }
+                        ptx::tmem_st32(tS + 32 * half, pk);
+                    }
+                    const uint64_t t01 = ptx::f2_add(sum2[0], sum2[1]), t23 = ptx::f2_add(sum2[2], sum2[3]);
+                    const uint64_t tot = ptx::f2_add(t01, t23);
+                    l_blk = ptx::f2_lo(tot) + ptx::f2_hi(tot);
                 }
-                const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
-                const uint64_t c2 = ptx::f2_pack(c, c), nm2 = ptx::f2_pack(neg_m, neg_m);
-                uint64_t sum2[4] = {0, 0, 0, 0};
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t sh[64];
-                    ptx::tmem_ld32(tS + 64 * half, sh);
-                    ptx::tmem_ld32(tS + 64 * half + 32, sh + 32);
-                    ptx::tmem_ld_wait();
-                    ptx::reg_fence32(sh);
-                    ptx::reg_fence32(sh + 32);
-                    if (!all_valid) {
-#pragma unroll
-                        for (int k = 0; k < 64; ++k)
-                            if (!((vb[2 * half + (k >> 5)] >> (k & 31)) & 1u))
-                                sh[k] = __float_as_uint(-INFINITY);
-                    }
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        const uint64_t arg = ptx::f2_fma(
-                            ptx::f2_pack(__uint_as_float(sh[2 * k]), __uint_as_float(sh[2 * k + 1])), c2, nm2);
-                        const float p0 = ptx::ex2_approx(ptx::f2_lo(arg));
-                        const float p1 = ptx::ex2_approx(ptx::f2_hi(arg));
-                        sum2[k & 3] = ptx::f2_add(sum2[k & 3], ptx::f2_pack(p0, p1));
-                        pk[k] = ptx::pack2<BF16>(p0, p1);
-                    }
-                    ptx::tmem_st32(tS + 32 * half, pk);
-                }
-                const uint64_t t01 = ptx::f2_add(sum2[0], sum2[1]), t23 = ptx::f2_add(sum2[2], sum2[3]);
-                const uint64_t tot = ptx::f2_add(t01, t23);
-                l_run += ptx::f2_lo(tot) + ptx::f2_hi(tot);
+                l_run += l_blk;
                 ptx::tmem_st_wait();
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(p_full + t);
@@ -763,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const unsigned long long orow =
                     qrow < q_end ? reinterpret_cast<unsigned long long>(out_row<D>(p, b, h, qrow)) : 0ull;
                 uint4 *const stg = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(bars) +
-                                                             (L::kEpiOff - L::kBarOff) + (warp - 2) * L::kEpiWarpBytes);
+                                                             (L::kEpiOff - L::kBarOff) + (warp - 4) * L::kEpiWarpBytes);
 #pragma unroll
                 for (int hf = 0; hf < D / 64; ++hf) {
 #pragma unroll
@@ -1029,6 +1099,16 @@ cudaError_t launch_typed(const AttnArgs &a, cudaStream_t stream)
     {
         std::lock_guard<std::mutex> g(mu);
         if (dev >= 64 || !attr_set[dev]) {
+            // The warpgroups' register budgets add up to the launch's total only
+            // if the compiled kernel uses exactly kRegsLaunch registers per
+            // thread; a larger split would never be granted, so refuse to launch
+            // any other build.
+            cudaFuncAttributes fa{};
+            err = cudaFuncGetAttributes(&fa, attn_fwd_kernel<D, BF16>);
+            if (err != cudaSuccess)
+                return err;
+            if (fa.numRegs != kRegsLaunch || fa.maxThreadsPerBlock < kThreads)
+                return cudaErrorInvalidDeviceFunction;
             err = cudaFuncSetAttribute(attn_fwd_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        L::kAlloc);
             if (err != cudaSuccess)
