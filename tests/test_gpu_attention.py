@@ -142,6 +142,31 @@ def test_growing_maximum_sorted_keys(ctx, orc):
     _check_full(orc, q, k, v, O, L, scale=0.5)
 
 
+@pytest.mark.parametrize("split", [False, True], ids=["per_unit", "balanced"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_running_maximum_jumps(ctx, orc, dtype, split):
+    """After a segment's first key block the kernel takes the exps against
+    the running maximum and checks the block's probability sum (at most 2^15)
+    instead of computing the block maximum. Query rows close to one direction
+    u and small random keys keep the early maxima near 0; in key block 5 one
+    key is a multiple of u whose score jumps by about 11.4 log2 units on head
+    0 (p ~ 2^11: accepted, no rescale) and by about 17.3 on head 1 (p ~ 2^17:
+    the block is redone with its exact maximum and O rescaled)."""
+    gen = torch.Generator().manual_seed(21)
+    B, Sq, Sk, H, D = 1, 256, 1024, 2, 128
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
+    u = torch.where(torch.rand(D, generator=gen) < 0.5, -1.0, 1.0)
+    q = (u.view(1, 1, 1, D) + 0.05 * torch.randn((B, Sq, H, D), generator=gen)).to(tdt)
+    k = (0.1 * torch.randn((B, Sk, H, D), generator=gen))
+    v = torch.randn((B, Sk, H, D), generator=gen).to(tdt)
+    j = 5 * 128 + 37
+    for h, s_nat in ((0, 8.0), (1, 12.0)):  # natural-log score of the special key
+        k[0, j, h] = u * (s_nat / math.sqrt(D))
+    k = k.to(tdt)
+    O, L = _run(ctx, q, k, v, split=split)
+    _check_full(orc, q, k, v, O, L, dtype=dtype)
+
+
 def test_deterministic(ctx):
     gen = torch.Generator().manual_seed(14)
     B, Sq, Sk, H, D = 1, 512, 2048, 4, 128
