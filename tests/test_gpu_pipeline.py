@@ -110,6 +110,8 @@ def test_pack_workload(ctx, orc):
     workloads.custom("u4a2_d64", B=1, S=1024, H=8, D=64, U=4, A=2),
     workloads.custom("u1a4_ragged", B=1, S=1000, H=3, D=128, U=1, A=4),
     workloads.custom("u3a1", B=2, S=378, H=6, D=128, U=3, A=1),
+    workloads.custom("u8a1_h16", B=1, S=1024, H=16, D=128, U=8, A=1),
+    workloads.custom("u2a4_h12_joint", B=1, S=768, H=12, D=128, U=2, A=4, joint=48, text_len_range=(8, 48)),
 ], ids=lambda w: w.name)
 def test_composed_small(ctx, orc, wl):
     _check_layer(ctx, orc, wl)

@@ -31,6 +31,8 @@ CASES = [  # (B, S_l, H, D, U)
     (2, 5, 40, 128, 4),     # long runs (10 heads x 128 -> several segments)
     (1, 13, 80, 128, 2),    # run of 40 heads: multi-segment
     (3, 3, 4, 16, 1),       # U = 1 identity
+    (1, 20, 96, 128, 8),    # U = 8, 12 heads per destination
+    (2, 9, 8, 64, 8),       # U = 8, one head per destination, ragged rows
 ]
 
 
