@@ -193,10 +193,14 @@ ctx_status ctx_unpack_out_ex(const void *recv, void *y, int B, int S_l,
  *            zeroed again; after CTX_ERR_TIMEOUT it must be re-zeroed. Calls
  *            that may run concurrently must not share a workspace.
  * D        : 64 or 128 (CTX_ERR_UNSUPPORTED otherwise).
- * Numerics : fp32 accumulation for QK^T, softmax and PV; the probabilities
- *            are rounded to the input dtype before the PV product; out is
- *            rounded to nearest even. Results do not depend on the workspace
- *            beyond fp32 rounding of the merge.
+ * Numerics : fp32 accumulation for QK^T, softmax and PV; the unnormalised
+ *            probabilities exp(s_j - m') are taken against a running maximum
+ *            m' (never more than 2^15, so they fit fp16) and rounded to the
+ *            input dtype before the PV product; the final division by the
+ *            row sum is exact up to fp32 rounding; out is rounded to nearest
+ *            even. The two schedules agree up to that rounding of the
+ *            probabilities (their running maxima differ where a key range
+ *            is cut) and fp32 rounding of the merge.
  */
 ctx_status ctx_attn_lq_gkv(const void *q, const void *k, const void *v,
                            const unsigned char *key_mask, float scale,
