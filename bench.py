@@ -537,6 +537,101 @@ def run_merge_bench(args):
     print(json.dumps(line), flush=True)
 
 
+def run_attn_bench(args):
+    """--kernel attn: one ctx_attn_lq_gkv call of --attn-shape B,Sq,Sk,H,D
+    (seeded N(0,1) inputs in --dtype, no mask, scale 1/sqrt(D)), balanced
+    schedule unless --unbalanced. L2 is flushed (a 256 MB write) before every
+    timed launch and each launch is timed alone with CUDA events on the
+    launching stream. Work: 4 * B * H * Sq * Sk * D FLOP per call."""
+    import numpy as np
+    import torch
+
+    import workloads
+    import diffusion_transformer_context_gb300 as ctx
+
+    B, Sq, Sk, H, D = (int(x) for x in args.attn_shape.split(","))
+    gen = torch.Generator().manual_seed(workloads.SEED)
+    q_h = workloads.randn((B, Sq, H, D), gen, args.dtype)
+    k_h = workloads.randn((B, Sk, H, D), gen, args.dtype)
+    v_h = workloads.randn((B, Sk, H, D), gen, args.dtype)
+    q, k, v = q_h.cuda(), k_h.cuda(), v_h.cuda()
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, Sq), dtype=torch.float32, device="cuda")
+    ws = None if args.unbalanced else ctx.attn_workspace(B, Sq, Sk, H, D)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    flops = 4.0 * B * H * Sq * Sk * D
+
+    def call():
+        ctx.ctx_attn_lq_gkv(q, k, v, out, lse, workspace=ws)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    st = ctx.ctx_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status: {ctx.ctx_status_string(st)}")
+    sampler = None if args.no_clocks else ClockSampler(0)
+    if sampler:
+        sampler.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for e0, e1 in ev:
+        flush.fill_(1)
+        e0.record()
+        call()
+        e1.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    ms = sum(e0.elapsed_time(e1) for e0, e1 in ev) / args.steps
+    tflops = flops / (ms * 1e-3) / 1e12
+    # e2e: Q/K/V in from pinned host memory, O and LSE back, one step after another
+    qp, kp, vp = (t.pin_memory() for t in (q_h, k_h, v_h))
+    oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    e0, e1 = ev[0]
+    e0.record()
+    for _ in range(args.steps):
+        q.copy_(qp, non_blocking=True)
+        k.copy_(kp, non_blocking=True)
+        v.copy_(vp, non_blocking=True)
+        call()
+        oh.copy_(out, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    peaks, kind = load_peaks()
+    line = {"metric": METRIC, "value": round(tflops, 3), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": args.dtype, "data": "synthetic",
+            "config": {"workload": "attn", "B": B, "Sq": Sq, "Sk": Sk, "H": H, "D": D,
+                       "l2": "flushed_between_steps",
+                       "attn_schedule": "one CTA per unit" if ws is None else "persistent, key-split tail"},
+            "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel", "achieved": round(tflops, 2),
+                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": round(tflops / peaks["bf16_tflops"], 4),
+                         "peak_source": f"{kind} bf16_tflops (burst)", "algorithmic_flops_per_launch": flops,
+                         "launch_ms": round(ms, 4), "traffic": None},
+            "gpu_launches": args.steps, "clocks": clocks,
+            "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": 2 * (qp.numel() + kp.numel() + vp.numel()),
+                    "d2h_bytes_per_step": 2 * oh.numel() + 4 * lh.numel(), "ms_per_step": round(e2e_ms, 4),
+                    "pipeline": "copies and compute one after another"}}
+    if not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        u16 = workloads.as_u16
+        rng = np.random.default_rng(workloads.SEED)
+        n = 256
+        bhi = np.stack([rng.integers(0, B, n), rng.integers(0, H, n), rng.integers(0, Sq, n)], axis=1)
+        t = time.perf_counter()
+        oracle.attention_rows(u16(q_h), u16(k_h), u16(v_h), bhi, dtype=args.dtype)
+        dt = time.perf_counter() - t
+        line["cpu_baseline"] = {"value": round(4.0 * Sk * D * n / dt / 1e12, 6), "unit": "TFLOP/s",
+                                "cores": oracle.num_threads(), "kind": "oracle",
+                                "sample": f"{n} random query rows, all {Sk} keys each"}
+    print(json.dumps(line), flush=True)
+
+
 VARLEN_DOCS = (12288, 8192, 6144, 4096, 2048)  # tokens per packed document (sum 32768)
 
 
@@ -680,7 +775,10 @@ def main():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--unbalanced", action="store_true", help="attention without workspace: one CTA per unit")
     ap.add_argument("--eager", action="store_true", help="launch every kernel from Python instead of CUDA graphs")
-    ap.add_argument("--kernel", default=None, choices=["lse_merge", "varlen"], help="time one kernel alone")
+    ap.add_argument("--kernel", default=None, choices=["lse_merge", "varlen", "attn"], help="time one kernel alone")
+    ap.add_argument("--attn-shape", default="1,4095,32760,12,128",
+                    help="--kernel attn: B,Sq,Sk,H,D of the attention call")
+    ap.add_argument("--dtype", default="bf16", choices=["bf16", "fp16"], help="--kernel attn: input dtype")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=64)
     args = ap.parse_args()
@@ -701,6 +799,10 @@ def main():
     if args.kernel == "varlen":
         if rank == 0:
             run_varlen_bench(args)
+        return
+    if args.kernel == "attn":
+        if rank == 0:
+            run_attn_bench(args)
         return
 
     import torch

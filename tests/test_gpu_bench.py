@@ -54,3 +54,14 @@ def test_attention_output_snapshot_path():
     assert "snapshot" in d["e2e"]["pipeline"]
     assert d["e2e"]["readback_verified"] is True
     assert d["roofline"]["algorithmic_flops_per_launch"] == pytest.approx(4.0 * 12 * 32760 * 32760 * 128)
+
+
+@pytest.mark.gpu
+def test_single_attention_call_line():
+    # --kernel attn: one call of a given shape, L2 flushed before every timed launch
+    d = run_bench("--kernel", "attn", "--attn-shape", "1,300,700,3,128", "--dtype", "fp16", "--steps", "3",
+                  "--warmup", "3", "--no-cpu-baseline", "--no-clocks")
+    assert d["unit"] == "TFLOP/s" and d["value"] > 0 and d["dtype"] == "fp16"
+    assert d["config"]["l2"] == "flushed_between_steps"
+    assert d["roofline"]["algorithmic_flops_per_launch"] == pytest.approx(4.0 * 3 * 300 * 700 * 128)
+    assert d["e2e"]["h2d_bytes_per_step"] == 2 * 128 * 3 * (300 + 2 * 700)
