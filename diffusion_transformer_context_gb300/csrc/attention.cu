@@ -897,47 +897,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++pc;
                 if (merge_flag[t]) {
                     // Last segment of this unit to finish: combine every segment by log-sum-exp.
-                    float M = -INFINITY;
-                    for (int cc = c_lo; cc <= c_hi; ++cc) {
-                        const int sl = (tail_start(p, total, cc) >= first) ? 2 * cc : 2 * cc + 1;
-                        M = fmaxf(M, __ldcg(p.part_ml + static_cast<size_t>(sl) * (kTiles * kBM) + prow).x);
-                    }
-                    float lsum = 0.f;
+                    // running maximum and sum of the pieces' (m, l) in one pass
+                    float M = -INFINITY, lsum = 0.f;
+#pragma unroll 4
                     for (int cc = c_lo; cc <= c_hi; ++cc) {
                         const int sl = (tail_start(p, total, cc) >= first) ? 2 * cc : 2 * cc + 1;
                         const float2 ml = __ldcg(p.part_ml + static_cast<size_t>(sl) * (kTiles * kBM) + prow);
-                        lsum += (ml.x == -INFINITY) ? 0.f : ptx::ex2_approx(ml.x - M) * ml.y;
+                        if (ml.x == -INFINITY)
+                            continue;
+                        if (ml.x > M) {
+                            lsum = (M == -INFINITY ? 0.f : lsum * ptx::ex2_approx(M - ml.x)) + ml.y;
+                            M = ml.x;
+                        } else {
+                            lsum += ptx::ex2_approx(ml.x - M) * ml.y;
+                        }
                     }
                     const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
-                    uint4 *orow = out_row<D>(p, b, h, qrow);
+                    // rows leave through the warp's staging area as whole 128-byte lines
+                    const unsigned long long orow =
+                        qrow < q_end ? reinterpret_cast<unsigned long long>(out_row<D>(p, b, h, qrow)) : 0ull;
+                    uint4 *const stg = reinterpret_cast<uint4 *>(
+                        reinterpret_cast<uint8_t *>(bars) + (L::kEpiOff - L::kBarOff) + (warp - 4) * L::kEpiWarpBytes);
 #pragma unroll 1
-                    for (int c0 = 0; c0 < D / 32; ++c0) {
-                        float o[32];
+                    for (int hf = 0; hf < D / 64; ++hf) {
+                        // 64 columns at a time: all 16 float4 of a piece are in flight
+                        // together, one L2 round trip per piece
+                        float o[64];
 #pragma unroll
-                        for (int k = 0; k < 32; ++k)
+                        for (int k = 0; k < 64; ++k)
                             o[k] = 0.f;
                         for (int cc = c_lo; cc <= c_hi; ++cc) {
                             const int sl = (tail_start(p, total, cc) >= first) ? 2 * cc : 2 * cc + 1;
                             const float2 ml = __ldcg(p.part_ml + static_cast<size_t>(sl) * (kTiles * kBM) + prow);
-                            const float w = (ml.x == -INFINITY) ? 0.f : ptx::ex2_approx(ml.x - M);
-                            const float4 *src = p.part_o + (static_cast<size_t>(sl) * (D / 4) + c0 * 8) * (kTiles * kBM) + prow;
+                            const float4 *src =
+                                p.part_o + (static_cast<size_t>(sl) * (D / 4) + hf * 16) * (kTiles * kBM) + prow;
+                            float4 v[16];
 #pragma unroll
-                            for (int k = 0; k < 8; ++k) {
-                                const float4 v = __ldcg(src + static_cast<size_t>(k) * (kTiles * kBM));
-                                o[4 * k] += w * v.x;
-                                o[4 * k + 1] += w * v.y;
-                                o[4 * k + 2] += w * v.z;
-                                o[4 * k + 3] += w * v.w;
+                            for (int k = 0; k < 16; ++k)
+                                v[k] = __ldcg(src + static_cast<size_t>(k) * (kTiles * kBM));
+                            const float w = (ml.x == -INFINITY) ? 0.f : ptx::ex2_approx(ml.x - M);
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) {
+                                o[4 * k] += w * v[k].x;
+                                o[4 * k + 1] += w * v[k].y;
+                                o[4 * k + 2] += w * v[k].z;
+                                o[4 * k + 3] += w * v[k].w;
                             }
                         }
-                        if (qrow < q_end) {
-#pragma unroll
-                            for (int k = 0; k < 4; ++k)
-                                orow[c0 * 4 + k] = make_uint4(ptx::pack2<BF16>(o[8 * k + 0] * inv, o[8 * k + 1] * inv),
-                                                              ptx::pack2<BF16>(o[8 * k + 2] * inv, o[8 * k + 3] * inv),
-                                                              ptx::pack2<BF16>(o[8 * k + 4] * inv, o[8 * k + 5] * inv),
-                                                              ptx::pack2<BF16>(o[8 * k + 6] * inv, o[8 * k + 7] * inv));
-                        }
+                        stage32<BF16>(stg, lane, 0, o, inv);
+                        stage32<BF16>(stg, lane, 1, o + 32, inv);
+                        store_staged(stg, lane, orow, hf * 8);
                     }
                     if (p.lse && qrow < q_end)
                         p.lse[(static_cast<size_t>(b) * p.H + h) * p.Sq + qrow] =
