@@ -24,9 +24,13 @@
 //     P back with tcgen05.st and signals the MMA warp. The MMA warp issues
 //     PV_0(j-1), S_0(j), PV_1(j-1), S_1(j), so the tensor core works on one
 //     tile while the other tile's softmax runs;
-//   * O is rescaled only when a row maximum grows by more than 2^8 (a stale
-//     maximum keeps every probability <= 2^8, exact after the final division),
-//     which the public FlashAttention-4 write-up calls conditional rescaling;
+//   * the first key block of a segment takes the block maximum and rescales
+//     O only when a row maximum grows by more than 2^8 (a stale maximum keeps
+//     every probability <= 2^8, exact after the final division), which the
+//     public FlashAttention-4 write-up calls conditional rescaling; every
+//     later block takes the exps against the running maximum directly and
+//     keeps them when the block's probability sum is at most 2^15 (else the
+//     block goes through the exact path, its scores still in TMEM);
 //   * epilogue: O / l rounded to the input type, LSE = ln2 * (m + log2 l);
 //   * schedules: one CTA per work unit, or (given a workspace) a persistent
 //     grid of one CTA per SM that cuts units' key ranges between SMs and
