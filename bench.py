@@ -823,7 +823,9 @@ def main():
     relayout_ms = avg(parts["exchange_in"])
     relayout_gbs = relayout_bytes / (relayout_ms * 1e-3) / 1e9
     reverse_ms = avg(parts["exchange_out"])
-    relayout = {"bound": "hbm", "kernel": "relayout_kernel (pack + all-to-all + unpack of all ranks)",
+    relayout_kernel = ("relayout_kernel (unpack of all ranks; at U = 1 a rank's staging buffer is its input)"
+                       if sim.pack_view else "relayout_kernel (pack + all-to-all + unpack of all ranks)")
+    relayout = {"bound": "hbm", "kernel": relayout_kernel,
                 "achieved": round(relayout_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(relayout_gbs / peaks["hbm_gbs"], 4), "peak_source": f"{peak_kind} hbm_gbs",
                 "ms": round(relayout_ms, 4), "algorithmic_bytes": relayout_bytes,

@@ -44,13 +44,18 @@ from . import (CTX_LAYOUT_TQKV, attn_workspace, ctx_attn_lq_gkv, ctx_attn_lq_gkv
 
 class SimLayer:
     def __init__(self, wl, device="cuda", dtype=torch.bfloat16, attention: bool | None = None,
-                 balanced: bool = True, layout: int = CTX_LAYOUT_TQKV, fuse_reverse: bool = True):
+                 balanced: bool = True, layout: int = CTX_LAYOUT_TQKV, fuse_reverse: bool = True,
+                 pack_view: bool = True):
         self.wl = wl
         self.dev = torch.device(device)
         self.dtype = dtype
         self.layout = layout
         # U > 1: the attention epilogue writes the reverse exchange's send buffers directly
         self.fuse_reverse = fuse_reverse and wl.U > 1
+        # U = 1 (AllGather-KV alone): a rank's [1, 3, B, S_l, H, D] staging buffer is
+        # its [3, B, S_l, H, D] input bit for bit, so the unpack (the AllGather
+        # placement) reads the input and no pack or all-to-all runs
+        self.pack_view = pack_view and wl.U == 1 and layout == CTX_LAYOUT_TQKV
         U, A, B, S, H, D, J = wl.U, wl.A, wl.B, wl.S, wl.H, wl.D, wl.joint
         if S % (U * A):
             raise ValueError("S must divide by U*A")
@@ -62,8 +67,9 @@ class SimLayer:
         kw = dict(dtype=dtype, device=self.dev)
         self.x = torch.empty((R, 3, B, S_l, H, D), **kw)           # per-rank inputs
         chunk = 3 * B * S_l * h_l * D
-        self.send = torch.empty((A, U, U, chunk), **kw)             # [group a, src u, dst chunk]
-        self.recv = torch.empty_like(self.send) if U > 1 else self.send
+        if not self.pack_view:
+            self.send = torch.empty((A, U, U, chunk), **kw)         # [group a, src u, dst chunk]
+            self.recv = torch.empty_like(self.send) if U > 1 else self.send
         self.qg = torch.empty((U, B, S, h_l, D), **kw)              # local-Q of all ranks
         self.kg = torch.empty((U, B, Sk, h_l, D), **kw)             # gathered K (+ joint)
         self.vg = torch.empty((U, B, Sk, h_l, D), **kw)
@@ -131,10 +137,12 @@ class SimLayer:
         def unpack(g, s):
             a, u = divmod(g, U)
             r0 = a * U * S_l
-            ctx_unpack_qkv_ex(self.recv[a, u], self.qg[u, :, r0:], self.kg[u, :, r0:], self.vg[u, :, r0:], U, B,
+            src = self.x[g] if self.pack_view else self.recv[a, u]
+            ctx_unpack_qkv_ex(src, self.qg[u, :, r0:], self.kg[u, :, r0:], self.vg[u, :, r0:], U, B,
                               S_l, h_l, D, self.layout, q_batch_stride_rows=S, kv_batch_stride_rows=Sk, stream=s)
 
-        self._per_rank(stream, pack)
+        if not self.pack_view:
+            self._per_rank(stream, pack)
         if U > 1:
             ctx_sim_all_to_all(self.send, self.recv, A, U, stream=stream)
         self._per_rank(stream, unpack)
@@ -209,7 +217,7 @@ class SimLayer:
 
     def launches_per_step(self) -> int:
         U, R = self.wl.U, self.R
-        n = 2 * R + (1 if U > 1 else 0)
+        n = (R if self.pack_view else 2 * R) + (1 if U > 1 else 0)
         if self.attention:
             n += 1
             if U > 1:
@@ -233,6 +241,8 @@ class SimLayer:
         """Algorithmic HBM bytes of all packs of one step: the real heads read,
         the padded heads written."""
         wl = self.wl
+        if self.pack_view:
+            return 0
         return 3 * self.R * wl.B * self.S_l * (wl.H + self.H_pad) * wl.D * 2
 
     def unpack_bytes(self) -> int:

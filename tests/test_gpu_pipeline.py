@@ -35,10 +35,10 @@ def _oracle_side(orc, inp, layout=0):
                                     wl.U, wl.A, jk, jv, layout)
 
 
-def _check_layer(ctx, orc, wl, n_rows=None, layout=0):
+def _check_layer(ctx, orc, wl, n_rows=None, layout=0, pack_view=True):
     from diffusion_transformer_context_gb300.simulate import SimLayer
     inp = workloads.make_inputs(wl)
-    sim = SimLayer(wl, layout=layout, fuse_reverse=False)
+    sim = SimLayer(wl, layout=layout, fuse_reverse=False, pack_view=pack_view)
     sim.load(inp)
     sim.step()
     st = ctx.ctx_device_status()
@@ -115,6 +115,15 @@ def test_pack_workload(ctx, orc):
 ], ids=lambda w: w.name)
 def test_composed_small(ctx, orc, wl):
     _check_layer(ctx, orc, wl)
+
+
+@pytest.mark.parametrize("wl", [
+    workloads.custom("u1a4_ragged_packed", B=1, S=1000, H=3, D=128, U=1, A=4),
+    workloads.custom("u1a8_b2_packed", B=2, S=1024, H=4, D=64, U=1, A=8),
+], ids=lambda w: w.name)
+def test_u1_pack_run(ctx, orc, wl):
+    """U = 1 with the identity pack launched (the default views the input instead)."""
+    _check_layer(ctx, orc, wl, pack_view=False)
 
 
 @pytest.mark.parametrize("wl", [
