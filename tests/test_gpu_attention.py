@@ -167,6 +167,22 @@ def test_running_maximum_jumps(ctx, orc, dtype, split):
     _check_full(orc, q, k, v, O, L, dtype=dtype)
 
 
+@pytest.mark.parametrize("masked", [False, True])
+def test_one_unit_cut_over_every_sm(ctx, orc, masked):
+    """One work unit (256 query rows of one head) against 304 key blocks: the
+    balanced schedule gives every SM two of its key blocks, so the unit's
+    last piece merges one partial result per SM by log-sum-exp."""
+    gen = torch.Generator().manual_seed(22)
+    B, Sq, Sk, H, D = 1, 256, 304 * 128, 1, 128
+    q, k, v = (workloads.randn(s, gen) for s in ((B, Sq, H, D), (B, Sk, H, D), (B, Sk, H, D)))
+    mask = None
+    if masked:  # whole pieces and single keys masked out
+        mask = (np.random.default_rng(22).random((B, Sk)) > 0.3).astype(np.uint8)
+        mask[:, 5000:9000] = 0
+    O, L = _run(ctx, q, k, v, mask=mask, split=True)
+    _check_full(orc, q, k, v, O, L, mask=mask)
+
+
 def test_deterministic(ctx):
     gen = torch.Generator().manual_seed(14)
     B, Sq, Sk, H, D = 1, 512, 2048, 4, 128
