@@ -682,15 +682,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t pk[kBN / 2];
                     {
                         uint32_t sh[kBN];
-                        ptx::tmem_ld32(tS + 0, sh + 0);
-                        ptx::tmem_ld32(tS + 32, sh + 32);
-                        ptx::tmem_ld32(tS + 64, sh + 64);
-                        ptx::tmem_ld32(tS + 96, sh + 96);
+                        static_assert(kBN == 128, "one 128-column TMEM load per block");
+                        ptx::tmem_ld128(tS, sh);
                         ptx::tmem_ld_wait();
-                        ptx::reg_fence32(sh + 0);
-                        ptx::reg_fence32(sh + 32);
-                        ptx::reg_fence32(sh + 64);
-                        ptx::reg_fence32(sh + 96);
+                        ptx::reg_fence128(sh);
                         if (!all_valid) {
 #pragma unroll
                             for (int k = 0; k < kBN; ++k)
@@ -713,8 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (__any_sync(0xffffffffu, !(l_blk <= kFastSumLimit))) {
                         fast = false;
                     } else {
-                        ptx::tmem_st32(tS, pk);
-                        ptx::tmem_st32(tS + 32, pk + 32);
+                        ptx::tmem_st64(tS, pk);
                     }
                 }
                 if (!fast) {

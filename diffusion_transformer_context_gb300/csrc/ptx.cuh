@@ -240,6 +240,28 @@ __device__ __forceinline__ void reg_fence32(uint32_t *r)
     asm volatile("" : CTX_P8(0), CTX_P8(8), CTX_P8(16), CTX_P8(24));
 }
 
+// 128 consecutive 32-bit columns of this thread's lane in one load.
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t *r)
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%128];"
+                 : CTX_R8(0), CTX_R8(8), CTX_R8(16), CTX_R8(24), CTX_R8(32), CTX_R8(40), CTX_R8(48), CTX_R8(56), CTX_R8(64), CTX_R8(72), CTX_R8(80), CTX_R8(88), CTX_R8(96), CTX_R8(104), CTX_R8(112), CTX_R8(120)
+                 : "r"(taddr));
+}
+
+// 64 consecutive 32-bit columns of this thread's lane in one store.
+__device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t *r)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64};"
+                 ::"r"(taddr), CTX_W8(0), CTX_W8(8), CTX_W8(16), CTX_W8(24), CTX_W8(32), CTX_W8(40), CTX_W8(48), CTX_W8(56)
+                 : "memory");
+}
+
+// As reg_fence32, for 128 registers.
+__device__ __forceinline__ void reg_fence128(uint32_t *r)
+{
+    asm volatile("" : CTX_P8(0), CTX_P8(8), CTX_P8(16), CTX_P8(24), CTX_P8(32), CTX_P8(40), CTX_P8(48), CTX_P8(56), CTX_P8(64), CTX_P8(72), CTX_P8(80), CTX_P8(88), CTX_P8(96), CTX_P8(104), CTX_P8(112), CTX_P8(120));
+}
+
 #undef CTX_R8
 #undef CTX_W8
 #undef CTX_P8
