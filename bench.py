@@ -374,6 +374,12 @@ def cpu_baseline_sample(wl_name: str, seconds: float, seed: int = 1234):
             "relayout_gbs": round(relayout_bytes / relayout_s / 1e9, 3)}
 
 
+def shape_config(wl) -> dict:
+    """The workload keys both arms report in `config`."""
+    return {"workload": wl.name, "B": wl.B, "S": wl.S, "H": wl.H, "D": wl.D, "U": wl.U, "A": wl.A,
+            "joint": wl.joint, "virtual_ranks": wl.U * wl.A}
+
+
 def run_reference(args, rank):
     """--impl reference: the oracle, on the host cores, a bounded sample per step."""
     if rank != 0:
@@ -421,7 +427,7 @@ def run_reference(args, rank):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 * dt_tot / args.steps, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "sample_rows_per_step": n_rows},
+            "config": {**shape_config(wl), "sample_rows_per_step": n_rows},
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
                              "kind": "oracle",
                              "sample": f"{n_rows} random query rows of {args.workload} per step, all keys"},
@@ -457,7 +463,7 @@ def run_reference_layout(args, wl, inp):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 * dt / args.steps, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "u16 (bit copy)", "data": "synthetic",
-            "config": {"workload": args.workload, "sample": "pack + unpack of one rank per step"},
+            "config": {**shape_config(wl), "sample": "pack + unpack of one rank per step"},
             "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": oracle.num_threads(),
                              "kind": "oracle", "sample": "pack + unpack of one rank per step"},
             "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -831,8 +837,7 @@ def main():
                 "ms": round(relayout_ms, 4), "algorithmic_bytes": relayout_bytes,
                 "reverse_ms": round(reverse_ms, 4), "reverse_bytes": sim.reverse_bytes(),
                 "traffic": recorded_traffic(args.workload, "relayout")}
-    config = {"workload": args.workload, "B": sim.wl.B, "S": sim.wl.S, "H": sim.wl.H, "D": sim.wl.D,
-              "U": sim.wl.U, "A": sim.wl.A, "joint": sim.wl.joint, "virtual_ranks": sim.R,
+    config = {**shape_config(sim.wl),
               "l2": "flushed_between_steps" if sim.l2_flushed else "inputs_larger_than_l2",
               "parallelism": f"replicas{world}",
               "launch": "eager" if args.eager else "cuda graphs (one per phase)"}
