@@ -198,6 +198,65 @@ def all_gather(shards, axis: int = 1):
     return np.concatenate([np.ascontiguousarray(s) for s in shards], axis=axis)
 
 
+# ------------------------------------------------- joint-text key mask
+
+class MaskMergeUnsupported(NotImplementedError):
+    """A mask combination the merge refuses (fail closed): a 4-D image mask,
+    alone (it belongs to a query-range slicing path outside this method's
+    key-mask merge) or next to a 2-D joint mask."""
+
+
+def merge_joint_attn_mask(image_mask, joint_mask, B: int, S_img: int, joint_len: int,
+                          joint_front: bool = False):
+    """The [B, K_final] key-validity mask of the gathered key layout
+    (vllm-omni PR #7641, follow-up review commit that makes the joint-mask
+    merge the single owner of 2-D key-mask handling after the K/V gather).
+
+    image_mask : None or array; as a 2-D mask it must be [B, S_img] over the
+                 gathered (global) image keys.
+    joint_mask : None or array; must be 2-D [B, joint_len].
+    joint_len  : joint keys re-attached after the gather, taken from the
+                 joint KEY tensor (the joint query may be empty when cached
+                 K/V is reused), 0 when there are none.
+    joint_front: joint segment before the image keys (else after them).
+
+    The steps, in the order the page gives them: ranks are checked joint
+    side first (a joint mask that is not 2-D is invalid; a 4-D image mask is
+    refused, with or without a joint mask); a joint mask needs joint K/V; each
+    side's shape must equal (B, its segment length); a missing side is filled
+    with True; the two segments are concatenated in placement order and
+    normalised to 0/1. Returns None when neither side has a mask (every key
+    valid), else uint8 [B, S_img + joint_len].
+    Raises ValueError for invalid inputs, MaskMergeUnsupported for refused
+    ones.
+    """
+    if image_mask is None and joint_mask is None:
+        return None
+    im = None if image_mask is None else np.asarray(image_mask)
+    jm = None if joint_mask is None else np.asarray(joint_mask)
+    if jm is not None and jm.ndim != 2:
+        raise ValueError("joint mask must be 2-D [B, joint_len]")
+    if im is not None and im.ndim == 4:
+        raise MaskMergeUnsupported("4-D image mask: no key-mask merge (refused next to a joint mask)")
+    if im is not None and im.ndim != 2:
+        raise ValueError("image mask must be 2-D [B, S_img]")
+    if jm is not None and joint_len == 0:
+        raise ValueError("joint mask given without joint keys/values")
+    if im is not None and tuple(im.shape) != (B, S_img):
+        raise ValueError(f"image mask shape {im.shape} != {(B, S_img)}")
+    if jm is not None and tuple(jm.shape) != (B, joint_len):
+        raise ValueError(f"joint mask shape {jm.shape} != {(B, joint_len)}")
+    K = S_img + joint_len
+    out = np.zeros((B, K), dtype=np.uint8)
+    for b in range(B):
+        img_seg = [1 if im is None or im[b, i] else 0 for i in range(S_img)]
+        jnt_seg = [1 if jm is None or jm[b, j] else 0 for j in range(joint_len)]
+        row = jnt_seg + img_seg if joint_front else img_seg + jnt_seg
+        for pos in range(K):
+            out[b, pos] = row[pos]
+    return out
+
+
 # ---------------------------------------------------------------- attention
 
 def default_scale(D: int) -> float:
@@ -273,12 +332,12 @@ def _pad_heads(x, H_pad):
 
 
 def ulysses_agkv_forward(q_shards, k_shards, v_shards, U: int, A: int,
-                         jk=None, jv=None, layout: int = LAYOUT_TQKV):
+                         jk=None, jv=None, layout: int = LAYOUT_TQKV, joint_front: bool = False):
     """The composed U x A input side, all ranks (vllm-omni PR #7641 order):
     Ulysses all-to-all inside each U group (ranks a*U .. a*U+U-1), then the
     K/V AllGather inside each A group (ranks u, U+u, ...), then the joint
-    (text) K/V appended after the gathered image keys. Heads that do not
-    divide by U are zero-padded to U*ceil(H/U).
+    (text) K/V re-attached after (or, joint_front, before) the gathered image
+    keys. Heads that do not divide by U are zero-padded to U*ceil(H/U).
 
     Inputs are per-rank [B,S_l,H,D] uint16 shards indexed by g = a*U + u.
     Returns dict with, per rank g: 'q' [B,S/A,h_l,D] local-Q, and per head
@@ -302,8 +361,10 @@ def ulysses_agkv_forward(q_shards, k_shards, v_shards, U: int, A: int,
         if jk is not None:
             h_l = kg.shape[2]
             jkp, jvp = _pad_heads(jk, U * h_l), _pad_heads(jv, U * h_l)
-            kg = np.concatenate([kg, np.ascontiguousarray(jkp[:, :, u * h_l:(u + 1) * h_l])], axis=1)
-            vg = np.concatenate([vg, np.ascontiguousarray(jvp[:, :, u * h_l:(u + 1) * h_l])], axis=1)
+            jks = np.ascontiguousarray(jkp[:, :, u * h_l:(u + 1) * h_l])
+            jvs = np.ascontiguousarray(jvp[:, :, u * h_l:(u + 1) * h_l])
+            kg = np.concatenate([jks, kg] if joint_front else [kg, jks], axis=1)
+            vg = np.concatenate([jvs, vg] if joint_front else [vg, jvs], axis=1)
         res["k"].append(kg)
         res["v"].append(vg)
     return res
