@@ -141,6 +141,31 @@ def max_over_ranks(x: float, world: int, device="cpu") -> float:
     return float(t.item())
 
 
+def valid_keys(inp):
+    """Per batch row, the gathered keys the masks leave valid: the image keys
+    outside the image padding plus the text keys inside the text length."""
+    wl = inp.wl
+    img = [wl.S if inp.image_mask is None else int(inp.image_mask[b].sum()) for b in range(wl.B)]
+    jnt = [wl.joint if inp.joint_mask is None else int(inp.joint_mask[b].sum()) for b in range(wl.B)]
+    return [i + j for i, j in zip(img, jnt)]
+
+
+def oracle_keys(inp, h_l):
+    """The oracle's gathered K/V of head group 0 and its merged key mask."""
+    import numpy as np
+    import oracle
+    import workloads
+
+    wl, u16 = inp.wl, workloads.as_u16
+    k, v = u16(inp.k[:, :, :h_l]), u16(inp.v[:, :, :h_l])
+    if wl.joint:
+        jk, jv = u16(inp.jk[:, :, :h_l]), u16(inp.jv[:, :, :h_l])
+        k = np.concatenate([jk, k] if wl.joint_front else [k, jk], axis=1)
+        v = np.concatenate([jv, v] if wl.joint_front else [v, jv], axis=1)
+    mask = oracle.merge_joint_attn_mask(inp.image_mask, inp.joint_mask, wl.B, wl.S, wl.joint, wl.joint_front)
+    return k, v, mask
+
+
 def whole_job_tflops(flops_per_rank: float, world: int, ms: float) -> float:
     """Weak scaling: every rank does the same work; the job's throughput is
     all ranks' FLOPs over the slowest rank's time."""
@@ -229,6 +254,86 @@ def run_gpu(args, rank, world, local_rank):
     return sim, inp, total_ms, parts, clocks, e2e
 
 
+def run_pack_line(args, dev, peaks, peak_kind):
+    """The layout-only workload timed beside the default line: U = 4 ranks,
+    each Q/K/V [1,1024,24,128], packed into [4,3,1,1024,6,128] staging
+    buffers and, after the exchange, unpacked to [1,4096,6,128] per rank.
+
+    `achieved` is the library's pack and unpack kernels in HBM terms: the
+    four ranks' packs (one CUDA graph, ranks' launches concurrent) and,
+    separately, the four unpacks, each replayed in rotation over buffer sets
+    whose total is several times L2, so every read comes from HBM and the
+    write-back of every written line falls inside the timed region (only the
+    last replay's dirty lines escape it, 1/K of the writes). `step_gbs` is
+    the whole simulated step (pack + all-to-all + unpack) back to back: there
+    the staging buffers written by one kernel are read by the next while they
+    are still in L2, so it is not an HBM figure."""
+    import torch
+
+    import workloads
+    from diffusion_transformer_context_gb300.simulate import SimLayer
+
+    wl = workloads.WORKLOADS["pack"]
+    inp = workloads.make_inputs(wl)
+    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
+    one = SimLayer(wl, device=dev)
+    set_bytes = (one.x.numel() + one.send.numel() + one.recv.numel() + 3 * one.qg.numel()) * 2
+    # a pack (or an unpack) touches half a set; between two uses of a buffer
+    # the other sets' kernels move at least 4x L2 through the cache
+    n_sets = 1 + -(-4 * l2_bytes // (set_bytes // 2))
+    sims = [one] + [SimLayer(wl, device=dev) for _ in range(n_sets - 1)]
+    for sim in sims:
+        sim.load(inp)
+        sim.step()  # library set-up outside any capture
+    torch.cuda.synchronize(dev)
+    graphs = {"pack": [], "unpack": [], "step": []}
+    for sim in sims:
+        for name, fn in (("pack", sim.pack_ranks), ("unpack", sim.unpack_ranks), ("step", sim.exchange_in)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn()
+            graphs[name].append(g)
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+    reps = max(args.steps, 20) * n_sets
+
+    def timed(name):
+        gs = graphs[name]
+        for i in range(2 * n_sets):
+            gs[i % n_sets].replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for i in range(reps):
+            gs[i % n_sets].replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / reps
+
+    ms_pack, ms_unpack, ms_step = timed("pack"), timed("unpack"), timed("step")
+    b_pack, b_unpack = one.pack_bytes(), one.unpack_bytes()
+    b_step = b_pack + one.a2a_bytes() + b_unpack
+    gbs = (b_pack + b_unpack) / ((ms_pack + ms_unpack) * 1e-3) / 1e9
+
+    def rate(b, ms):
+        return round(b / (ms * 1e-3) / 1e9, 1)
+
+    return {"workload": "pack", "U": wl.U, "per_rank": [wl.B, wl.S_l, wl.H, wl.D],
+            "staging": [wl.U, 3, wl.B, wl.S_l, wl.h_l, wl.D], "bound": "hbm",
+            "kernel": "relayout_kernel (4 packs; 4 unpacks)", "achieved": round(gbs, 1),
+            "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+            "peak_source": f"{peak_kind} hbm_gbs",
+            "pack_gbs": rate(b_pack, ms_pack), "unpack_gbs": rate(b_unpack, ms_unpack),
+            "pack_ms": round(ms_pack, 4), "unpack_ms": round(ms_unpack, 4),
+            "algorithmic_bytes": {"pack": b_pack, "unpack": b_unpack},
+            "timing": f"CUDA graphs replayed back to back over {n_sets} buffer sets of {set_bytes >> 20} MiB "
+                      f"(L2 {l2_bytes >> 20} MiB): reads from HBM, write-back inside the timed region",
+            "replays": reps, "gpu_launches_per_replay": {"pack": wl.ranks, "unpack": wl.ranks},
+            "step_gbs": rate(b_step, ms_step), "step_ms": round(ms_step, 4),
+            "step_note": "pack + simulated all-to-all + unpack back to back; staging buffers re-read from L2",
+            "traffic": recorded_traffic("pack", "relayout")}
+
+
 def run_e2e(sim, inp, args, world, dev, run_phase, barrier):
     """The same steps with every step's inputs copied in from pinned host
     memory and its result copied back, all inside the timed region.
@@ -305,7 +410,7 @@ def run_e2e(sim, inp, args, world, dev, run_phase, barrier):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     # after the timed region: the host copy of the last step's result equals the device result
     verified = all(torch.equal(h.to(dev), r) for h, r in zip(host_y, results))
-    flops = sim.attn_flops(inp.text_len)
+    flops = sim.attn_flops(valid_keys(inp))
     return {"value": round(whole_job_tflops(flops * args.steps, world, e2e_ms), 3), "unit": "TFLOP/s",
             "h2d_bytes_per_step": host_x.numel() * host_x.element_size(),
             "d2h_bytes_per_step": sum(h.numel() * h.element_size() for h in host_y),
@@ -340,13 +445,7 @@ def cpu_baseline_sample(wl_name: str, seconds: float, seed: int = 1234):
     # attention: head group 0, gathered K/V, query rows of every rank
     h_l = wl.h_l
     q = u16(inp.q[:, :, :h_l])
-    k = u16(inp.k[:, :, :h_l])
-    v = u16(inp.v[:, :, :h_l])
-    mask = None
-    if wl.joint:
-        k = np.concatenate([k, u16(inp.jk[:, :, :h_l])], axis=1)
-        v = np.concatenate([v, u16(inp.jv[:, :, :h_l])], axis=1)
-        mask = inp.key_mask()
+    k, v, mask = oracle_keys(inp, h_l)
     Sk = k.shape[1]
     rng = np.random.default_rng(seed)
 
@@ -396,12 +495,8 @@ def run_reference(args, rank):
         run_reference_layout(args, wl, inp)
         return
     h_l = wl.h_l
-    q, k, v = u16(inp.q[:, :, :h_l]), u16(inp.k[:, :, :h_l]), u16(inp.v[:, :, :h_l])
-    mask = None
-    if wl.joint:
-        k = np.concatenate([k, u16(inp.jk[:, :, :h_l])], axis=1)
-        v = np.concatenate([v, u16(inp.jv[:, :, :h_l])], axis=1)
-        mask = inp.key_mask()
+    q = u16(inp.q[:, :, :h_l])
+    k, v, mask = oracle_keys(inp, h_l)
     Sk = k.shape[1]
     rng = np.random.default_rng(1234)
     n_rows = args.ref_rows
@@ -779,6 +874,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-pack", action="store_true", help="skip the layout-only pack workload line")
     ap.add_argument("--unbalanced", action="store_true", help="attention without workspace: one CTA per unit")
     ap.add_argument("--eager", action="store_true", help="launch every kernel from Python instead of CUDA graphs")
     ap.add_argument("--kernel", default=None, choices=["lse_merge", "varlen", "attn"], help="time one kernel alone")
@@ -819,7 +915,7 @@ def main():
     sim, inp, total_ms, parts, clocks, e2e = run_gpu(args, rank, world, local_rank)
     peaks, peak_kind = load_peaks()
     K = args.steps
-    attn_flops = sim.attn_flops(inp.text_len)
+    attn_flops = sim.attn_flops(valid_keys(inp))
     ms_step = total_ms / K
 
     def avg(x):
@@ -865,6 +961,9 @@ def main():
             e2e["value"] = round(world * relayout_bytes / (e2e["ms_per_step"] * 1e-3) / 1e9, 1)
             e2e["unit"] = "GB/s"
     line.update({"gpu_launches": sim.launches_per_step() * K, "clocks": clocks, "e2e": e2e})
+    if sim.attention and not args.no_pack:
+        # the pack/unpack target's own workload, after the timed region of the headline step
+        line["pack"] = run_pack_line(args, torch.device("cuda", local_rank), peaks, peak_kind)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb = cpu_baseline_sample(args.workload, args.cpu_seconds)
         if not sim.attention:

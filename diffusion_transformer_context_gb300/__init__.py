@@ -40,6 +40,7 @@ SIGNATURES = {
     "ctx_pack_out": (_I, [_P, _P, _LL, _I, _I, _I, _I, _I, _I, _P]),
     "ctx_unpack_out": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "ctx_lse_merge": (_I, [_P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "ctx_merge_joint_attn_mask": (_I, [_P, _I, _P, _P, _I, _P, _I, _I, _I, _I, _P, _P]),
     "ctx_varlen_remap": (_I, [_P, _I, _LL, _LL, _P, _P, _P, _P]),
     "ctx_attn_varlen": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _F, _P, _P, _P, _LL, _I, _I, _I, _I, _I, _P]),
     "ctx_attn_varlen_workspace_size": (_LL, [_I, _I, _I, _I]),
@@ -104,6 +105,15 @@ def _ptr(t):
     return None if t is None else t.data_ptr()
 
 
+def _check_span(name: str, t, nbytes: int):
+    """A strided output addressed from t.data_ptr() must lie inside t's
+    storage: the C library sees only the pointer, so a view too short for
+    the rows it is asked to write is refused here, before the call."""
+    have = t.untyped_storage().nbytes() - t.storage_offset() * t.element_size()
+    if nbytes > have:
+        raise ValueError(f"{name}: {nbytes} bytes addressed from the tensor's first element, storage holds {have}")
+
+
 def ctx_pack_qkv(q, k, v, staging, U: int, stream=None):
     """q, k, v [B,S_l,H,D] -> staging [U,3,B,S_l,H/U,D] (all contiguous CUDA tensors)."""
     B, S_l, H, D = q.shape
@@ -125,6 +135,10 @@ def ctx_unpack_qkv_ex(recv, q, k, v, U: int, B: int, S_l: int, h_l: int, D: int,
     """recv in `layout` -> q, k, v bases of [B, stride_rows, h_l, D] buffers."""
     qs = U * S_l if q_batch_stride_rows is None else q_batch_stride_rows
     ks = U * S_l if kv_batch_stride_rows is None else kv_batch_stride_rows
+    row = h_l * D * recv.element_size()
+    _check_span("ctx_unpack_qkv_ex q", q, ((B - 1) * qs + U * S_l) * row)
+    for name, t in (("k", k), ("v", v)):
+        _check_span("ctx_unpack_qkv_ex " + name, t, ((B - 1) * ks + U * S_l) * row)
     _check("ctx_unpack_qkv_ex", lib().ctx_unpack_qkv_ex(_ptr(recv), _ptr(q), _ptr(k), _ptr(v), qs, ks, B, S_l, h_l,
                                                         D, U, layout, _dtype(recv), _stream(stream)))
 
@@ -154,6 +168,10 @@ def ctx_unpack_qkv(recv, q, k, v, U: int, q_batch_stride_rows: int | None = None
     assert U2 == U and three == 3
     qs = U * S_l if q_batch_stride_rows is None else q_batch_stride_rows
     ks = U * S_l if kv_batch_stride_rows is None else kv_batch_stride_rows
+    row = h_l * D * recv.element_size()
+    _check_span("ctx_unpack_qkv q", q, ((B - 1) * qs + U * S_l) * row)
+    for name, t in (("k", k), ("v", v)):
+        _check_span("ctx_unpack_qkv " + name, t, ((B - 1) * ks + U * S_l) * row)
     _check("ctx_unpack_qkv", lib().ctx_unpack_qkv(_ptr(recv), _ptr(q), _ptr(k), _ptr(v), qs, ks,
                                                   B, S_l, h_l, D, U, _dtype(recv), _stream(stream)))
 
@@ -219,6 +237,7 @@ def ctx_pack_out(o, send, U: int, o_batch_stride_rows: int | None = None, stream
     Us, B, S_l, h_l, D = send.shape
     assert Us == U
     st = U * S_l if o_batch_stride_rows is None else o_batch_stride_rows
+    _check_span("ctx_pack_out o", o, ((B - 1) * st + U * S_l) * h_l * D * send.element_size())
     _check("ctx_pack_out", lib().ctx_pack_out(_ptr(o), _ptr(send), st, B, S_l, h_l, D, U, _dtype(send),
                                               _stream(stream)))
     return send
@@ -238,6 +257,29 @@ def ctx_lse_merge(o_parts, lse_parts, out, lse=None, stream=None):
     _check("ctx_lse_merge", lib().ctx_lse_merge(_ptr(o_parts), _ptr(lse_parts), P, _ptr(out), _ptr(lse), B, Sq, H,
                                                 D, _dtype(o_parts), _stream(stream)))
     return out
+
+
+def _mask_arg(t):
+    """(pointer, rank, host array of sizes) of an optional mask tensor."""
+    if t is None:
+        return None, 0, None
+    dims = (ctypes.c_longlong * t.dim())(*t.shape)
+    return t.data_ptr(), t.dim(), dims
+
+
+def ctx_merge_joint_attn_mask(image_mask, joint_mask, B: int, S_img: int, J: int, key_mask,
+                              joint_front: bool = False, stream=None):
+    """Optional image mask [B, S_img] and joint mask [B, J] (uint8 or bool CUDA
+    tensors, nonzero = attend) -> key_mask [B, S_img + J] uint8 0/1, the joint
+    segment first when joint_front. The masks' ranks and sizes are passed as
+    they are; the library checks them."""
+    ip, ind, idims = _mask_arg(image_mask)
+    jp, jnd, jdims = _mask_arg(joint_mask)
+    _check("ctx_merge_joint_attn_mask", lib().ctx_merge_joint_attn_mask(
+        ip, ind, None if idims is None else ctypes.cast(idims, ctypes.c_void_p),
+        jp, jnd, None if jdims is None else ctypes.cast(jdims, ctypes.c_void_p),
+        B, S_img, J, 1 if joint_front else 0, _ptr(key_mask), _stream(stream)))
+    return key_mask
 
 
 def ctx_varlen_remap(cu_seqlens_q, span_begin: int, span_len: int, cu_seqlens_q_local, packed_padding=None,

@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG, "libctx.so")
-SOURCES = ["api.cu", "relayout.cu", "attention.cu", "noalloc.cu", "merge.cu", "varlen.cu"]
+SOURCES = ["api.cu", "relayout.cu", "attention.cu", "noalloc.cu", "merge.cu", "varlen.cu", "mask.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

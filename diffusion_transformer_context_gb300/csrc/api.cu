@@ -15,7 +15,6 @@ __device__ int g_status_word;
 namespace {
 struct DeviceCache {
     std::mutex mu;
-    int *status[64] = {nullptr};
     int sms[64] = {0};
 };
 DeviceCache &cache()
@@ -25,26 +24,39 @@ DeviceCache &cache()
 }
 }  // namespace
 
-int *device_status_word(cudaError_t *err)
+cudaError_t device_symbol_address(const void *symbol, void **slots, cudaStream_t stream, void **out)
 {
     int dev = 0;
-    *err = cudaGetDevice(&dev);
-    if (*err != cudaSuccess)
-        return nullptr;
-    if (dev < 0 || dev >= 64) {
-        *err = cudaErrorInvalidDevice;
-        return nullptr;
-    }
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= 64)
+        return cudaErrorInvalidDevice;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(stream, &cs);
+    if (e != cudaSuccess)
+        return e;
     DeviceCache &c = cache();
     std::lock_guard<std::mutex> g(c.mu);
-    if (!c.status[dev]) {
+    if (cs == cudaStreamCaptureStatusNone) {
         void *p = nullptr;
-        *err = cudaGetSymbolAddress(&p, g_status_word);
-        if (*err != cudaSuccess)
-            return nullptr;
-        c.status[dev] = static_cast<int *>(p);
+        e = cudaGetSymbolAddress(&p, symbol);
+        if (e != cudaSuccess)
+            return e;
+        slots[dev] = p;
+    } else if (!slots[dev]) {
+        return cudaErrorStreamCaptureUnsupported;
     }
-    return c.status[dev];
+    *out = slots[dev];
+    return cudaSuccess;
+}
+
+int *device_status_word(cudaStream_t stream, cudaError_t *err)
+{
+    static void *addr[64] = {nullptr};
+    void *p = nullptr;
+    *err = device_symbol_address(reinterpret_cast<const void *>(&g_status_word), addr, stream, &p);
+    return *err == cudaSuccess ? static_cast<int *>(p) : nullptr;
 }
 
 int sm_count(cudaError_t *err)
@@ -469,6 +481,8 @@ static ctx_status attn_common(const void *q, const void *k, const void *v, const
         return CTX_ERR_INVALID_ARG;
     if (!mul_ok(nk, B) || !mul_ok(nk, Sk) || !mul_ok(nk, H) || !mul_ok(nk, D))
         return CTX_ERR_INVALID_ARG;
+    if (ctx::attention_units(B, Sq, H) > 0x7fffffffLL)
+        return CTX_ERR_INVALID_ARG;
     if (std::isnan(scale))
         scale = 1.0f / std::sqrt(static_cast<float>(D));
     if (!std::isfinite(scale) || !(scale > 0.f))
@@ -550,7 +564,8 @@ ctx_status ctx_attn_lq_gkv_pack_out(const void *q, const void *k, const void *v,
 long long ctx_attn_lq_gkv_workspace_size(int B, int Sq, int Sk, int H, int D)
 {
     long long n = 1;
-    if (!mul_ok(n, B) || !mul_ok(n, Sq) || !mul_ok(n, Sk) || !mul_ok(n, H) || (D != 64 && D != 128))
+    if (!mul_ok(n, B) || !mul_ok(n, Sq) || !mul_ok(n, Sk) || !mul_ok(n, H) || (D != 64 && D != 128) ||
+        ctx::attention_units(B, Sq, H) > 0x7fffffffLL)
         return -1;
     cudaError_t e = cudaSuccess;
     const long long bytes = ctx::attention_workspace_size(B, Sq, Sk, H, D, &e);
@@ -673,6 +688,43 @@ long long ctx_attn_varlen_workspace_size(int n_docs, int max_seqlen_q, int H, in
     return bytes;
 }
 
+ctx_status ctx_merge_joint_attn_mask(const unsigned char *image_mask, int image_ndim, const long long *image_dims,
+                                     const unsigned char *joint_mask, int joint_ndim, const long long *joint_dims,
+                                     int B, int S_img, int J, int joint_front, unsigned char *key_mask, void *stream)
+{
+    if (!key_mask || B <= 0 || S_img < 0 || J < 0 || static_cast<long long>(S_img) + J <= 0 ||
+        static_cast<long long>(S_img) + J > 0x7fffffffLL)
+        return CTX_ERR_INVALID_ARG;
+    // ranks, joint side first: a joint mask is only ever 2-D; a 4-D image
+    // mask has no key-mask form (refused with or without a joint mask)
+    if (joint_mask && (joint_ndim != 2 || !joint_dims))
+        return CTX_ERR_INVALID_ARG;
+    if (image_mask && !image_dims)
+        return CTX_ERR_INVALID_ARG;
+    if (image_mask && image_ndim == 4)
+        return CTX_ERR_UNSUPPORTED;
+    if (image_mask && image_ndim != 2)
+        return CTX_ERR_INVALID_ARG;
+    // a joint mask needs joint keys; each side must cover (B, its segment)
+    if (joint_mask && J == 0)
+        return CTX_ERR_INVALID_ARG;
+    if (image_mask && (image_dims[0] != B || image_dims[1] != S_img))
+        return CTX_ERR_INVALID_ARG;
+    if (joint_mask && (joint_dims[0] != B || joint_dims[1] != J))
+        return CTX_ERR_INVALID_ARG;
+    const long long out_bytes = static_cast<long long>(B) * (static_cast<long long>(S_img) + J);
+    const Extent eo = extent(key_mask, out_bytes);
+    if ((image_mask && overlap(eo, extent(image_mask, static_cast<long long>(B) * S_img))) ||
+        (joint_mask && overlap(eo, extent(joint_mask, static_cast<long long>(B) * J))))
+        return CTX_ERR_ALIASING;
+    ctx_status s = check_device_ptrs({image_mask, joint_mask, key_mask});
+    if (s != CTX_OK)
+        return s;
+    cudaError_t e = ctx::launch_merge_mask(image_mask, joint_mask, B, S_img, J, joint_front ? 1 : 0, key_mask,
+                                           static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CTX_OK : cuda_fail(e);
+}
+
 ctx_status ctx_lse_merge(const void *o_parts, const float *lse_parts, int P, void *out, float *lse, int B, int Sq,
                          int H, int D, ctx_dtype dtype, void *stream)
 {
@@ -715,7 +767,7 @@ ctx_status ctx_device_status(void *stream)
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e);
-    int *word = ctx::device_status_word(&e);
+    int *word = ctx::device_status_word(static_cast<cudaStream_t>(stream), &e);
     if (e != cudaSuccess)
         return cuda_fail(e);
     int value = 0;

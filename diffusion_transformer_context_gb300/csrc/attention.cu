@@ -1036,9 +1036,9 @@ constexpr long long kMinTailBlocks = 32;
 Schedule plan(int B, int Sq, int Sk, int H, int sms, bool split)
 {
     Schedule s{};
-    // packed varlen: B counts documents and Sq is the longest document
-    const int n_qpairs = (Sq + kTiles * kBM - 1) / (kTiles * kBM);
-    s.n_units = n_qpairs * H * B;
+    // packed varlen: B counts documents and Sq is the longest document;
+    // callers have checked that the unit count fits in an int
+    s.n_units = static_cast<int>(attention_units(B, Sq, H));
     s.n_kblocks = (Sk + kBN - 1) / kBN;
     if (!split) {
         s.grid = s.n_units;
@@ -1163,7 +1163,7 @@ cudaError_t launch_typed(const AttnArgs &a, cudaStream_t stream)
     p.dp_waves = sc.dp_waves;
     p.tail_iters = sc.tail_iters;
     p.scale_log2 = a.scale * 1.4426950408889634f;
-    p.status = device_status_word(&err);
+    p.status = device_status_word(stream, &err);
     if (err != cudaSuccess)
         return err;
     p.wait_limit_ns = kDefaultWaitLimitNs;
@@ -1196,6 +1196,16 @@ long long varlen_workspace_size(int n_docs, int max_seqlen_q, int H, int D, cuda
     return ws_bytes(sc, D) + ws_prefix_bytes(n_docs);
 }
 
+long long attention_units(int B, int Sq, int H)
+{
+    return (static_cast<long long>(Sq) + kTiles * kBM - 1) / (kTiles * kBM) * H * B;
+}
+
+long long attention_counter_bytes(int B, int Sq, int H)
+{
+    return (attention_units(B, Sq, H) * kTiles * 4 + 255) / 256 * 256;
+}
+
 long long attention_workspace_size(int B, int Sq, int Sk, int H, int D, cudaError_t *err)
 {
     const int sms = sm_count(err);
@@ -1216,7 +1226,7 @@ cudaError_t launch_attention(const AttnArgs &a, cudaStream_t stream)
 cudaError_t launch_selftest_wait(unsigned long long limit_ns, cudaStream_t stream)
 {
     cudaError_t err = cudaSuccess;
-    int *status = device_status_word(&err);
+    int *status = device_status_word(stream, &err);
     if (err != cudaSuccess)
         return err;
     selftest_wait_kernel<<<1, 32, 0, stream>>>(status, limit_ns);

@@ -20,8 +20,15 @@ constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;
 constexpr int kAttnUnitRows = 256;
 constexpr int kAttnKeyBlock = 128;
 
-// Address of the current device's status word (set up once per device).
-int *device_status_word(cudaError_t *err);
+// Device address of a __device__ symbol on the current device. Outside a
+// stream capture it is looked up on every call (a device reset reloads the
+// module, possibly elsewhere) and remembered in slots[device]; while `stream`
+// is capturing, the address of the last lookup on this device is used (none
+// yet: cudaErrorStreamCaptureUnsupported), since a lookup may load the module.
+cudaError_t device_symbol_address(const void *symbol, void **slots, cudaStream_t stream, void **out);
+
+// Address of the current device's status word (see device_symbol_address).
+int *device_status_word(cudaStream_t stream, cudaError_t *err);
 
 // Number of SMs of the current device (cached per device).
 int sm_count(cudaError_t *err);
@@ -81,6 +88,14 @@ cudaError_t launch_attention(const AttnArgs &a, cudaStream_t stream);
 // Bytes of workspace the balanced (split) schedule needs on the current device.
 long long attention_workspace_size(int B, int Sq, int Sk, int H, int D, cudaError_t *err);
 
+// Work units of a dense attention call (kAttnUnitRows query rows of one head
+// and batch), in 64 bits; callers reject counts above INT_MAX.
+long long attention_units(int B, int Sq, int H);
+
+// Bytes at the head of the workspace that hold the arrival counters of the
+// split units (zero between calls).
+long long attention_counter_bytes(int B, int Sq, int H);
+
 cudaError_t launch_selftest_wait(unsigned long long limit_ns, cudaStream_t stream);
 
 struct LseMergeArgs {
@@ -105,6 +120,11 @@ cudaError_t launch_varlen_plan(const int *cu_q, const int *cu_k, int n_docs, int
 
 // Bytes of workspace the balanced packed-varlen attention needs on the current device.
 long long varlen_workspace_size(int n_docs, int max_seqlen_q, int H, int D, cudaError_t *err);
+
+// Key mask of the gathered layout: [B, S_img + J] bytes 0/1 from the optional
+// image [B, S_img] and joint [B, J] masks (joint segment first when front).
+cudaError_t launch_merge_mask(const unsigned char *img, const unsigned char *jnt, int B, int S_img, int J, int front,
+                              unsigned char *out, cudaStream_t stream);
 
 // Records a CUDA error for ctx_last_cuda_error() on the calling thread.
 void record_cuda_error(cudaError_t e);

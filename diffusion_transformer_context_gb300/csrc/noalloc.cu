@@ -12,14 +12,15 @@
 // that every GPU loading the library holds until the process exits.
 //
 // Nothing is allocated on any call: the array exists once the module is
-// loaded, and its device address is looked up once per device, on the first
-// call made with that device current (so make that first call before any
-// stream capture begins). All calls share the array and it keeps the last
-// call's contents; the part that must start at zero (the arrival counters)
-// is cleared after every call. Calls that can overlap on the GPU (different
-// streams, or different host threads) race on the array: serialise them.
+// loaded. Its device address is looked up again on every call made outside a
+// stream capture (a device reset reloads the module, possibly at another
+// address); during a capture the address found by the last uncaptured call on
+// that device is used, so make one call on each device before capturing. All
+// calls share the array and it keeps the last call's contents; the part that
+// must start at zero (the arrival counters) is cleared after every call.
+// Calls that can overlap on the GPU (different streams, or different host
+// threads) race on the array: serialise them.
 #include <cstdint>
-#include <mutex>
 
 #include "../../include/ctx.h"
 #include "internal.h"
@@ -32,30 +33,30 @@ constexpr long long kScratchBytes = 44LL << 20;
 
 static __device__ __align__(256) unsigned char g_attn_scratch[kScratchBytes];
 
-std::mutex g_mu;
+// Last looked-up device address of g_attn_scratch, per device. In host code
+// the array's name only stands in for the symbol; the kernel must get this
+// address instead.
 void *g_scratch_addr[64] = {nullptr};
 
-// Device address of g_attn_scratch on the current device. In host code the
-// array's name only stands in for the symbol; the kernel must get this
-// address instead.
-cudaError_t scratch_address(void **out)
+// B*Sq*H*D and B*Sk*H*D within 2^62 and at most INT_MAX work units: the sizes
+// the attention entry point accepts.
+bool sizes_ok(int B, int Sq, int Sk, int H, int D)
 {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
-        return e;
-    if (dev < 0 || dev >= 64)
-        return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> g(g_mu);
-    if (!g_scratch_addr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_attn_scratch);
-        if (e != cudaSuccess)
-            return e;
-        g_scratch_addr[dev] = p;
+    const long long lim = 1LL << 62;
+    long long nq = 1, nk = 1;
+    for (long long x : {static_cast<long long>(B), static_cast<long long>(Sq), static_cast<long long>(H),
+                        static_cast<long long>(D)}) {
+        if (nq > lim / x)
+            return false;
+        nq *= x;
     }
-    *out = g_scratch_addr[dev];
-    return cudaSuccess;
+    for (long long x : {static_cast<long long>(B), static_cast<long long>(Sk), static_cast<long long>(H),
+                        static_cast<long long>(D)}) {
+        if (nk > lim / x)
+            return false;
+        nk *= x;
+    }
+    return ctx::attention_units(B, Sq, H) <= 0x7fffffffLL;
 }
 
 }  // namespace
@@ -68,15 +69,19 @@ extern "C" ctx_status ctx_attn_lq_gkv_noalloc(const void *q, const void *k, cons
         return CTX_ERR_INVALID_ARG;
     if (D != 64 && D != 128)
         return CTX_ERR_UNSUPPORTED;
-    const long long need = ctx_attn_lq_gkv_workspace_size(B, Sq, Sk, H, D);
-    if (need < 0) {
-        ctx::record_cuda_error(cudaErrorUnknown);
+    if (!sizes_ok(B, Sq, Sk, H, D))
+        return CTX_ERR_INVALID_ARG;
+    cudaError_t e = cudaSuccess;
+    const long long need = ctx::attention_workspace_size(B, Sq, Sk, H, D, &e);
+    if (e != cudaSuccess) {
+        ctx::record_cuda_error(e);
         return CTX_ERR_CUDA;
     }
     if (need > kScratchBytes)
         return CTX_ERR_UNSUPPORTED;  // more work units or SMs than the fixed scratch holds
     void *ws = nullptr;
-    cudaError_t e = scratch_address(&ws);
+    e = ctx::device_symbol_address(reinterpret_cast<const void *>(&g_attn_scratch), g_scratch_addr,
+                                   static_cast<cudaStream_t>(stream), &ws);
     if (e != cudaSuccess) {
         ctx::record_cuda_error(e);
         return CTX_ERR_CUDA;
@@ -87,9 +92,8 @@ extern "C" ctx_status ctx_attn_lq_gkv_noalloc(const void *q, const void *k, cons
         return s;
     // Arrival counters sit at the head of the workspace: clear them for the
     // next call even if this one ended early on the device.
-    const long long n_units = static_cast<long long>((Sq + 255) / 256) * H * B;
-    const long long counter_bytes = (n_units * 2 * 4 + 255) / 256 * 256;
-    e = cudaMemsetAsync(ws, 0, static_cast<size_t>(counter_bytes), static_cast<cudaStream_t>(stream));
+    e = cudaMemsetAsync(ws, 0, static_cast<size_t>(ctx::attention_counter_bytes(B, Sq, H)),
+                        static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {
         ctx::record_cuda_error(e);
         return CTX_ERR_CUDA;

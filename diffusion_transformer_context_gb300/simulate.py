@@ -10,8 +10,10 @@ of Q, K, V [B, S, H, D]. One step runs, through the C ABI only:
      exchange is the identity);
   3. ctx_unpack_qkv_ex for every rank, writing its local Q rows into the
      all-ranks query buffer and its K/V rows straight into the gathered K/V
-     buffer of its head group at rows [a*S/A, (a+1)*S/A): the K/V AllGather is
-     this placement, no bytes are copied for it;
+     buffer of its head group at image rows [a*S/A, (a+1)*S/A): the K/V
+     AllGather is this placement, no bytes are copied for it; then
+     ctx_merge_joint_attn_mask builds the [B, S + joint] key mask of the
+     gathered layout from the raw image and joint masks (when there are any);
   4. one ctx_attn_lq_gkv over all ranks: the ranks of head group u share the
      gathered K/V, so their local-Q slices stack into one [S, h_l] query set
      per u, batched over u (rows are independent, so this equals one launch
@@ -30,16 +32,18 @@ instead of queueing one behind the other.
 
 Joint (text) keys and values are inputs every rank already holds; they are
 written once, head-sliced, after the S image rows of each gathered K/V buffer
-(the "re-attach" of the same page), and the merged key mask [B, S + joint]
-is replicated per head group.
+(or before them, for a workload with the joint segment in front: the
+"re-attach" of the same page), and the merged key mask [B, S + joint] is
+built once per head group.
 """
 from __future__ import annotations
 
 import numpy as np
 import torch
 
-from . import (CTX_LAYOUT_TQKV, attn_workspace, ctx_attn_lq_gkv, ctx_attn_lq_gkv_pack_out, ctx_pack_out,
-               ctx_pack_qkv_ex, ctx_sim_all_to_all, ctx_unpack_out_ex, ctx_unpack_qkv_ex)
+from . import (CTX_LAYOUT_TQKV, attn_workspace, ctx_attn_lq_gkv, ctx_attn_lq_gkv_pack_out,
+               ctx_merge_joint_attn_mask, ctx_pack_out, ctx_pack_qkv_ex, ctx_sim_all_to_all, ctx_unpack_out_ex,
+               ctx_unpack_qkv_ex)
 
 
 class SimLayer:
@@ -73,7 +77,14 @@ class SimLayer:
         self.qg = torch.empty((U, B, S, h_l, D), **kw)              # local-Q of all ranks
         self.kg = torch.empty((U, B, Sk, h_l, D), **kw)             # gathered K (+ joint)
         self.vg = torch.empty((U, B, Sk, h_l, D), **kw)
-        self.mask = torch.ones((U * B, Sk), dtype=torch.uint8, device=self.dev) if wl.joint else None
+        # gathered rows: image keys from img0, joint keys from j0 (joint segment in front or after)
+        self.img0, self.j0 = (J, 0) if wl.joint_front else (0, S)
+        u8 = dict(dtype=torch.uint8, device=self.dev)
+        # raw masks as the model hands them over, and the merged key mask of every head group
+        self.img_mask = torch.ones((B, S), **u8) if wl.image_pad_range is not None else None
+        self.jnt_mask = torch.ones((B, J), **u8) if (J and wl.text_len_range is not None) else None
+        has_mask = self.img_mask is not None or self.jnt_mask is not None
+        self.mask = torch.empty((U * B, Sk), **u8) if has_mask else None
         self.out = torch.empty((U, B, S, h_l, D), **kw)
         self.lse = torch.empty((U * B, h_l, S), dtype=torch.float32, device=self.dev)
         # workspace of the balanced (persistent, key-split) attention schedule
@@ -109,42 +120,62 @@ class SimLayer:
             for t, src in enumerate((inp.q, inp.k, inp.v)):
                 self.x[g, t].copy_(inp.shard(src, g))
         if wl.joint:
-            S, h_l, H = wl.S, self.h_l, wl.H
+            J, h_l, H = wl.joint, self.h_l, wl.H
+            j0, j1 = self.j0, self.j0 + J
             for u in range(U):
                 lo, hi = u * h_l, min((u + 1) * h_l, H)
-                self.kg[u, :, S:].zero_()
-                self.vg[u, :, S:].zero_()
+                self.kg[u, :, j0:j1].zero_()
+                self.vg[u, :, j0:j1].zero_()
                 if hi > lo:
-                    self.kg[u, :, S:, :hi - lo].copy_(inp.jk[:, :, lo:hi])
-                    self.vg[u, :, S:, :hi - lo].copy_(inp.jv[:, :, lo:hi])
-            m = inp.key_mask()
-            if m is not None:
-                self.mask.copy_(torch.from_numpy(np.tile(m, (U, 1))))
+                    self.kg[u, :, j0:j1, :hi - lo].copy_(inp.jk[:, :, lo:hi])
+                    self.vg[u, :, j0:j1, :hi - lo].copy_(inp.jv[:, :, lo:hi])
+        if self.img_mask is not None:
+            self.img_mask.copy_(torch.from_numpy(np.ascontiguousarray(inp.image_mask)))
+        if self.jnt_mask is not None:
+            self.jnt_mask.copy_(torch.from_numpy(np.ascontiguousarray(inp.joint_mask)))
         torch.cuda.synchronize(self.dev)
 
     # ---------------------------------------------------------- one step
     def exchange_in(self, stream=None):
-        """Steps 1-3: pack, all-to-all, unpack into the gathered buffers."""
+        """Steps 1-3: pack, all-to-all, unpack into the gathered buffers, and
+        the key mask of the gathered layout."""
         wl = self.wl
-        U, A, B, S, D = wl.U, wl.A, wl.B, wl.S, wl.D
-        S_l, h_l, Sk = self.S_l, self.h_l, self.Sk
+        U, A, B, S = wl.U, wl.A, wl.B, wl.S
+        if not self.pack_view:
+            self.pack_ranks(stream)
+        if U > 1:
+            ctx_sim_all_to_all(self.send, self.recv, A, U, stream=stream)
+        self.unpack_ranks(stream)
+        if self.mask is not None:
+            for u in range(U):
+                ctx_merge_joint_attn_mask(self.img_mask, self.jnt_mask, B, S, wl.joint, self.mask[u * B:(u + 1) * B],
+                                          joint_front=wl.joint_front, stream=stream)
+
+    def pack_ranks(self, stream=None):
+        """Step 1 alone: every rank's pack into its staging buffer."""
+        U = self.wl.U
 
         def pack(g, s):
             a, u = divmod(g, U)
             x = self.x[g]
             ctx_pack_qkv_ex(x[0], x[1], x[2], self.send[a, u], U, self.layout, stream=s)
 
+        self._per_rank(stream, pack)
+
+    def unpack_ranks(self, stream=None):
+        """Step 3 alone: every rank's unpack into the gathered buffers."""
+        wl = self.wl
+        U, B, S, D = wl.U, wl.B, wl.S, wl.D
+        S_l, h_l, Sk = self.S_l, self.h_l, self.Sk
+
         def unpack(g, s):
             a, u = divmod(g, U)
-            r0 = a * U * S_l
+            rq = a * U * S_l            # local-Q rows of rank (a, u) among all ranks' queries
+            rk = self.img0 + rq         # its image rows in the gathered K/V (after joint keys in front)
             src = self.x[g] if self.pack_view else self.recv[a, u]
-            ctx_unpack_qkv_ex(src, self.qg[u, :, r0:], self.kg[u, :, r0:], self.vg[u, :, r0:], U, B,
+            ctx_unpack_qkv_ex(src, self.qg[u, :, rq:], self.kg[u, :, rk:], self.vg[u, :, rk:], U, B,
                               S_l, h_l, D, self.layout, q_batch_stride_rows=S, kv_batch_stride_rows=Sk, stream=s)
 
-        if not self.pack_view:
-            self._per_rank(stream, pack)
-        if U > 1:
-            ctx_sim_all_to_all(self.send, self.recv, A, U, stream=stream)
         self._per_rank(stream, unpack)
 
     def attend(self, stream=None):
@@ -217,7 +248,7 @@ class SimLayer:
 
     def launches_per_step(self) -> int:
         U, R = self.wl.U, self.R
-        n = (R if self.pack_view else 2 * R) + (1 if U > 1 else 0)
+        n = (R if self.pack_view else 2 * R) + (1 if U > 1 else 0) + (U if self.mask is not None else 0)
         if self.attention:
             n += 1
             if U > 1:
@@ -262,16 +293,18 @@ class SimLayer:
         pack_out = 0 if self.fuse_reverse else 2 * one
         return pack_out + 2 * one + one + self.R * wl.B * self.S_l * wl.H * wl.D * 2
 
-    def attn_flops(self, text_len=None, dense: bool = False) -> float:
-        """4 * Sq * K_valid * D per head (QK^T and PV), summed over all ranks."""
+    def attn_flops(self, valid_keys=None, dense: bool = False) -> float:
+        """4 * Sq * K_valid * D per head (QK^T and PV), summed over all ranks.
+        valid_keys: per batch row, the keys the mask leaves valid (None or
+        dense: every gathered key)."""
         wl = self.wl
         if not self.attention:
             return 0.0
         per_b = []
         for b in range(wl.B):
             kv = self.Sk
-            if not dense and wl.joint and text_len is not None:
-                kv = wl.S + int(text_len[b])
+            if not dense and valid_keys is not None:
+                kv = int(valid_keys[b])
             per_b.append(kv)
         # useful work: the real heads (padded heads are overhead, not counted)
         return float(sum(4.0 * wl.H * wl.S * kv * wl.D for kv in per_b))

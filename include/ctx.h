@@ -15,6 +15,8 @@
  *   ctx_unpack_qkv   received buffer -> [B,U*S_l,H/U,D] x3, written at a
  *                    caller-chosen row offset/stride so that K/V land in the
  *                    gathered global buffer (the AllGather placement)
+ *   ctx_merge_joint_attn_mask   the key mask of the gathered layout from
+ *                    the image and joint-text masks (missing side = valid)
  *   ctx_attn_lq_gkv  non-causal MHA of local queries against gathered keys,
  *                    optional per-key mask, scale, fp32 LSE
  *   ctx_pack_out / ctx_unpack_out   the reverse (output) exchange
@@ -163,6 +165,44 @@ ctx_status ctx_unpack_out_ex(const void *recv, void *y, int B, int S_l,
                              void *stream);
 
 /*
+ * ctx_merge_joint_attn_mask — the key mask of the gathered key layout
+ * (vllm-omni PR #7641, follow-up review commit: after the K/V AllGather and
+ * the re-attach of the joint text keys, one merge owns the 2-D key mask).
+ * The gathered keys are S_img image keys and J joint keys, the joint segment
+ * first (joint_front != 0) or last. For every batch row b and key position:
+ *
+ *   key_mask[b][p] = 1 if the key is valid, else 0; image key i is valid
+ *   when image_mask is NULL or image_mask[b][i] != 0, joint key j when
+ *   joint_mask is NULL or joint_mask[b][j] != 0 (a missing side is all valid).
+ *
+ * The result is the key_mask argument of ctx_attn_lq_gkv for the same keys.
+ *
+ * image_mask : NULL, or a byte mask (nonzero = attend) over the gathered
+ *              global image keys whose shape is image_ndim sizes in the host
+ *              array image_dims; it must be 2-D {B, S_img}.
+ * joint_mask : NULL, or a byte mask of the joint keys, shape joint_ndim sizes
+ *              in the host array joint_dims; it must be 2-D {B, J}. J is the
+ *              length of the joint KEY tensor (a cached-K/V step without
+ *              joint queries still has it).
+ * key_mask   : [B, S_img + J] bytes, device, written in full (0/1). With
+ *              both masks NULL every byte is 1, the same as passing no key
+ *              mask to the attention.
+ * Byte arrays have no alignment requirement. Checks, in this order (fail
+ * closed, nothing enqueued): a joint mask that is not 2-D -> INVALID_ARG; a
+ * 4-D image mask -> UNSUPPORTED (it has no key-mask form here, with or
+ * without a joint mask); any other image rank but 2 -> INVALID_ARG; a joint
+ * mask with J = 0 (no joint keys) -> INVALID_ARG; a mask whose dims are not
+ * (B, its segment length) -> INVALID_ARG; key_mask overlapping an input ->
+ * ALIASING; then the common checks.
+ */
+ctx_status ctx_merge_joint_attn_mask(const unsigned char *image_mask, int image_ndim,
+                                     const long long *image_dims,
+                                     const unsigned char *joint_mask, int joint_ndim,
+                                     const long long *joint_dims, int B, int S_img,
+                                     int J, int joint_front, unsigned char *key_mask,
+                                     void *stream);
+
+/*
  * ctx_attn_lq_gkv — local-Q / global-KV attention forward (vllm-omni PR
  * #7641: each rank attends its query slice against the gathered K/V as a
  * plain non-causal attention problem; ChituDiffusion "Fast CP" support
@@ -183,7 +223,14 @@ ctx_status ctx_unpack_out_ex(const void *recv, void *y, int B, int S_l,
  * out      : [B, Sq, H, D], device, same dtype as q.
  * lse      : NULL or [B, H, Sq] float32, device (natural log).
  * workspace, workspace_bytes :
- *            NULL / 0: one CTA per (256 query rows, head, batch) unit.
+ *            NULL / 0: one CTA per (256 query rows, head, batch) unit. This
+ *            form is slower whenever the unit count leaves a partial last
+ *            wave on the GPU's SMs: on a 152-SM GB300, one rank of a 480p
+ *            video layer (Q [1,4095,12,128], 192 units) runs at about 0.69 of
+ *            the balanced schedule's speed, and small calls (fewer units than
+ *            SMs) leave SMs idle. Callers that can should pass a workspace
+ *            (size from ctx_attn_lq_gkv_workspace_size; callers that cannot
+ *            allocate have ctx_attn_lq_gkv_noalloc).
  *            Otherwise device memory of at least
  *            ctx_attn_lq_gkv_workspace_size(B, Sq, Sk, H, D) bytes, 256-byte
  *            aligned, filled with zeros before its first use: a persistent
@@ -249,13 +296,17 @@ long long ctx_attn_lq_gkv_workspace_size(int B, int Sq, int Sk, int H, int D);
  * Same arguments, layouts and results as ctx_attn_lq_gkv, without the
  * workspace: the library keeps a fixed 44 MiB scratch array in device memory
  * (held by every GPU that loads the library until the process exits) and
- * allocates nothing on any call. The first call on each device looks up the
- * array's device address; make that first call before any stream capture.
- * Calls share the array: calls that can overlap on the GPU race and must be
- * serialised by the caller. The arrival counters are cleared after every
- * call. Returns CTX_ERR_UNSUPPORTED when the problem needs more scratch than
- * 44 MiB (more than 131072 work units of 256 query rows, or a grid of more
- * than 160 SMs at D = 128).
+ * allocates nothing on any call. Every call made outside a stream capture
+ * looks up the array's device address on the current device (so a device
+ * reset, which can move it, is followed); a call made while `stream` is
+ * capturing reuses the address of the last uncaptured call on that device, so
+ * make one call on each device before any stream capture (otherwise
+ * CTX_ERR_CUDA, cudaErrorStreamCaptureUnsupported). Calls share the array:
+ * calls that can overlap on the GPU race and must be serialised by the
+ * caller. The arrival counters are cleared after every call. Returns
+ * CTX_ERR_INVALID_ARG for sizes ctx_attn_lq_gkv rejects, CTX_ERR_UNSUPPORTED
+ * when the problem needs more scratch than 44 MiB (more than 131072 work
+ * units of 256 query rows, or a grid of more than 160 SMs at D = 128).
  */
 ctx_status ctx_attn_lq_gkv_noalloc(const void *q, const void *k, const void *v,
                                    const unsigned char *key_mask, float scale,

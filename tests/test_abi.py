@@ -178,3 +178,30 @@ def test_pack_out_fused_validation(lib):
     # more batch blocks (B / B_rank = 5) than destinations U = 4
     assert f(q, k, v, None, nan, o, None, None, 0, 5, 32, 16, 2, 128, 4, 1, 8, 0, None) == INVALID
     assert f(q, k, v, None, nan, o, None, None, 0, 1, 32, 16, 2, 96, 4, 1, 8, 0, None) == UNSUPPORTED
+
+
+def test_mask_merge_validation(lib):
+    """The page's fail-closed cases, rejected on the host in the page's order
+    (joint rank first, then the image rank, joint keys, shapes)."""
+    f = lib.ctx_merge_joint_attn_mask
+    im, jm, out = A0, A0 + MB, A0 + 2 * MB
+    L = ctypes.c_longlong
+
+    def dims(*d):
+        return ctypes.cast((L * len(d))(*d), ctypes.c_void_p)
+
+    B, S, J = 2, 100, 8
+    assert f(im, 2, dims(B, S), jm, 3, dims(B, 1, J), B, S, J, 0, out, None) == INVALID      # joint mask 3-D
+    assert f(im, 4, dims(B, 1, 5, S), jm, 3, dims(B, 1, J), B, S, J, 0, out, None) == INVALID  # joint rank first
+    assert f(im, 4, dims(B, 1, 5, S), jm, 2, dims(B, J), B, S, J, 0, out, None) == UNSUPPORTED  # 4-D + joint
+    assert f(im, 4, dims(B, 1, 5, S), None, 0, None, B, S, J, 0, out, None) == UNSUPPORTED     # 4-D alone
+    assert f(im, 1, dims(S), None, 0, None, B, S, J, 0, out, None) == INVALID                  # image 1-D
+    assert f(None, 0, None, jm, 2, dims(B, J), B, S, 0, 0, out, None) == INVALID               # joint mask, no keys
+    assert f(im, 2, dims(B, S + 1), None, 0, None, B, S, J, 0, out, None) == INVALID           # image length
+    assert f(im, 2, dims(B + 1, S), None, 0, None, B, S, J, 0, out, None) == INVALID           # image batch
+    assert f(None, 0, None, jm, 2, dims(B, J - 1), B, S, J, 0, out, None) == INVALID           # joint length
+    assert f(None, 0, None, jm, 2, dims(1, J), B, S, J, 0, out, None) == INVALID               # joint batch
+    assert f(im, 2, None, None, 0, None, B, S, J, 0, out, None) == INVALID                     # no dims
+    assert f(None, 0, None, None, 0, None, B, S, J, 0, None, None) == INVALID                  # no output
+    assert f(None, 0, None, None, 0, None, 0, S, J, 0, out, None) == INVALID                   # B = 0
+    assert f(im, 2, dims(B, S), None, 0, None, B, S, J, 0, im + 50, None) == ALIASING           # out over image

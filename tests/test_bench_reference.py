@@ -20,7 +20,7 @@ def _line(*args):
     return json.loads(lines[0])
 
 
-@pytest.mark.parametrize("workload,unit", [("tiny", "TFLOP/s"), ("pack", "GB/s")])
+@pytest.mark.parametrize("workload,unit", [("tiny", "TFLOP/s"), ("pack", "GB/s"), ("qwen", "TFLOP/s")])
 def test_reference_line(workload, unit):
     d = _line("--workload", workload, "--steps", "1", "--warmup", "1", "--ref-rows", "8")
     assert d["impl"] == "reference" and d["unit"] == unit and d["value"] > 0

@@ -207,40 +207,91 @@ def test_lse_optional(ctx, orc):
 
 # ---------------------------------------------------------------- full sizes
 
-def _sampled(ctx, orc, B, Sq, Sk, H, D, n_rows, mask=None, seed=1234, split=True):
+def full_size_rows(B, H, Sq, n_random, seed=1234):
+    """(b, h, i) rows checked at full size: n_random seeded random rows spread
+    evenly over every (b, h) pair, the first 128-row tile of the first and
+    last (b, h), and, for EVERY (b, h), the last 256-row work unit (the
+    ragged tail included) and the last 256 rows (so the last full 128-row
+    tile too when the last unit is short)."""
+    rng = np.random.default_rng(seed)
+    rows = set()
+    pairs = [(b, h) for b in range(B) for h in range(H)]
+    for k in range(n_random):
+        b, h = pairs[k % len(pairs)]
+        rows.add((b, h, int(rng.integers(0, Sq))))
+    for b, h in (pairs[0], pairs[-1]):
+        rows.update((b, h, i) for i in range(min(128, Sq)))
+    unit0 = min(((Sq - 1) // 256) * 256, max(0, Sq - 256))
+    for b, h in pairs:
+        rows.update((b, h, i) for i in range(unit0, Sq))
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+def _sampled(ctx, orc, B, Sq, Sk, H, D, n_rows, mask=None, seed=1234, split=True, all_heads_tail=False):
     gen = torch.Generator().manual_seed(seed)
     q, k, v = (workloads.randn(s, gen) for s in ((B, Sq, H, D), (B, Sk, H, D), (B, Sk, H, D)))
     O, L = _run(ctx, q, k, v, mask=mask, split=split)
-    rows_i = workloads.sample_rows(Sq, n_rows)
-    rng = np.random.default_rng(seed)
-    bhi = np.stack([rng.integers(0, B, rows_i.size), rng.integers(0, H, rows_i.size), rows_i], axis=1)
+    if all_heads_tail:
+        bhi = full_size_rows(B, H, Sq, n_rows, seed)
+    else:
+        rows_i = workloads.sample_rows(Sq, n_rows)
+        rng = np.random.default_rng(seed)
+        bhi = np.stack([rng.integers(0, B, rows_i.size), rng.integers(0, H, rows_i.size), rows_i], axis=1)
     eo, el = orc.attention_rows(u16(q), u16(k), u16(v), bhi, mask)
-    got_o = np.stack([O[b, i, h] for b, h, i in bhi])
-    got_l = np.array([L[b, h, i] for b, h, i in bhi])
+    got_o = O[bhi[:, 0], bhi[:, 2], bhi[:, 1]]
+    got_l = L[bhi[:, 0], bhi[:, 1], bhi[:, 2]]
     err = np.abs(got_o - eo)
     assert err.max() <= O_MAX, err.max()
     assert err.mean() <= O_MEAN, err.mean()
     assert np.abs(got_l - el).max() <= LSE_TOL
+    return len(bhi)
+
+
+def test_full_size_row_sample_covers_the_tails():
+    """The sampler itself: >= 512 random rows over all heads plus every
+    (b, h)'s last unit (the 480p call: 4095 query rows, a ragged last tile)."""
+    bhi = full_size_rows(1, 12, 4095, 512)
+    assert len(bhi) >= 512 + 12 * 255
+    for h in range(12):
+        sel = bhi[bhi[:, 1] == h, 2]
+        assert set(range(3840, 4095)) <= set(sel.tolist())
 
 
 def test_qwen_full_size_sampled(ctx, orc):
     """U=2 x A=2 Qwen-Image-like: both head groups batched, local-Q of both
     A ranks stacked: Q [2,4096,12,128] vs K/V [2,4352,12,128] with the
-    text-padding mask (valid text length uniform in [32,256])."""
+    text-padding mask (valid text length uniform in [32,256]), merged by the
+    oracle from the raw joint mask (joint keys after the image keys)."""
     wl = workloads.WORKLOADS["qwen"]
     inp = workloads.make_inputs(wl)
-    mask = np.tile(inp.key_mask(), (wl.U, 1))
-    _sampled(ctx, orc, wl.U * wl.B, wl.S, wl.Sk, wl.h_l, wl.D, 512, mask=mask)
+    m = orc.merge_joint_attn_mask(inp.image_mask, inp.joint_mask, wl.B, wl.S, wl.joint, wl.joint_front)
+    mask = np.tile(m, (wl.U, 1))
+    _sampled(ctx, orc, wl.U * wl.B, wl.S, wl.Sk, wl.h_l, wl.D, 512, mask=mask, all_heads_tail=True)
 
 
 def test_wan480_full_size_sampled(ctx, orc):
+    """The 480p call as the benchmark runs it (8 ranks' local-Q stacked: Q
+    [1,32760,12,128] vs K/V [1,32760,12,128], balanced schedule): 512 random
+    rows over all 12 heads plus every head's last 256 rows."""
     wl = workloads.WORKLOADS["wan480"]
-    _sampled(ctx, orc, wl.U * wl.B, wl.S, wl.Sk, wl.h_l, wl.D, 384)
+    n = _sampled(ctx, orc, wl.U * wl.B, wl.S, wl.Sk, wl.h_l, wl.D, 512, all_heads_tail=True)
+    assert n >= 512 + 12 * 256
+
+
+def test_wan480_one_rank_full_size_sampled(ctx, orc):
+    """One rank of the 480p layer alone (Q [1,4095,12,128], the ragged last
+    tile of 127 rows) against the whole gathered K/V."""
+    _sampled(ctx, orc, 1, 4095, 32760, 12, 128, 512, all_heads_tail=True)
 
 
 def test_wan14b_full_size_sampled(ctx, orc):
+    """The Wan-14B-like call as the layer runs it (4 head groups batched, the
+    local-Q of both A ranks stacked: Q [4,75600,10,128] vs K/V
+    [4,75600,10,128]): 512 random rows over all 40 (b, h) pairs plus every
+    pair's last 256 rows (the last unit holds 80)."""
     wl = workloads.WORKLOADS["wan14b"]
-    _sampled(ctx, orc, wl.U * wl.B, wl.S, wl.Sk, wl.h_l, wl.D, 256)
+    n = _sampled(ctx, orc, wl.U * wl.B, wl.S, wl.Sk, wl.h_l, wl.D, 512, all_heads_tail=True)
+    assert n >= 512 + 40 * 256
 
 
 @pytest.mark.parametrize("B,Sq,Sk,H", [(1, 4095, 32760, 12), (1, 300, 4096, 1), (2, 2000, 3000, 5),

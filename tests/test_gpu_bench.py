@@ -35,6 +35,24 @@ def test_attention_workload_line():
     e = d["e2e"]
     assert e["readback_verified"] is True
     assert e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0 and e["value"] > 0
+    # the layout-only workload beside the attention line: U = 4 pack + all-to-all + unpack
+    p = d["pack"]
+    assert p["workload"] == "pack" and p["unit"] == "GB/s" and p["bound"] == "hbm" and p["achieved"] > 0
+    assert p["frac"] == pytest.approx(p["achieved"] / p["peak"], abs=1e-4)
+    # the packs and the unpacks each read and write the 75.5 MB of all ranks' Q/K/V once
+    assert p["algorithmic_bytes"] == {"pack": 2 * 3 * 4 * 1024 * 24 * 128 * 2, "unpack": 2 * 3 * 4 * 1024 * 24 * 128 * 2}
+    assert p["gpu_launches_per_replay"] == {"pack": 4, "unpack": 4}
+    assert p["pack_gbs"] > 0 and p["unpack_gbs"] > 0 and p["step_gbs"] > 0
+
+
+@pytest.mark.gpu
+def test_masked_workload_line():
+    # the Qwen-like layer: the key-mask merge runs in the step, FLOPs count the valid keys only
+    d = run_bench("--workload", "qwen", "--steps", "3", "--warmup", "3", "--no-cpu-baseline", "--no-clocks",
+                  "--no-pack")
+    assert d["unit"] == "TFLOP/s" and d["value"] > 0 and "pack" not in d
+    assert d["roofline"]["algorithmic_flops_per_launch"] < 4.0 * 24 * 4096 * 4352 * 128
+    assert d["e2e"]["readback_verified"] is True
 
 
 @pytest.mark.gpu

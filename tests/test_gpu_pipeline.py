@@ -32,7 +32,7 @@ def _oracle_side(orc, inp, layout=0):
     jk = u16(inp.jk) if inp.jk is not None else None
     jv = u16(inp.jv) if inp.jv is not None else None
     return orc.ulysses_agkv_forward([s[0] for s in sh], [s[1] for s in sh], [s[2] for s in sh],
-                                    wl.U, wl.A, jk, jv, layout)
+                                    wl.U, wl.A, jk, jv, layout, joint_front=wl.joint_front)
 
 
 def _check_layer(ctx, orc, wl, n_rows=None, layout=0, pack_view=True):
@@ -53,7 +53,14 @@ def _check_layer(ctx, orc, wl, n_rows=None, layout=0, pack_view=True):
         assert np.array_equal(u16(sim.rank_q(g)), res["q"][g]), f"Q rank {g}"
     if not sim.attention:
         return
-    mask = inp.key_mask()
+    # the key mask of the gathered layout: the oracle's merge of the raw masks,
+    # and the library's (one per head group) bit for bit
+    mask = orc.merge_joint_attn_mask(inp.image_mask, inp.joint_mask, wl.B, wl.S, wl.joint, wl.joint_front)
+    if mask is None:
+        assert sim.mask is None
+    else:
+        for u in range(U):
+            assert np.array_equal(sim.mask[u * wl.B:(u + 1) * wl.B].cpu().numpy(), mask), f"key mask group {u}"
     # attention of every rank (rank g: its local-Q against its head group's K/V)
     out = sim.out.float().cpu().numpy()
     lse = sim.lse.cpu().numpy().reshape(U, wl.B, sim.h_l, wl.S)
@@ -143,6 +150,27 @@ def test_uneven_heads(ctx, orc, wl):
 ], ids=lambda w: w.name)
 def test_interleaved_staging_layout(ctx, orc, wl):
     _check_layer(ctx, orc, wl, layout=1)
+
+
+@pytest.mark.parametrize("wl", [
+    # a 2-D image mask (padded suffix of the global sequence) with text padding, joint keys in front
+    workloads.custom("img_mask_front_u2a2", B=2, S=512, H=8, D=128, U=2, A=2, joint=64, text_len_range=(1, 64),
+                     joint_front=True, image_pad_range=(1, 100)),
+    # the same rear, uneven heads
+    workloads.custom("img_mask_rear_u4a2_h14", B=2, S=512, H=14, D=64, U=4, A=2, joint=32, text_len_range=(4, 32),
+                     image_pad_range=(10, 60)),
+    # an image mask only (no joint keys): the key mask is the image mask
+    workloads.custom("img_mask_only_u1a4", B=1, S=1000, H=3, D=128, U=1, A=4, image_pad_range=(200, 300)),
+    # joint keys without any mask (cached K/V reuse: joint K/V, no joint query): no key mask at all
+    workloads.custom("joint_nomask_front_u2a2", B=1, S=512, H=4, D=128, U=2, A=2, joint=48, joint_front=True),
+    # joint keys without a joint mask but with an image mask: the joint segment is filled with True
+    workloads.custom("joint_fill_u2a1", B=2, S=384, H=4, D=128, U=2, A=1, joint=40, image_pad_range=(0, 50)),
+], ids=lambda w: w.name)
+def test_mask_merge_layers(ctx, orc, wl):
+    """The a4 step with non-trivial masks (vllm-omni PR #7641 follow-up
+    review commit's cases): the merged key mask of every head group equals
+    the oracle's bit for bit and the attention of every rank matches."""
+    _check_layer(ctx, orc, wl)
 
 
 def test_qwen_layer(ctx, orc):

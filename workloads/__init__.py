@@ -10,7 +10,13 @@ Recipe (the same for every workload):
     multi-rank test on the sglang PR #33667 page, "test_usp_packed_qkv_a2a");
   * ``randn`` in fp32, then a round-to-nearest-even cast to bf16 (or fp16);
   * Q, K, V are independent draws from the same generator, in that order,
-    followed by the joint (text) K/V and then the per-batch text lengths;
+    followed by the joint (text) K/V, the per-batch text lengths and, where a
+    workload pads its image sequence, the per-batch image padding lengths;
+  * masks are produced raw, one per side, as the model would hand them over:
+    the joint (text) mask [B, joint] marks the first L_t text tokens valid,
+    the image mask [B, S] marks a padded suffix of the global image sequence
+    invalid; merging them into the gathered key layout is a step of the
+    method (the oracle and the CUDA library each do it themselves);
   * the GLOBAL sequence ``[B, S, H, D]`` is generated once and split into the
     per-rank input shards, rank ``g = a*U + u`` holding rows
     ``[g*S_l, (g+1)*S_l)`` (vllm-omni PR #7641, "Compose Ulysses with
@@ -43,9 +49,13 @@ class Workload:
     D      : head dim
     U      : Ulysses degree (head reshard group size)
     A      : AllGather-KV degree
-    joint  : joint (text) tokens appended to the gathered K/V (rear), 0 = none
-    text_len_range : inclusive range of valid text lengths (key padding mask)
+    joint  : joint (text) tokens re-attached to the gathered K/V, 0 = none
+    text_len_range : inclusive range of valid text lengths (joint padding
+             mask), None = no joint mask
     attention : whether the workload runs the attention step
+    joint_front : joint keys placed before the image keys (default after)
+    image_pad_range : inclusive range of padded image tokens at the end of
+             the global sequence (2-D image mask), None = no image mask
     """
 
     name: str
@@ -58,6 +68,8 @@ class Workload:
     joint: int = 0
     text_len_range: Optional[tuple] = None
     attention: bool = True
+    joint_front: bool = False
+    image_pad_range: Optional[tuple] = None
 
     @property
     def ranks(self) -> int:
@@ -104,9 +116,10 @@ WORKLOADS = {
 
 
 def custom(name: str, B: int, S: int, H: int, D: int, U: int, A: int = 1,
-           joint: int = 0, text_len_range=None, attention: bool = True) -> Workload:
+           joint: int = 0, text_len_range=None, attention: bool = True, joint_front: bool = False,
+           image_pad_range=None) -> Workload:
     """A workload with explicit sizes (used for ragged / edge-case tests)."""
-    return Workload(name, B, S, H, D, U, A, joint, text_len_range, attention)
+    return Workload(name, B, S, H, D, U, A, joint, text_len_range, attention, joint_front, image_pad_range)
 
 
 def randn(shape, gen: torch.Generator, dtype: str = "bf16") -> torch.Tensor:
@@ -125,25 +138,13 @@ class Inputs:
     jv: Optional[torch.Tensor]  # [B, joint, H, D]
     text_len: Optional[np.ndarray]  # [B] valid text lengths (int64) or None
     dtype: str = "bf16"
+    image_mask: Optional[np.ndarray] = None  # [B, S] uint8, 1 = valid image key, or None
+    joint_mask: Optional[np.ndarray] = None  # [B, joint] uint8, 1 = valid text key, or None
 
     def shard(self, t: torch.Tensor, g: int) -> torch.Tensor:
         """Rank g's input rows [g*S_l, (g+1)*S_l) (contiguous copy)."""
         S_l = self.wl.S_l
         return t[:, g * S_l:(g + 1) * S_l].contiguous()
-
-    def key_mask(self) -> Optional[np.ndarray]:
-        """[B, S + joint] uint8 key mask, 1 = attend, for the gathered keys.
-
-        Image keys are always valid; text keys [0, L_t) are valid and the
-        padded suffix [L_t, joint) is masked (joint placed after the image).
-        """
-        if self.text_len is None:
-            return None
-        B, S, J = self.wl.B, self.wl.S, self.wl.joint
-        m = np.ones((B, S + J), dtype=np.uint8)
-        for b in range(B):
-            m[b, S + int(self.text_len[b]):] = 0
-        return m
 
 
 def make_inputs(wl: Workload, seed: int = SEED, dtype: str = "bf16") -> Inputs:
@@ -154,6 +155,7 @@ def make_inputs(wl: Workload, seed: int = SEED, dtype: str = "bf16") -> Inputs:
     v = randn(shape, gen, dtype)
     jk = jv = None
     text_len = None
+    joint_mask = image_mask = None
     if wl.joint:
         jshape = (wl.B, wl.joint, wl.H, wl.D)
         jk = randn(jshape, gen, dtype)
@@ -161,7 +163,16 @@ def make_inputs(wl: Workload, seed: int = SEED, dtype: str = "bf16") -> Inputs:
         if wl.text_len_range is not None:
             lo, hi = wl.text_len_range
             text_len = torch.randint(lo, hi + 1, (wl.B,), generator=gen).numpy().astype(np.int64)
-    return Inputs(wl, q, k, v, jk, jv, text_len, dtype)
+            joint_mask = np.zeros((wl.B, wl.joint), dtype=np.uint8)
+            for b in range(wl.B):
+                joint_mask[b, :int(text_len[b])] = 1
+    if wl.image_pad_range is not None:
+        lo, hi = wl.image_pad_range
+        pad = torch.randint(lo, hi + 1, (wl.B,), generator=gen).numpy()
+        image_mask = np.ones((wl.B, wl.S), dtype=np.uint8)
+        for b in range(wl.B):
+            image_mask[b, wl.S - int(pad[b]):] = 0
+    return Inputs(wl, q, k, v, jk, jv, text_len, dtype, image_mask, joint_mask)
 
 
 def as_u16(t: torch.Tensor) -> np.ndarray:
