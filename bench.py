@@ -259,15 +259,17 @@ def run_pack_line(args, dev, peaks, peak_kind):
     each Q/K/V [1,1024,24,128], packed into [4,3,1,1024,6,128] staging
     buffers and, after the exchange, unpacked to [1,4096,6,128] per rank.
 
-    `achieved` is the library's pack and unpack kernels in HBM terms: the
-    four ranks' packs (one CUDA graph, ranks' launches concurrent) and,
-    separately, the four unpacks, each replayed in rotation over buffer sets
-    whose total is several times L2, so every read comes from HBM and the
-    write-back of every written line falls inside the timed region (only the
-    last replay's dirty lines escape it, 1/K of the writes). `step_gbs` is
-    the whole simulated step (pack + all-to-all + unpack) back to back: there
-    the staging buffers written by one kernel are read by the next while they
-    are still in L2, so it is not an HBM figure."""
+    `achieved` is the library's pack and unpack kernels in HBM terms. The
+    work rotates over n buffer sets whose total is several times L2, so every
+    read comes from HBM and every written line is written back inside the
+    timed region (all but the last replay's). One CUDA graph holds the four
+    ranks' packs (launches concurrent, as ranks run) of every set in turn,
+    another the unpacks; each is replayed back to back, so graph launches
+    are amortised over n sets as inside a layer's graph. `copy_gbs` is a
+    plain device copy of the same bytes per set timed the same way: the
+    reference for transfers of this size. `step_gbs` is the whole simulated
+    step (pack + all-to-all + unpack): there the staging buffers written by
+    one kernel are read by the next from L2, so it is not an HBM figure."""
     import torch
 
     import workloads
@@ -285,34 +287,41 @@ def run_pack_line(args, dev, peaks, peak_kind):
     for sim in sims:
         sim.load(inp)
         sim.step()  # library set-up outside any capture
+    b_pack, b_unpack = one.pack_bytes(), one.unpack_bytes()
+    b_step = b_pack + one.a2a_bytes() + b_unpack
+    src = [torch.empty(b_pack // 4, dtype=torch.bfloat16, device=dev).fill_(1) for _ in range(n_sets)]
+    dst = [torch.empty_like(x) for x in src]
     torch.cuda.synchronize(dev)
-    graphs = {"pack": [], "unpack": [], "step": []}
-    for sim in sims:
-        for name, fn in (("pack", sim.pack_ranks), ("unpack", sim.unpack_ranks), ("step", sim.exchange_in)):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                fn()
-            graphs[name].append(g)
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n_sets):
+                fn(i)
+        return g
+
+    graphs = {"pack": capture(lambda i: sims[i].pack_ranks()),
+              "unpack": capture(lambda i: sims[i].unpack_ranks()),
+              "step": capture(lambda i: sims[i].exchange_in()),
+              "copy": capture(lambda i: dst[i].copy_(src[i]))}
     torch.cuda.synchronize(dev)
     stream = torch.cuda.current_stream(dev)
-    reps = max(args.steps, 20) * n_sets
+    reps = max(args.steps, 20)
 
     def timed(name):
-        gs = graphs[name]
-        for i in range(2 * n_sets):
-            gs[i % n_sets].replay()
+        g = graphs[name]
+        for _ in range(3):
+            g.replay()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize(dev)
         e0.record(stream)
-        for i in range(reps):
-            gs[i % n_sets].replay()
+        for _ in range(reps):
+            g.replay()
         e1.record(stream)
         torch.cuda.synchronize(dev)
-        return e0.elapsed_time(e1) / reps
+        return e0.elapsed_time(e1) / (reps * n_sets)  # per set
 
-    ms_pack, ms_unpack, ms_step = timed("pack"), timed("unpack"), timed("step")
-    b_pack, b_unpack = one.pack_bytes(), one.unpack_bytes()
-    b_step = b_pack + one.a2a_bytes() + b_unpack
+    ms_pack, ms_unpack, ms_step, ms_copy = timed("pack"), timed("unpack"), timed("step"), timed("copy")
     gbs = (b_pack + b_unpack) / ((ms_pack + ms_unpack) * 1e-3) / 1e9
 
     def rate(b, ms):
@@ -326,11 +335,12 @@ def run_pack_line(args, dev, peaks, peak_kind):
             "pack_gbs": rate(b_pack, ms_pack), "unpack_gbs": rate(b_unpack, ms_unpack),
             "pack_ms": round(ms_pack, 4), "unpack_ms": round(ms_unpack, 4),
             "algorithmic_bytes": {"pack": b_pack, "unpack": b_unpack},
-            "timing": f"CUDA graphs replayed back to back over {n_sets} buffer sets of {set_bytes >> 20} MiB "
-                      f"(L2 {l2_bytes >> 20} MiB): reads from HBM, write-back inside the timed region",
-            "replays": reps, "gpu_launches_per_replay": {"pack": wl.ranks, "unpack": wl.ranks},
+            "copy_gbs": rate(b_pack, ms_copy),
+            "timing": f"one CUDA graph over {n_sets} buffer sets of {set_bytes >> 20} MiB (L2 {l2_bytes >> 20} MiB), "
+                      f"replayed {reps} times back to back: reads from HBM, write-back inside the timed region",
+            "gpu_launches_per_set": {"pack": wl.ranks, "unpack": wl.ranks},
             "step_gbs": rate(b_step, ms_step), "step_ms": round(ms_step, 4),
-            "step_note": "pack + simulated all-to-all + unpack back to back; staging buffers re-read from L2",
+            "step_note": "pack + simulated all-to-all + unpack; staging buffers re-read from L2",
             "traffic": recorded_traffic("pack", "relayout")}
 
 

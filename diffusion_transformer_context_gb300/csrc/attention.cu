@@ -89,7 +89,7 @@ struct Params {
     float scale_log2;
     int *status;
     unsigned long long wait_limit_ns;
-    int *counters;         // [n_units][kTiles] arrivals at split units (zero between calls)
+    int *counters;         // [n_units][kTiles][2] arrived / written pieces of split units (zero between calls)
     float2 *part_ml;       // [2*grid][kTiles*kBM] (m, l) of partial segments
     float4 *part_o;        // [2*grid][D/4][kTiles*kBM] unnormalised O of partial segments
 };
@@ -106,8 +106,8 @@ struct Layout {
     static constexpr int kVOff = kKOff + kStages * kKVBytes;
     static constexpr int kBarOff = kVOff + kStages * kKVBytes;
     // q_full, q_empty, k_full[S], k_empty[S], v_full[S], v_empty[S],
-    // s_full[T], p_full[T], o_full[T], o_empty[T], seg_done[T], merge_go[T], mma_done
-    static constexpr int kNumBars = 2 + 4 * kStages + 6 * kTiles + 1;
+    // s_full[T], p_full[T], o_full[T], o_empty[T], seg_done[T], merge_go[T], written_go[T], mma_done
+    static constexpr int kNumBars = 2 + 4 * kStages + 7 * kTiles + 1;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     // per softmax warp: its 32 rows x 64 output columns, staged so that the
     // output rows leave as whole 128-byte lines
@@ -231,6 +231,14 @@ __device__ __forceinline__ long long tail_start(const Params &p, long long total
 __device__ __forceinline__ int tail_cta_of(const Params &p, long long total, long long it)
 {
     return static_cast<int>(((it + 1) * p.grid + total - 1) / total) - 1;
+}
+
+// Slot of CTA cc's piece of the unit whose first split iteration is `first`:
+// the CTA's first segment when its range starts inside the unit, else its
+// last one.
+__device__ __forceinline__ int tail_slot(const Params &p, long long total, long long first, int cc)
+{
+    return (tail_start(p, total, cc) >= first) ? 2 * cc : 2 * cc + 1;
 }
 
 // Iterations shared by the split schedule: the tail of the dense schedule,
@@ -399,7 +407,14 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint3
     }
 }
 
-template <int D, bool BF16>
+// kTicketMerge: the merge protocol of units cut between CTAs (see the partial
+// segment branch): a piece takes its arrival ticket as soon as its O is
+// complete and the last one merges the others with its own O from TMEM
+// (true), or every piece writes its partial and the last to have written
+// merges them all from the workspace (false). The first shortens the end of
+// a short call; the second is kept for long calls, where the kernel built
+// without the ticket code runs its key-block loop faster.
+template <int D, bool BF16, bool kTicketMerge>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const Params p)
@@ -420,7 +435,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *o_empty = o_full + kTiles;
     uint64_t *seg_done = o_empty + kTiles;
     uint64_t *merge_go = seg_done + kTiles;
-    uint64_t *mma_done = merge_go + kTiles;
+    uint64_t *written_go = merge_go + kTiles;
+    uint64_t *mma_done = written_go + kTiles;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
     volatile int *merge_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 8);  // [kTiles]
@@ -444,6 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(o_empty + t, 128);
             ptx::mbar_init(seg_done + t, 128);
             ptx::mbar_init(merge_go + t, 1);
+            ptx::mbar_init(written_go + t, 1);
             merge_flag[t] = 0;
         }
         ptx::mbar_init(mma_done, 1);
@@ -610,7 +627,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tS = tmem + lane_off + t * kBN;
         const uint32_t tO = tmem + lane_off + 2 * kBN + t * D;
         const float c = p.scale_log2;
-        int g = 0, segi = 0, pc = 0, act = 0;
+        int g = 0, segi = 0, act = 0;
+        int ph = 0;  // phase parities of merge_go (bit 0), seg_done (bit 1) and written_go (bit 2)
         bool ok = true;
         for (; ok; ++segi) {
             const unsigned char *mrow;
@@ -854,6 +872,157 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (p.lse && qrow < q_end)
                     p.lse[(static_cast<size_t>(b) * p.H + h) * p.Sq + qrow] = lse_val;
+            } else if constexpr (kTicketMerge) {
+                // Partial segment (the unit is cut between CTAs). The tile's leader
+                // takes an arrival ticket as soon as O is complete. Every piece but
+                // the last to arrive writes its unnormalised O and (m, l) to this
+                // CTA's slot and then counts itself written; the last piece waits
+                // for the others' writes and merges them by log-sum-exp with its
+                // own O, read straight from TMEM (it never writes or re-reads it).
+                const long long total = split_total(p);
+                const long long first = sg.first;  // the unit's first iteration in the split order
+                const int c_lo = tail_cta_of(p, total, first), c_hi = tail_cta_of(p, total, first + sg.nb - 1);
+                int *const arrive = p.counters + (static_cast<size_t>(sg.unit) * kTiles + t) * 2;
+                int *const written = arrive + 1;
+                if (tile_leader) {
+                    merge_flag[t] = (atomicAdd(arrive, 1) == c_hi - c_lo);
+                    ptx::mbar_arrive(merge_go + t);
+                }
+                if (!(ok = wait_bar_warp(merge_go + t, ph & 1, abort_flag, p)))
+                    break;
+                ph ^= 1;
+                if (!merge_flag[t]) {
+                    float4 *po = p.part_o + static_cast<size_t>(sg.slot) * (D / 4) * (kTiles * kBM) + prow;
+#pragma unroll
+                    for (int c0 = 0; c0 < D / 32; ++c0) {
+                        uint32_t o[32];
+                        ptx::tmem_ld32(tO + c0 * 32, o);
+                        ptx::tmem_ld_wait();
+                        ptx::reg_fence32(o);
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            __stcg(po + static_cast<size_t>(c0 * 8 + k) * (kTiles * kBM),
+                                   make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
+                                               __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3])));
+                    }
+                    __stcg(p.part_ml + static_cast<size_t>(sg.slot) * (kTiles * kBM) + prow,
+                           make_float2(m_run, l_run));
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(o_empty + t);
+                    __threadfence();
+                    ptx::mbar_arrive(seg_done + t);
+                    if (tile_leader && wait_bar(seg_done + t, (ph >> 1) & 1, abort_flag, p)) {
+                        __threadfence();
+                        atomicAdd(written, 1);
+                    }
+                    ph ^= 2;
+                } else {
+                    // Wait (bounded) until the other pieces' partials are written; the
+                    // leader then releases the tile's threads through written_go.
+                    if (tile_leader) {
+                        const uint64_t t0 = ptx::globaltimer();
+                        while (!*abort_flag) {
+                            if (*reinterpret_cast<volatile int *>(written) == c_hi - c_lo) {
+                                __threadfence();
+                                break;
+                            }
+                            if (ptx::globaltimer() - t0 > p.wait_limit_ns) {
+                                *abort_flag = 1;
+                                atomicExch(p.status, kStatusTimeout);
+                                break;
+                            }
+                            __nanosleep(64);
+                        }
+                        ptx::mbar_arrive(written_go + t);
+                    }
+                    if (!(ok = wait_bar_warp(written_go + t, (ph >> 2) & 1, abort_flag, p)) || *abort_flag) {
+                        ok = false;
+                        break;
+                    }
+                    ph ^= 4;
+                    // Every piece in the unit's order (this one's values from registers
+                    // and TMEM, the others' from their slots): the same arithmetic
+                    // whichever piece arrives last, so results are reproducible.
+                    // Running maximum and sum of the pieces' (m, l) in one pass:
+                    float M = -INFINITY, lsum = 0.f;
+#pragma unroll 4
+                    for (int cc = c_lo; cc <= c_hi; ++cc) {
+                        const float2 ml =
+                            cc == cta ? make_float2(m_run, l_run)
+                                      : __ldcg(p.part_ml + static_cast<size_t>(tail_slot(p, total, first, cc)) *
+                                                               (kTiles * kBM) + prow);
+                        if (ml.x == -INFINITY)
+                            continue;
+                        if (ml.x > M) {
+                            lsum = (M == -INFINITY ? 0.f : lsum * ptx::ex2_approx(M - ml.x)) + ml.y;
+                            M = ml.x;
+                        } else {
+                            lsum += ptx::ex2_approx(ml.x - M) * ml.y;
+                        }
+                    }
+                    const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
+                    // rows leave through the warp's staging area as whole 128-byte lines
+                    const unsigned long long orow =
+                        qrow < q_end ? reinterpret_cast<unsigned long long>(out_row<D>(p, b, h, qrow)) : 0ull;
+                    uint4 *const stg = reinterpret_cast<uint4 *>(
+                        reinterpret_cast<uint8_t *>(bars) + (L::kEpiOff - L::kBarOff) + (warp - 4) * L::kEpiWarpBytes);
+#pragma unroll 1
+                    for (int hf = 0; hf < D / 64; ++hf) {
+                        // 64 columns at a time: a slot's 16 float4 in flight together
+                        // (one L2 round trip per piece), this piece's from TMEM
+                        float o[64];
+#pragma unroll
+                        for (int k = 0; k < 64; ++k)
+                            o[k] = 0.f;
+                        for (int cc = c_lo; cc <= c_hi; ++cc) {
+                            float2 ml;
+                            float4 v[16];
+                            if (cc == cta) {
+                                ml = make_float2(m_run, l_run);
+                                uint32_t r[64];
+                                ptx::tmem_ld32(tO + hf * 64, r);
+                                ptx::tmem_ld32(tO + hf * 64 + 32, r + 32);
+                                ptx::tmem_ld_wait();
+                                ptx::reg_fence32(r);
+                                ptx::reg_fence32(r + 32);
+                                if (hf == D / 64 - 1) {
+                                    ptx::tc_fence_before();
+                                    ptx::mbar_arrive(o_empty + t);  // O is in registers: the next PV may start
+                                }
+#pragma unroll
+                                for (int k = 0; k < 16; ++k)
+                                    v[k] = make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
+                                                       __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
+                            } else {
+                                const int sl = tail_slot(p, total, first, cc);
+                                ml = __ldcg(p.part_ml + static_cast<size_t>(sl) * (kTiles * kBM) + prow);
+                                const float4 *src =
+                                    p.part_o + (static_cast<size_t>(sl) * (D / 4) + hf * 16) * (kTiles * kBM) + prow;
+#pragma unroll
+                                for (int k = 0; k < 16; ++k)
+                                    v[k] = __ldcg(src + static_cast<size_t>(k) * (kTiles * kBM));
+                            }
+                            const float w = (ml.x == -INFINITY) ? 0.f : ptx::ex2_approx(ml.x - M);
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) {
+                                o[4 * k] += w * v[k].x;
+                                o[4 * k + 1] += w * v[k].y;
+                                o[4 * k + 2] += w * v[k].z;
+                                o[4 * k + 3] += w * v[k].w;
+                            }
+                        }
+                        stage32<BF16>(stg, lane, 0, o, inv);
+                        stage32<BF16>(stg, lane, 1, o + 32, inv);
+                        store_staged(stg, lane, orow, hf * 8);
+                    }
+                    if (p.lse && qrow < q_end)
+                        p.lse[(static_cast<size_t>(b) * p.H + h) * p.Sq + qrow] =
+                            lsum > 0.f ? (M + log2f(lsum)) * kLn2 : -INFINITY;
+                    if (tile_leader) {
+                        *arrive = 0;  // every piece has arrived and written: leave the
+                        *written = 0; // workspace zeroed for the next call
+                    }
+                }
             } else {
                 // Partial segment: unnormalised O and (m, l) go to this CTA's slot.
                 float4 *po = p.part_o + static_cast<size_t>(sg.slot) * (D / 4) * (kTiles * kBM) + prow;
@@ -879,8 +1048,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int c_lo = tail_cta_of(p, total, first), c_hi = tail_cta_of(p, total, first + sg.nb - 1);
                 if (tile_leader) {
                     int last = 0;
-                    if (wait_bar(seg_done + t, pc & 1, abort_flag, p)) {
-                        int *cnt = p.counters + static_cast<size_t>(sg.unit) * kTiles + t;
+                    if (wait_bar(seg_done + t, (ph >> 1) & 1, abort_flag, p)) {
+                        int *cnt = p.counters + (static_cast<size_t>(sg.unit) * kTiles + t) * 2;
                         const int old = atomicAdd(cnt, 1);
                         last = (old == c_hi - c_lo);
                         if (last)
@@ -890,16 +1059,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     merge_flag[t] = last;
                     ptx::mbar_arrive(merge_go + t);
                 }
-                if (!(ok = wait_bar_warp(merge_go + t, pc & 1, abort_flag, p)))
+                if (!(ok = wait_bar_warp(merge_go + t, ph & 1, abort_flag, p)))
                     break;
-                ++pc;
+                ph ^= 3;  // merge_go and seg_done each took one phase
                 if (merge_flag[t]) {
                     // Last segment of this unit to finish: combine every segment by log-sum-exp.
                     // running maximum and sum of the pieces' (m, l) in one pass
                     float M = -INFINITY, lsum = 0.f;
 #pragma unroll 4
                     for (int cc = c_lo; cc <= c_hi; ++cc) {
-                        const int sl = (tail_start(p, total, cc) >= first) ? 2 * cc : 2 * cc + 1;
+                        const int sl = tail_slot(p, total, first, cc);
                         const float2 ml = __ldcg(p.part_ml + static_cast<size_t>(sl) * (kTiles * kBM) + prow);
                         if (ml.x == -INFINITY)
                             continue;
@@ -925,7 +1094,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int k = 0; k < 64; ++k)
                             o[k] = 0.f;
                         for (int cc = c_lo; cc <= c_hi; ++cc) {
-                            const int sl = (tail_start(p, total, cc) >= first) ? 2 * cc : 2 * cc + 1;
+                            const int sl = tail_slot(p, total, first, cc);
                             const float2 ml = __ldcg(p.part_ml + static_cast<size_t>(sl) * (kTiles * kBM) + prow);
                             const float4 *src =
                                 p.part_o + (static_cast<size_t>(sl) * (D / 4) + hf * 16) * (kTiles * kBM) + prow;
@@ -1019,7 +1188,17 @@ cudaError_t make_map(CUtensorMap *m, const void *base, int B, int S, int H, int 
 struct Schedule {
     int n_units, n_kblocks, grid, dp_waves;
     long long tail_iters;
+    bool ticket_merge;  // merge split units with the ticket-first protocol
 };
+
+// Calls whose CTAs each run at most this many key blocks (about 250 us at the
+// kernel's rate) take the ticket-first merge: the merge that ends them is a
+// large share of their time. Measured on GB300, same box, outputs bitwise
+// equal: one Qwen-like rank (21 key blocks per CTA) 757 -> 803 TFLOP/s, the
+// batched Qwen-like layer (86) 1254 -> 1284; one Wan-like 480p rank (323)
+// 1644 -> 1614 and the batched 480p call 1658 -> 1619 with it, so those keep
+// the write-then-count merge.
+constexpr long long kTicketMergeMaxBlocks = 160;
 
 // Work split for one call. Without a workspace every CTA takes one whole unit
 // (grid = units). With one, a persistent grid of one CTA per SM runs whole-unit
@@ -1054,6 +1233,8 @@ Schedule plan(int B, int Sq, int Sk, int H, int sms, bool split)
     else
         s.dp_waves = std::max(0, waves - 1);
     s.tail_iters = static_cast<long long>(s.n_units - s.dp_waves * s.grid) * s.n_kblocks;
+    const long long per_cta = static_cast<long long>(s.dp_waves) * s.n_kblocks + (s.tail_iters + s.grid - 1) / s.grid;
+    s.ticket_merge = per_cta <= kTicketMergeMaxBlocks;
     return s;
 }
 
@@ -1080,7 +1261,7 @@ long long ws_prefix_bytes(int n_docs)
 
 long long ws_counter_bytes(const Schedule &s)
 {
-    return (static_cast<long long>(s.n_units) * kTiles * 4 + 255) / 256 * 256;
+    return (static_cast<long long>(s.n_units) * kTiles * 2 * 4 + 255) / 256 * 256;
 }
 
 long long ws_ml_bytes(const Schedule &s)
@@ -1093,37 +1274,42 @@ long long ws_bytes(const Schedule &s, int D)
     return ws_counter_bytes(s) + ws_ml_bytes(s) + 2LL * s.grid * (D / 4) * kTiles * kBM * 16;
 }
 
-template <int D, bool BF16>
-cudaError_t launch_typed(const AttnArgs &a, cudaStream_t stream)
+// Once per device and kernel instantiation: refuse a build whose register
+// count differs from kRegsLaunch (the warpgroups' register budgets add up to
+// the launch's total only then; a larger split would never be granted), and
+// raise the kernel's dynamic shared memory limit.
+template <int D, bool BF16, bool TM>
+cudaError_t prepare_kernel()
 {
-    using L = Layout<D>;
     static bool attr_set[64] = {false};
     static std::mutex mu;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess)
         return err;
-    {
-        std::lock_guard<std::mutex> g(mu);
-        if (dev >= 64 || !attr_set[dev]) {
-            // The warpgroups' register budgets add up to the launch's total only
-            // if the compiled kernel uses exactly kRegsLaunch registers per
-            // thread; a larger split would never be granted, so refuse to launch
-            // any other build.
-            cudaFuncAttributes fa{};
-            err = cudaFuncGetAttributes(&fa, attn_fwd_kernel<D, BF16>);
-            if (err != cudaSuccess)
-                return err;
-            if (fa.numRegs != kRegsLaunch || fa.maxThreadsPerBlock < kThreads)
-                return cudaErrorInvalidDeviceFunction;
-            err = cudaFuncSetAttribute(attn_fwd_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       L::kAlloc);
-            if (err != cudaSuccess)
-                return err;
-            if (dev < 64)
-                attr_set[dev] = true;
-        }
-    }
+    std::lock_guard<std::mutex> g(mu);
+    if (dev < 64 && attr_set[dev])
+        return cudaSuccess;
+    cudaFuncAttributes fa{};
+    err = cudaFuncGetAttributes(&fa, attn_fwd_kernel<D, BF16, TM>);
+    if (err != cudaSuccess)
+        return err;
+    if (fa.numRegs != kRegsLaunch || fa.maxThreadsPerBlock < kThreads)
+        return cudaErrorInvalidDeviceFunction;
+    err = cudaFuncSetAttribute(attn_fwd_kernel<D, BF16, TM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               Layout<D>::kAlloc);
+    if (err != cudaSuccess)
+        return err;
+    if (dev < 64)
+        attr_set[dev] = true;
+    return cudaSuccess;
+}
+
+template <int D, bool BF16>
+cudaError_t launch_typed(const AttnArgs &a, cudaStream_t stream)
+{
+    using L = Layout<D>;
+    cudaError_t err = cudaSuccess;
     const int sms = sm_count(&err);
     if (err != cudaSuccess)
         return err;
@@ -1181,7 +1367,16 @@ cudaError_t launch_typed(const AttnArgs &a, cudaStream_t stream)
             return err;
         p.var_prefix = prefix;
     }
-    attn_fwd_kernel<D, BF16><<<static_cast<unsigned>(sc.grid), kThreads, L::kAlloc, stream>>>(mq, mk, mv, p);
+    if (sc.ticket_merge) {
+        if ((err = prepare_kernel<D, BF16, true>()) != cudaSuccess)
+            return err;
+        attn_fwd_kernel<D, BF16, true><<<static_cast<unsigned>(sc.grid), kThreads, L::kAlloc, stream>>>(mq, mk, mv, p);
+    } else {
+        if ((err = prepare_kernel<D, BF16, false>()) != cudaSuccess)
+            return err;
+        attn_fwd_kernel<D, BF16, false><<<static_cast<unsigned>(sc.grid), kThreads, L::kAlloc, stream>>>(mq, mk, mv,
+                                                                                                          p);
+    }
     return cudaGetLastError();
 }
 
@@ -1203,7 +1398,7 @@ long long attention_units(int B, int Sq, int H)
 
 long long attention_counter_bytes(int B, int Sq, int H)
 {
-    return (attention_units(B, Sq, H) * kTiles * 4 + 255) / 256 * 256;
+    return (attention_units(B, Sq, H) * kTiles * 2 * 4 + 255) / 256 * 256;
 }
 
 long long attention_workspace_size(int B, int Sq, int Sk, int H, int D, cudaError_t *err)

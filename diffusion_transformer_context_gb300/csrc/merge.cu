@@ -4,7 +4,10 @@
 //   lse = ln sum_p exp(lse_p),   out = sum_p exp(lse_p - lse) * o_p.
 // HBM bound: a lane owns one 16-byte chunk (8 elements) of an output row,
 // accumulates the P matching chunks in fp32 with weights from the row's P
-// segment LSEs, and writes one rounded chunk.
+// segment LSEs, and writes one rounded chunk. The weights take one
+// exponential per segment: with m = max_p lse_p, e_p = exp(lse_p - m),
+// l = sum_p e_p, the weight is e_p / l and lse = m + ln l (exp and log by
+// the special-function unit's base-2 instructions).
 #include <algorithm>
 #include <cmath>
 #include <cuda_fp16.h>
@@ -15,6 +18,9 @@
 
 namespace ctx {
 namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.693147180559945309f;
 
 template <bool BF16>
 __device__ __forceinline__ void widen8(const uint4 &v, float *f)
@@ -90,16 +96,18 @@ __global__ void __launch_bounds__(256, merge_min_blocks(PT)) lse_merge_kernel(co
             float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             float total = -INFINITY;
             if (m != -INFINITY) {
-                float l = 0.f;
-#pragma unroll
-                for (int p = 0; p < PT; ++p)
-                    l += (lv[u][p] == -INFINITY) ? 0.f : expf(lv[u][p] - m);
-                total = m + logf(l);
+                // e_p = 2^((lse_p - m) log2 e): 0 for an empty segment (lse_p = -inf), 1 for the largest
+                float e[PT], l = 0.f;
 #pragma unroll
                 for (int p = 0; p < PT; ++p) {
-                    if (lv[u][p] == -INFINITY)
-                        continue;
-                    const float w = expf(lv[u][p] - total);
+                    e[p] = ptx::ex2_approx((lv[u][p] - m) * kLog2e);
+                    l += e[p];
+                }
+                const float inv = __frcp_rn(l);  // l >= 1
+                total = m + kLn2 * ptx::lg2_approx(l);
+#pragma unroll
+                for (int p = 0; p < PT; ++p) {
+                    const float w = e[p] * inv;
                     float f[8];
                     widen8<BF16>(ov[u][p], f);
 #pragma unroll
@@ -117,7 +125,7 @@ __global__ void __launch_bounds__(256, merge_min_blocks(PT)) lse_merge_kernel(co
     }
 }
 
-// Any D that is a multiple of 8: one thread per 16-byte chunk.
+// Any D that is a multiple of 8: one thread per 16-byte chunk (same weights).
 template <bool BF16>
 __global__ void __launch_bounds__(256) lse_merge_generic(const uint4 *__restrict__ o_parts,
                                                          const float *__restrict__ lse_parts, int P, uint4 *out,
@@ -139,17 +147,15 @@ __global__ void __launch_bounds__(256) lse_merge_generic(const uint4 *__restrict
         float total = -INFINITY;
         if (m != -INFINITY) {
             float l = 0.f;
-            for (int p = 0; p < P; ++p) {
-                const float lp = __ldg(lse_parts + p * rows + lrow);
-                if (lp != -INFINITY)
-                    l += expf(lp - m);
-            }
-            total = m + logf(l);
+            for (int p = 0; p < P; ++p)
+                l += ptx::ex2_approx((__ldg(lse_parts + p * rows + lrow) - m) * kLog2e);
+            const float inv = __frcp_rn(l);
+            total = m + kLn2 * ptx::lg2_approx(l);
             for (int p = 0; p < P; ++p) {
                 const float lp = __ldg(lse_parts + p * rows + lrow);
                 if (lp == -INFINITY)
                     continue;
-                const float w = expf(lp - total);
+                const float w = ptx::ex2_approx((lp - m) * kLog2e) * inv;
                 float f[8];
                 widen8<BF16>(__ldg(o_parts + (p * rows + r) * dv + c), f);
 #pragma unroll

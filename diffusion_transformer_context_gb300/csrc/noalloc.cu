@@ -27,8 +27,8 @@
 
 namespace {
 
-// 44 MiB: the partial-result slots of a 160-SM grid at D = 128 (41.6 MB)
-// plus arrival counters for up to 131072 work units.
+// 44 MiB: the partial-result slots of a 160-SM grid at D = 128 (42.6 MB)
+// plus the arrived / written counters of up to 131072 work units (2 MiB).
 constexpr long long kScratchBytes = 44LL << 20;
 
 static __device__ __align__(256) unsigned char g_attn_scratch[kScratchBytes];

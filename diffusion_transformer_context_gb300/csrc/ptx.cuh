@@ -306,6 +306,14 @@ __device__ __forceinline__ float ex2_approx(float x)
     return y;
 }
 
+// log2 by the special-function unit (lg2.approx.ftz.f32).
+__device__ __forceinline__ float lg2_approx(float x)
+{
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ float max3(float a, float b, float c)
 {
     float d;

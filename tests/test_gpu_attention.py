@@ -47,7 +47,7 @@ def _run(ctx, q, k, v, mask=None, scale=None, guard=False, split=False):
     if split:
         # the arrival counters at the head of the workspace are zero again
         n_units = ((Sq + 255) // 256) * H * B
-        assert int(ws[:n_units * 2 * 4].count_nonzero()) == 0
+        assert int(ws[:n_units * 2 * 2 * 4].count_nonzero()) == 0  # arrived / written per tile
     return o_t.float().cpu().numpy(), l_t.cpu().numpy()
 
 

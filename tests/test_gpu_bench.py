@@ -41,8 +41,8 @@ def test_attention_workload_line():
     assert p["frac"] == pytest.approx(p["achieved"] / p["peak"], abs=1e-4)
     # the packs and the unpacks each read and write the 75.5 MB of all ranks' Q/K/V once
     assert p["algorithmic_bytes"] == {"pack": 2 * 3 * 4 * 1024 * 24 * 128 * 2, "unpack": 2 * 3 * 4 * 1024 * 24 * 128 * 2}
-    assert p["gpu_launches_per_replay"] == {"pack": 4, "unpack": 4}
-    assert p["pack_gbs"] > 0 and p["unpack_gbs"] > 0 and p["step_gbs"] > 0
+    assert p["gpu_launches_per_set"] == {"pack": 4, "unpack": 4}
+    assert p["pack_gbs"] > 0 and p["unpack_gbs"] > 0 and p["step_gbs"] > 0 and p["copy_gbs"] > 0
 
 
 @pytest.mark.gpu

@@ -168,7 +168,7 @@ def _varlen_pair(ctx, q, k, v, cu_q, cu_k, max_q, mask=None):
         assert o2.intact() and l2.intact()
         outs.append((o2.t, l2.t))
     n_units = ((max_q + 255) // 256) * H * (len(cu_q) - 1)
-    assert int(ws[:n_units * 2 * 4].count_nonzero()) == 0
+    assert int(ws[:n_units * 2 * 2 * 4].count_nonzero()) == 0  # arrived / written per tile
     return (o1, l1), outs
 
 
