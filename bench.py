@@ -874,6 +874,65 @@ def run_varlen_bench(args):
     print(json.dumps(line), flush=True)
 
 
+def run_per_rank(args, rank, world, local_rank):
+    """--per-rank: one process per rank of the workload's U x A job (launched
+    by torchrun with U*A processes, one GPU each): the library's kernels for
+    every data step and NCCL all_to_all_single / all_gather between them
+    (diffusion_transformer_context_gb300.ranks). Timed like the default line:
+    W warm-up steps, K steps between barriers, the slowest rank's time;
+    `value` = the attention FLOPs of all ranks / that time."""
+    import torch
+    import torch.distributed as dist
+
+    import workloads
+    from diffusion_transformer_context_gb300.ranks import Groups, RankLayer
+
+    wl = workloads.WORKLOADS[args.workload]
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist.init_process_group("nccl", device_id=dev)
+    try:
+        G = Groups(wl.U, wl.A)
+        inp = workloads.make_inputs(wl)
+        layer = RankLayer(wl, G, dev)
+        layer.load(*(inp.shard(t, rank).to(dev) for t in (inp.q, inp.k, inp.v)),
+                   None if inp.jk is None else inp.jk.to(dev), None if inp.jv is None else inp.jv.to(dev),
+                   inp.image_mask, inp.joint_mask)
+        for _ in range(args.warmup):
+            layer.step()
+        dist.barrier()
+        torch.cuda.synchronize(dev)
+        sampler = ClockSampler(local_rank) if (rank == 0 and not args.no_clocks) else None
+        if sampler:
+            sampler.start()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            layer.step()
+        e1.record()
+        dist.barrier()
+        torch.cuda.synchronize(dev)
+        clocks = sampler.stop() if sampler else None
+        ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+        flops = layer.attn_flops(valid_keys(inp))
+        total = torch.tensor([flops], dtype=torch.float64, device=dev)
+        dist.all_reduce(total)
+        U, S_l = wl.U, layer.S_l
+        # this library's launches per rank and step (NCCL's own kernels not counted)
+        launches = (4 if U > 1 else 2) + (1 if layer.mask is not None else 0)
+        line = {"metric": METRIC, "value": round(float(total.item()) / (ms / args.steps * 1e-3) / 1e12, 3),
+                "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True, "scaling": "strong",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {**shape_config(wl), "parallelism": f"ulysses{wl.U} x agkv{wl.A}, one rank per GPU (NCCL)",
+                           "per_rank": [wl.B, S_l, wl.H, wl.D], "l2": "inputs_larger_than_l2"},
+                "gpu_launches": launches * args.steps, "clocks": clocks, "e2e": None}
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+    finally:
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -885,6 +944,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-pack", action="store_true", help="skip the layout-only pack workload line")
+    ap.add_argument("--per-rank", action="store_true",
+                    help="one process per rank of the workload's U x A job (torchrun with U*A GPUs), NCCL between")
     ap.add_argument("--unbalanced", action="store_true", help="attention without workspace: one CTA per unit")
     ap.add_argument("--eager", action="store_true", help="launch every kernel from Python instead of CUDA graphs")
     ap.add_argument("--kernel", default=None, choices=["lse_merge", "varlen", "attn"], help="time one kernel alone")
@@ -915,6 +976,9 @@ def main():
     if args.kernel == "attn":
         if rank == 0:
             run_attn_bench(args)
+        return
+    if args.per_rank:
+        run_per_rank(args, rank, world, local_rank)
         return
 
     import torch
