@@ -12,12 +12,11 @@
 // that every GPU loading the library holds until the process exits.
 //
 // Nothing is allocated on any call: the array exists once the module is
-// loaded. Its device address is looked up again on every call made outside a
+// loaded. Its device address is looked up again by every call made outside a
 // stream capture (a device reset reloads the module, possibly at another
-// address); during a capture the address found by the last uncaptured call on
-// that device is used, so make one call on each device before capturing. All
-// calls share the array and it keeps the last call's contents; the part that
-// must start at zero (the arrival counters) is cleared after every call.
+// address); make the first call on each device before any stream capture.
+// All calls share the array and it keeps the last call's contents; the part
+// that must start at zero (the arrival counters) is cleared after every call.
 // Calls that can overlap on the GPU (different streams, or different host
 // threads) race on the array: serialise them.
 #include <cstdint>

@@ -296,12 +296,10 @@ long long ctx_attn_lq_gkv_workspace_size(int B, int Sq, int Sk, int H, int D);
  * Same arguments, layouts and results as ctx_attn_lq_gkv, without the
  * workspace: the library keeps a fixed 44 MiB scratch array in device memory
  * (held by every GPU that loads the library until the process exits) and
- * allocates nothing on any call. Every call made outside a stream capture
- * looks up the array's device address on the current device (so a device
- * reset, which can move it, is followed); a call made while `stream` is
- * capturing reuses the address of the last uncaptured call on that device, so
- * make one call on each device before any stream capture (otherwise
- * CTX_ERR_CUDA, cudaErrorStreamCaptureUnsupported). Calls share the array:
+ * allocates nothing on any call. The array's device address is looked up on
+ * the current device by the calls made outside a stream capture (a device
+ * reset can move it); make the first call on each device before any stream
+ * capture. Calls share the array:
  * calls that can overlap on the GPU race and must be serialised by the
  * caller. The arrival counters are cleared after every call. Returns
  * CTX_ERR_INVALID_ARG for sizes ctx_attn_lq_gkv rejects, CTX_ERR_UNSUPPORTED

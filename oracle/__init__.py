@@ -18,9 +18,30 @@ two things that are plain data movement written from the pages:
 
 ``py_*`` functions are pure-Python loop twins for tiny shapes.
 
-Every function is pinned by ``tests/test_oracle_pack.py`` and
-``tests/test_oracle_attention.py`` against the pages' own test construction,
-closed forms, invariants or a library routine for the same quantity.
+Every function is pinned by a CPU test against the pages' own test
+construction, closed forms, invariants, numpy slicing of the global tensors
+or a library routine for the same quantity (none against a retyped copy of
+itself):
+
+  pack_qkv, unpack_qkv, all_to_all  tests/test_oracle_pack.py (the sglang test's
+                       construction and shapes against its head-slice spec;
+                       packed == three separate exchanges)
+  pack_out, unpack_out tests/test_oracle_pack.py (round trips, head concat)
+  all_gather, ulysses_agkv_forward  tests/test_oracle_pack.py (the composed
+                       order rebuilds the sequence, the reverse order does not),
+                       tests/test_oracle_composed.py (padded heads + joint keys,
+                       both placements, interleaved layout, against numpy slicing)
+  ulysses_reverse      tests/test_oracle_composed.py (A > 1 and uneven heads
+                       against the input shards; a planted u-major reverse fails)
+  pack_qkv_ex, unpack_qkv_ex, unpack_out_ex  tests/test_oracle_uaa.py
+  merge_joint_attn_mask  tests/test_oracle_mask.py (the page's case list)
+  attention_rows, attention, attention_probs, py_attention_row
+                       tests/test_oracle_attention.py (closed forms, invariants,
+                       scipy logsumexp / softmax)
+  lse_merge            tests/test_oracle_merge.py (segments == full attention)
+  varlen_remap, padding_remap, attention_varlen  tests/test_oracle_varlen.py
+                       (the page's worked example; documents are independent)
+  py_pack_qkv          tests/test_oracle_pack.py (equals pack_qkv)
 """
 from __future__ import annotations
 

@@ -59,7 +59,11 @@ def test_masked_workload_line():
 def test_layout_workload_line():
     d = run_bench("--workload", "pack", "--steps", "3", "--warmup", "3", "--no-cpu-baseline", "--no-clocks")
     assert d["unit"] == "GB/s" and d["value"] > 0
-    assert d["roofline"]["bound"] == "hbm"
+    r = d["roofline"]
+    assert r["bound"] == "hbm" and r["workload"] == "pack" and d["value"] == r["achieved"]
+    assert r["frac"] == pytest.approx(r["achieved"] / r["peak"], abs=1e-4)
+    assert "write-back inside the timed region" in r["timing"]
+    assert d["step"]["bound"] == "hbm"   # the in-step figure, kept beside it
     assert d["config"]["l2"] == "flushed_between_steps"
     assert d["e2e"]["readback_verified"] is True
     assert d["e2e"]["unit"] == "GB/s"

@@ -112,6 +112,11 @@ WORKLOADS = {
     # Ulysses-2 x AllGather-2 divides evenly
     "uaa14_usp4": Workload("uaa14_usp4", B=1, S=65536, H=14, D=128, U=4, A=1),
     "uaa14_cp2usp2": Workload("uaa14_cp2usp2", B=1, S=65536, H=14, D=128, U=2, A=2),
+    # the same comparison at the page's other sequence lengths (16384, 32768)
+    "uaa14_usp4_s16k": Workload("uaa14_usp4_s16k", B=1, S=16384, H=14, D=128, U=4, A=1),
+    "uaa14_cp2usp2_s16k": Workload("uaa14_cp2usp2_s16k", B=1, S=16384, H=14, D=128, U=2, A=2),
+    "uaa14_usp4_s32k": Workload("uaa14_usp4_s32k", B=1, S=32768, H=14, D=128, U=4, A=1),
+    "uaa14_cp2usp2_s32k": Workload("uaa14_cp2usp2_s32k", B=1, S=32768, H=14, D=128, U=2, A=2),
 }
 
 
