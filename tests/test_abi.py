@@ -205,3 +205,22 @@ def test_mask_merge_validation(lib):
     assert f(None, 0, None, None, 0, None, B, S, J, 0, None, None) == INVALID                  # no output
     assert f(None, 0, None, None, 0, None, 0, S, J, 0, out, None) == INVALID                   # B = 0
     assert f(im, 2, dims(B, S), None, 0, None, B, S, J, 0, im + 50, None) == ALIASING           # out over image
+
+
+def test_binding_refuses_views_that_overrun_their_storage(lib):
+    """The library sees only a pointer, so the binding checks that the rows a
+    strided output addresses lie inside the tensor's storage, before the call
+    (here on host tensors: the refusal comes first)."""
+    import torch
+
+    import diffusion_transformer_context_gb300 as ctx
+    U, B, S_l, h_l, D = 2, 1, 4, 2, 8
+    recv = torch.zeros((U, 3, B, S_l, h_l, D), dtype=torch.bfloat16)
+    big = torch.zeros((1, 16, h_l, D), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        # 8 rows from row 10 of a 16-row buffer
+        ctx.ctx_unpack_qkv_ex(recv, big[:, 10:], big[:, :8], big[:, :8], U, B, S_l, h_l, D)
+    o = torch.zeros((1, 6, h_l, D), dtype=torch.bfloat16)
+    send = torch.zeros((U, B, S_l, h_l, D), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        ctx.ctx_pack_out(o, send, U)  # U*S_l = 8 rows of a 6-row output
