@@ -341,7 +341,7 @@ def run_pack_line(args, dev, peaks, peak_kind):
             "gpu_launches_per_set": {"pack": wl.ranks, "unpack": wl.ranks},
             "step_gbs": rate(b_step, ms_step), "step_ms": round(ms_step, 4),
             "step_note": "pack + simulated all-to-all + unpack; staging buffers re-read from L2",
-            "traffic": recorded_traffic("pack", "relayout")}
+            "traffic": recorded_traffic("pack_kernels", "relayout")}
 
 
 def run_e2e(sim, inp, args, world, dev, run_phase, barrier):
@@ -1006,7 +1006,9 @@ def main():
                 "frac": round(relayout_gbs / peaks["hbm_gbs"], 4), "peak_source": f"{peak_kind} hbm_gbs",
                 "ms": round(relayout_ms, 4), "algorithmic_bytes": relayout_bytes,
                 "reverse_ms": round(reverse_ms, 4), "reverse_bytes": sim.reverse_bytes(),
-                "traffic": recorded_traffic(args.workload, "relayout")}
+                "traffic": recorded_traffic(args.workload, "relayout"),
+                "note": "inside the step: written rows drain from L2 during the next kernel, so an upper bound; "
+                        "the `pack` object times the layout kernels with reads from HBM and timed write-backs"}
     config = {**shape_config(sim.wl),
               "l2": "flushed_between_steps" if sim.l2_flushed else "inputs_larger_than_l2",
               "parallelism": f"replicas{world}",
