@@ -294,6 +294,26 @@ def test_wan14b_full_size_sampled(ctx, orc):
     assert n >= 512 + 40 * 256
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_masked_long_call_takes_the_write_then_count_merge(ctx, orc, dtype):
+    """A call whose CTAs run more than 160 key blocks (64 units of 512 key
+    blocks on 152 SMs: ~215 each) merges its split units with the
+    write-then-count protocol; here with a random key mask with masked
+    stretches, in both 16-bit types, against the oracle at full size."""
+    B, Sq, Sk, H, D = 1, 4096, 65536, 4, 128
+    gen = torch.Generator().manual_seed(41)
+    q, k, v = (workloads.randn(s, gen, dtype) for s in ((B, Sq, H, D), (B, Sk, H, D), (B, Sk, H, D)))
+    rng = np.random.default_rng(41)
+    mask = (rng.random((B, Sk)) > 0.2).astype(np.uint8)
+    mask[:, 10000:30000] = 0
+    O, L = _run(ctx, q, k, v, mask=mask, split=True)
+    bhi = full_size_rows(B, H, Sq, 512, seed=41)
+    eo, el = orc.attention_rows(u16(q), u16(k), u16(v), bhi, mask, dtype=dtype)
+    err = np.abs(O[bhi[:, 0], bhi[:, 2], bhi[:, 1]] - eo)
+    assert err.max() <= O_MAX and err.mean() <= O_MEAN, (err.max(), err.mean())
+    assert np.abs(L[bhi[:, 0], bhi[:, 1], bhi[:, 2]] - el).max() <= LSE_TOL
+
+
 @pytest.mark.parametrize("B,Sq,Sk,H", [(1, 4095, 32760, 12), (1, 300, 4096, 1), (2, 2000, 3000, 5),
                                        (1, 40000, 700, 16)])
 def test_balanced_schedule_matches_per_unit(ctx, B, Sq, Sk, H):
