@@ -407,9 +407,36 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint3
     }
 }
 
+// Log-sum-exp merge of the pieces of a split unit (log2 domain): fold_ml
+// takes the next piece's (m, l) into the running maximum M and sum lsum (a
+// piece without a valid key, m = -inf, adds nothing); piece_weight is a
+// piece's factor against the final M; add_piece accumulates a weighted
+// piece. The ticket-first merge goes through these on both of its paths.
+__device__ __forceinline__ void fold_ml(float &M, float &lsum, float2 ml)
+{
+    if (ml.x == -INFINITY)
+        return;
+    if (ml.x > M) {
+        lsum = (M == -INFINITY) ? ml.y : fmaf(lsum, ptx::ex2_approx(M - ml.x), ml.y);
+        M = ml.x;
+    } else {
+        lsum = fmaf(ptx::ex2_approx(ml.x - M), ml.y, lsum);
+    }
+}
+
+__device__ __forceinline__ float piece_weight(float2 ml, float M)
+{
+    return (ml.x == -INFINITY) ? 0.f : ptx::ex2_approx(ml.x - M);
+}
+
+__device__ __forceinline__ float add_piece(float acc, float w, float v)
+{
+    return fmaf(w, v, acc);
+}
+
 // kTicketMerge: the merge protocol of units cut between CTAs (see the partial
-// segment branch): a piece takes its arrival ticket as soon as its O is
-// complete and the last one merges the others with its own O from TMEM
+// segment branch): a piece takes its arrival ticket as its last key block
+// starts and the last one merges the others with its own O from TMEM
 // (true), or every piece writes its partial and the last to have written
 // merges them all from the workspace (false). The first shortens the end of
 // a short call; the second is kept for long calls, where the kernel built
@@ -633,10 +660,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (; ok; ++segi) {
             const unsigned char *mrow;
             int n, jb, k_len;
+            int tix = -1;    // ticket merge: the unit of a piece of a split unit, else -1
+            int ticket = 0;  // ticket merge: this piece's arrival ticket
             {
                 Segment sg;
                 if (!segment_at(p, cta, segi, sg))
                     break;
+                if constexpr (kTicketMerge)
+                    tix = sg.full ? -1 : sg.unit;
                 Geom ge;
                 unit_geom(p, sg.unit, ge);
                 // the key mask is indexed by the key's global position: batch row, then k0 + offset
@@ -679,6 +710,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 const bool all_valid = (vb[0] & vb[1] & vb[2] & vb[3]) == 0xffffffffu;
+                if constexpr (kTicketMerge) {
+                    // A piece of a split unit takes its arrival ticket as its last
+                    // key block starts: the atomic's round trip overlaps the block,
+                    // and the pieces still arrive in about the order they finish.
+                    if (i == n - 1 && tix >= 0 && tile_leader)
+                        ticket = atomicAdd(p.counters + (static_cast<size_t>(tix) * kTiles + t) * 2, 1);
+                }
 
                 if (!(ok = wait_bar_warp(s_full + t, (g + i) & 1, abort_flag, p)))
                     break;
@@ -874,7 +912,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     p.lse[(static_cast<size_t>(b) * p.H + h) * p.Sq + qrow] = lse_val;
             } else if constexpr (kTicketMerge) {
                 // Partial segment (the unit is cut between CTAs). The tile's leader
-                // takes an arrival ticket as soon as O is complete. Every piece but
+                // took an arrival ticket as the last key block started. Every piece but
                 // the last to arrive writes its unnormalised O and (m, l) to this
                 // CTA's slot and then counts itself written; the last piece waits
                 // for the others' writes and merges them by log-sum-exp with its
@@ -885,7 +923,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int *const arrive = p.counters + (static_cast<size_t>(sg.unit) * kTiles + t) * 2;
                 int *const written = arrive + 1;
                 if (tile_leader) {
-                    merge_flag[t] = (atomicAdd(arrive, 1) == c_hi - c_lo);
+                    merge_flag[t] = (ticket == c_hi - c_lo);
                     ptx::mbar_arrive(merge_go + t);
                 }
                 if (!(ok = wait_bar_warp(merge_go + t, ph & 1, abort_flag, p)))
@@ -941,79 +979,124 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     ph ^= 4;
                     // Every piece in the unit's order (this one's values from registers
-                    // and TMEM, the others' from their slots): the same arithmetic
+                    // and TMEM, the others' from their slots), folded and weighted by
+                    // the same two functions on either path: the same arithmetic
                     // whichever piece arrives last, so results are reproducible.
-                    // Running maximum and sum of the pieces' (m, l) in one pass:
                     float M = -INFINITY, lsum = 0.f;
-#pragma unroll 4
-                    for (int cc = c_lo; cc <= c_hi; ++cc) {
-                        const float2 ml =
-                            cc == cta ? make_float2(m_run, l_run)
-                                      : __ldcg(p.part_ml + static_cast<size_t>(tail_slot(p, total, first, cc)) *
-                                                               (kTiles * kBM) + prow);
-                        if (ml.x == -INFINITY)
-                            continue;
-                        if (ml.x > M) {
-                            lsum = (M == -INFINITY ? 0.f : lsum * ptx::ex2_approx(M - ml.x)) + ml.y;
-                            M = ml.x;
-                        } else {
-                            lsum += ptx::ex2_approx(ml.x - M) * ml.y;
-                        }
-                    }
-                    const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
                     // rows leave through the warp's staging area as whole 128-byte lines
                     const unsigned long long orow =
                         qrow < q_end ? reinterpret_cast<unsigned long long>(out_row<D>(p, b, h, qrow)) : 0ull;
                     uint4 *const stg = reinterpret_cast<uint4 *>(
                         reinterpret_cast<uint8_t *>(bars) + (L::kEpiOff - L::kBarOff) + (warp - 4) * L::kEpiWarpBytes);
-#pragma unroll 1
-                    for (int hf = 0; hf < D / 64; ++hf) {
-                        // 64 columns at a time: a slot's 16 float4 in flight together
-                        // (one L2 round trip per piece), this piece's from TMEM
-                        float o[64];
+                    const float2 mine = make_float2(m_run, l_run);
+                    if (c_hi - c_lo == 1) {
+                        // Two pieces (the usual cut): the other piece's (m, l) and its
+                        // first 64 columns are fetched together, and each next 64
+                        // columns while the current ones are stored; this piece's O is
+                        // combined as it leaves TMEM.
+                        const bool own_lo = cta == c_lo;
+                        const int sl = tail_slot(p, total, first, own_lo ? c_hi : c_lo);
+                        const float2 mo = __ldcg(p.part_ml + static_cast<size_t>(sl) * (kTiles * kBM) + prow);
+                        const float4 *src = p.part_o + static_cast<size_t>(sl) * (D / 4) * (kTiles * kBM) + prow;
+                        float4 vo[16];
 #pragma unroll
-                        for (int k = 0; k < 64; ++k)
-                            o[k] = 0.f;
-                        for (int cc = c_lo; cc <= c_hi; ++cc) {
-                            float2 ml;
-                            float4 v[16];
-                            if (cc == cta) {
-                                ml = make_float2(m_run, l_run);
-                                uint32_t r[64];
-                                ptx::tmem_ld32(tO + hf * 64, r);
-                                ptx::tmem_ld32(tO + hf * 64 + 32, r + 32);
+                        for (int k = 0; k < 16; ++k)
+                            vo[k] = __ldcg(src + static_cast<size_t>(k) * (kTiles * kBM));
+                        fold_ml(M, lsum, own_lo ? mine : mo);
+                        fold_ml(M, lsum, own_lo ? mo : mine);
+                        const float w_own = piece_weight(mine, M), w_oth = piece_weight(mo, M);
+                        const float w_lo = own_lo ? w_own : w_oth, w_hi = own_lo ? w_oth : w_own;
+                        const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
+#pragma unroll
+                        for (int hf = 0; hf < D / 64; ++hf) {
+#pragma unroll
+                            for (int qq = 0; qq < 2; ++qq) {
+                                uint32_t r[32];
+                                ptx::tmem_ld32(tO + hf * 64 + qq * 32, r);
                                 ptx::tmem_ld_wait();
                                 ptx::reg_fence32(r);
-                                ptx::reg_fence32(r + 32);
-                                if (hf == D / 64 - 1) {
+                                if (hf == D / 64 - 1 && qq == 1) {
                                     ptx::tc_fence_before();
                                     ptx::mbar_arrive(o_empty + t);  // O is in registers: the next PV may start
                                 }
+                                float of[32];
+#pragma unroll
+                                for (int k = 0; k < 8; ++k) {
+                                    const float4 x = vo[qq * 8 + k];
+                                    const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                                    for (int j = 0; j < 4; ++j) {
+                                        const float a = __uint_as_float(r[4 * k + j]);
+                                        of[4 * k + j] = add_piece(add_piece(0.f, w_lo, own_lo ? a : xs[j]), w_hi,
+                                                                  own_lo ? xs[j] : a);
+                                    }
+                                }
+                                stage32<BF16>(stg, lane, qq, of, inv);
+                            }
+                            if (hf + 1 < D / 64) {
 #pragma unroll
                                 for (int k = 0; k < 16; ++k)
-                                    v[k] = make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
-                                                       __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
-                            } else {
-                                const int sl = tail_slot(p, total, first, cc);
-                                ml = __ldcg(p.part_ml + static_cast<size_t>(sl) * (kTiles * kBM) + prow);
-                                const float4 *src =
-                                    p.part_o + (static_cast<size_t>(sl) * (D / 4) + hf * 16) * (kTiles * kBM) + prow;
-#pragma unroll
-                                for (int k = 0; k < 16; ++k)
-                                    v[k] = __ldcg(src + static_cast<size_t>(k) * (kTiles * kBM));
+                                    vo[k] = __ldcg(src + static_cast<size_t>((hf + 1) * 16 + k) * (kTiles * kBM));
                             }
-                            const float w = (ml.x == -INFINITY) ? 0.f : ptx::ex2_approx(ml.x - M);
-#pragma unroll
-                            for (int k = 0; k < 16; ++k) {
-                                o[4 * k] += w * v[k].x;
-                                o[4 * k + 1] += w * v[k].y;
-                                o[4 * k + 2] += w * v[k].z;
-                                o[4 * k + 3] += w * v[k].w;
-                            }
+                            store_staged(stg, lane, orow, hf * 8);
                         }
-                        stage32<BF16>(stg, lane, 0, o, inv);
-                        stage32<BF16>(stg, lane, 1, o + 32, inv);
-                        store_staged(stg, lane, orow, hf * 8);
+                    } else {
+#pragma unroll 4
+                        for (int cc = c_lo; cc <= c_hi; ++cc)
+                            fold_ml(M, lsum,
+                                    cc == cta ? mine
+                                              : __ldcg(p.part_ml + static_cast<size_t>(tail_slot(p, total, first, cc)) *
+                                                                       (kTiles * kBM) + prow));
+                        const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
+#pragma unroll 1
+                        for (int hf = 0; hf < D / 64; ++hf) {
+                            // 64 columns at a time: a slot's 16 float4 in flight together
+                            // (one L2 round trip per piece), this piece's from TMEM
+                            float o[64];
+#pragma unroll
+                            for (int k = 0; k < 64; ++k)
+                                o[k] = 0.f;
+                            for (int cc = c_lo; cc <= c_hi; ++cc) {
+                                float2 ml;
+                                float4 v[16];
+                                if (cc == cta) {
+                                    ml = mine;
+                                    uint32_t r[64];
+                                    ptx::tmem_ld32(tO + hf * 64, r);
+                                    ptx::tmem_ld32(tO + hf * 64 + 32, r + 32);
+                                    ptx::tmem_ld_wait();
+                                    ptx::reg_fence32(r);
+                                    ptx::reg_fence32(r + 32);
+                                    if (hf == D / 64 - 1) {
+                                        ptx::tc_fence_before();
+                                        ptx::mbar_arrive(o_empty + t);  // O is in registers: the next PV may start
+                                    }
+#pragma unroll
+                                    for (int k = 0; k < 16; ++k)
+                                        v[k] = make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
+                                                           __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
+                                } else {
+                                    const int sl = tail_slot(p, total, first, cc);
+                                    ml = __ldcg(p.part_ml + static_cast<size_t>(sl) * (kTiles * kBM) + prow);
+                                    const float4 *src =
+                                        p.part_o + (static_cast<size_t>(sl) * (D / 4) + hf * 16) * (kTiles * kBM) + prow;
+#pragma unroll
+                                    for (int k = 0; k < 16; ++k)
+                                        v[k] = __ldcg(src + static_cast<size_t>(k) * (kTiles * kBM));
+                                }
+                                const float w = piece_weight(ml, M);
+#pragma unroll
+                                for (int k = 0; k < 16; ++k) {
+                                    o[4 * k] = add_piece(o[4 * k], w, v[k].x);
+                                    o[4 * k + 1] = add_piece(o[4 * k + 1], w, v[k].y);
+                                    o[4 * k + 2] = add_piece(o[4 * k + 2], w, v[k].z);
+                                    o[4 * k + 3] = add_piece(o[4 * k + 3], w, v[k].w);
+                                }
+                            }
+                            stage32<BF16>(stg, lane, 0, o, inv);
+                            stage32<BF16>(stg, lane, 1, o + 32, inv);
+                            store_staged(stg, lane, orow, hf * 8);
+                        }
                     }
                     if (p.lse && qrow < q_end)
                         p.lse[(static_cast<size_t>(b) * p.H + h) * p.Sq + qrow] =

@@ -183,6 +183,28 @@ def test_one_unit_cut_over_every_sm(ctx, orc, masked):
     _check_full(orc, q, k, v, O, L, mask=mask)
 
 
+@pytest.mark.parametrize("shape", [(1, 2048, 4352, 12), (1, 300, 4096, 1)], ids=["two_three_pieces", "many_pieces"])
+def test_split_merge_reproducible(ctx, shape):
+    """A short call's split units are merged by whichever piece arrives last;
+    the result must not depend on which one that is. One Qwen-like rank (96
+    units of 34 key blocks over the SMs' even shares: units cut into two and
+    into three pieces) and one unit cut over every SM, each called repeatedly
+    on one workspace: outputs and LSE bit-identical every time."""
+    B, Sq, Sk, H = shape
+    gen = torch.Generator().manual_seed(23)
+    q, k, v = (workloads.randn(s, gen).cuda() for s in ((B, Sq, H, 128), (B, Sk, H, 128), (B, Sk, H, 128)))
+    ws = ctx.attn_workspace(B, Sq, Sk, H, 128)
+    o0, l0 = torch.empty_like(q), torch.empty((B, H, Sq), device="cuda")
+    ctx.ctx_attn_lq_gkv(q, k, v, o0, l0, workspace=ws)
+    for _ in range(6):
+        o, l = torch.empty_like(q), torch.empty((B, H, Sq), device="cuda")
+        ctx.ctx_attn_lq_gkv(q, k, v, o, l, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(o.view(torch.int16), o0.view(torch.int16))
+        assert torch.equal(l.view(torch.int32), l0.view(torch.int32))
+    assert ctx.ctx_device_status() == 0
+
+
 def test_deterministic(ctx):
     gen = torch.Generator().manual_seed(14)
     B, Sq, Sk, H, D = 1, 512, 2048, 4, 128
