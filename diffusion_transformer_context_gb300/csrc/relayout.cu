@@ -28,75 +28,78 @@ __device__ __forceinline__ uint4 ld_stream(const uint4 *p)
 // Source and destination of run `run` (in 16-byte vectors). rv = run length;
 // a row of H heads is U runs long (H*D/8 = U*rv). `valid` is the number of
 // vectors of the run that exist in the source (padded modes): the pack
-// zero-fills the rest, the padded reverse exchange skips it.
-template <RelayoutMode M>
-__device__ __forceinline__ void map_run(const RelayoutArgs &a, long long run, const uint4 *&src, uint4 *&dst,
+// zero-fills the rest, the padded reverse exchange skips it. I is the type
+// the run index is decomposed in: unsigned 32-bit whenever every run index
+// fits (a 64-bit division is a long software sequence and a run takes up to
+// five of them), else 64-bit; offsets are formed in 64-bit either way.
+template <RelayoutMode M, typename I>
+__device__ __forceinline__ void map_run(const RelayoutArgs &a, I run, const uint4 *&src, uint4 *&dst,
                                         long long &valid)
 {
     const long long rv = a.run_vec;
+    const I S_l = static_cast<I>(a.S_l), B = static_cast<I>(a.B), U = static_cast<I>(a.U);
     valid = rv;
     if constexpr (M == RelayoutMode::PackQKV) {
         // run = ((r*3 + t)*B + b)*S_l + s  (destination order)
-        long long s = run % a.S_l, x = run / a.S_l;
-        long long b = x % a.B;
-        x /= a.B;
-        long long t = x % 3, r = x / 3;
+        const I s = run % S_l, x = run / S_l;
+        const I b = x % B, y = x / B;
+        const I t = y % 3u, r = y / 3u;
         const uint4 *base = static_cast<const uint4 *>(t == 0 ? a.src0 : (t == 1 ? a.src1 : a.src2));
-        src = base + ((b * a.S_l + s) * a.U + r) * rv;
-        dst = static_cast<uint4 *>(a.dst0) + run * rv;
+        src = base + ((static_cast<long long>(b) * a.S_l + s) * a.U + r) * rv;
+        dst = static_cast<uint4 *>(a.dst0) + static_cast<long long>(run) * rv;
     } else if constexpr (M == RelayoutMode::PackQKVPad) {
         // as PackQKV over U*h_l padded heads; the source rows hold H_real heads
-        long long s = run % a.S_l, x = run / a.S_l;
-        long long b = x % a.B;
-        x /= a.B;
-        long long t = x % 3, r = x / 3;
+        const I s = run % S_l, x = run / S_l;
+        const I b = x % B, y = x / B;
+        const I t = y % 3u, r = y / 3u;
         const long long dv = rv / a.h_l;  // vectors per head
-        const long long heads = min(max(a.H_real - r * a.h_l, 0LL), a.h_l);
+        const long long heads = min(max(a.H_real - static_cast<long long>(r) * a.h_l, 0LL), a.h_l);
         valid = heads * dv;
         const uint4 *base = static_cast<const uint4 *>(t == 0 ? a.src0 : (t == 1 ? a.src1 : a.src2));
-        src = base + ((b * a.S_l + s) * a.H_real + r * a.h_l) * dv;
-        dst = static_cast<uint4 *>(a.dst0) + run * rv;
+        src = base + ((static_cast<long long>(b) * a.S_l + s) * a.H_real + static_cast<long long>(r) * a.h_l) * dv;
+        dst = static_cast<uint4 *>(a.dst0) + static_cast<long long>(run) * rv;
     } else if constexpr (M == RelayoutMode::UnpackQKV) {
         // run = ((r*3 + t)*B + b)*S_l + s  (source order)
-        long long s = run % a.S_l, x = run / a.S_l;
-        long long b = x % a.B;
-        x /= a.B;
-        long long t = x % 3, r = x / 3;
+        const I s = run % S_l, x = run / S_l;
+        const I b = x % B, y = x / B;
+        const I t = y % 3u, r = y / 3u;
         uint4 *base = static_cast<uint4 *>(t == 0 ? a.dst0 : (t == 1 ? a.dst1 : a.dst2));
         const long long stride = t == 0 ? a.q_batch_stride_rows : a.kv_batch_stride_rows;
-        src = static_cast<const uint4 *>(a.src0) + run * rv;
-        dst = base + (b * stride + r * a.S_l + s) * rv;
+        src = static_cast<const uint4 *>(a.src0) + static_cast<long long>(run) * rv;
+        dst = base + (static_cast<long long>(b) * stride + static_cast<long long>(r) * a.S_l + s) * rv;
     } else if constexpr (M == RelayoutMode::PackOut) {
         // run = (r*B + b)*S_l + s  (destination order)
-        long long s = run % a.S_l, x = run / a.S_l;
-        long long b = x % a.B, r = x / a.B;
-        src = static_cast<const uint4 *>(a.src0) + (b * a.q_batch_stride_rows + r * a.S_l + s) * rv;
-        dst = static_cast<uint4 *>(a.dst0) + run * rv;
+        const I s = run % S_l, x = run / S_l;
+        const I b = x % B, r = x / B;
+        src = static_cast<const uint4 *>(a.src0) +
+              (static_cast<long long>(b) * a.q_batch_stride_rows + static_cast<long long>(r) * a.S_l + s) * rv;
+        dst = static_cast<uint4 *>(a.dst0) + static_cast<long long>(run) * rv;
     } else if constexpr (M == RelayoutMode::UnpackOut) {
         // run = (r*B + b)*S_l + s  (source order)
-        long long s = run % a.S_l, x = run / a.S_l;
-        long long b = x % a.B, r = x / a.B;
-        src = static_cast<const uint4 *>(a.src0) + run * rv;
-        dst = static_cast<uint4 *>(a.dst0) + ((b * a.S_l + s) * a.U + r) * rv;
+        const I s = run % S_l, x = run / S_l;
+        const I b = x % B, r = x / B;
+        src = static_cast<const uint4 *>(a.src0) + static_cast<long long>(run) * rv;
+        dst = static_cast<uint4 *>(a.dst0) + ((static_cast<long long>(b) * a.S_l + s) * a.U + r) * rv;
     } else if constexpr (M == RelayoutMode::UnpackOutPad) {
         // as UnpackOut; destination rows hold H_real heads, pad heads are dropped
-        long long s = run % a.S_l, x = run / a.S_l;
-        long long b = x % a.B, r = x / a.B;
+        const I s = run % S_l, x = run / S_l;
+        const I b = x % B, r = x / B;
         const long long dv = rv / a.h_l;
-        const long long heads = min(max(a.H_real - r * a.h_l, 0LL), a.h_l);
+        const long long heads = min(max(a.H_real - static_cast<long long>(r) * a.h_l, 0LL), a.h_l);
         valid = heads * dv;
-        src = static_cast<const uint4 *>(a.src0) + run * rv;
-        dst = static_cast<uint4 *>(a.dst0) + ((b * a.S_l + s) * a.H_real + r * a.h_l) * dv;
+        src = static_cast<const uint4 *>(a.src0) + static_cast<long long>(run) * rv;
+        dst = static_cast<uint4 *>(a.dst0) +
+              ((static_cast<long long>(b) * a.S_l + s) * a.H_real + static_cast<long long>(r) * a.h_l) * dv;
     } else {
         // AllToAll: run = (g*U + r)*U + j (source order) -> recv[g][j][r]
-        long long j = run % a.U, x = run / a.U;
-        long long r = x % a.U, g = x / a.U;
-        src = static_cast<const uint4 *>(a.src0) + run * rv;
-        dst = static_cast<uint4 *>(a.dst0) + ((g * a.U + j) * a.U + r) * rv;
+        const I j = run % U, x = run / U;
+        const I r = x % U, g = x / U;
+        src = static_cast<const uint4 *>(a.src0) + static_cast<long long>(run) * rv;
+        dst = static_cast<uint4 *>(a.dst0) + ((static_cast<long long>(g) * a.U + j) * a.U + r) * rv;
     }
 }
 
-template <RelayoutMode M, int VPL>
+template <RelayoutMode M, int VPL, typename I>
 __global__ void __launch_bounds__(256) relayout_kernel(RelayoutArgs a, long long n_items, int n_segs)
 {
     constexpr long long kSegVec = 32LL * VPL;
@@ -105,16 +108,16 @@ __global__ void __launch_bounds__(256) relayout_kernel(RelayoutArgs a, long long
     const long long warp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const long long n_warps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
     for (long long item = warp; item < n_items; item += n_warps) {
-        long long run = item, seg = 0;
+        I run = static_cast<I>(item), seg = 0;
         if (n_segs > 1) {
-            run = item / n_segs;
-            seg = item - run * n_segs;
+            run = static_cast<I>(item) / static_cast<I>(n_segs);
+            seg = static_cast<I>(item) - run * static_cast<I>(n_segs);
         }
         const uint4 *src;
         uint4 *dst;
         long long valid;
-        map_run<M>(a, run, src, dst, valid);
-        const long long base = seg * kSegVec;
+        map_run<M, I>(a, run, src, dst, valid);
+        const long long base = static_cast<long long>(seg) * kSegVec;
         const long long lim = min(a.run_vec - base, kSegVec);
         const long long vlim = min(valid - base, kSegVec);
         uint4 buf[VPL];
@@ -170,7 +173,7 @@ __global__ void __launch_bounds__(256) relayout_inter_kernel(RelayoutArgs a, lon
     }
 }
 
-template <RelayoutMode M, int VPL>
+template <RelayoutMode M, int VPL, typename I>
 cudaError_t launch_vpl(const RelayoutArgs &a, cudaStream_t stream)
 {
     static int blocks_per_sm[64] = {0};
@@ -187,7 +190,7 @@ cudaError_t launch_vpl(const RelayoutArgs &a, cudaStream_t stream)
     {
         std::lock_guard<std::mutex> g(mu);
         if (dev < 64 && blocks_per_sm[dev] == 0) {
-            err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm[dev], relayout_kernel<M, VPL>, 256, 0);
+            err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm[dev], relayout_kernel<M, VPL, I>, 256, 0);
             if (err != cudaSuccess)
                 return err;
             if (blocks_per_sm[dev] < 1)
@@ -201,24 +204,35 @@ cudaError_t launch_vpl(const RelayoutArgs &a, cudaStream_t stream)
     const long long want = (n_items + 7) / 8;  // 8 warps per block
     const long long cap = static_cast<long long>(sms) * bps;
     const unsigned grid = static_cast<unsigned>(std::max(1LL, std::min(want, cap)));
-    relayout_kernel<M, VPL><<<grid, 256, 0, stream>>>(a, n_items, n_segs);
+    relayout_kernel<M, VPL, I><<<grid, 256, 0, stream>>>(a, n_items, n_segs);
     return cudaGetLastError();
+}
+
+template <RelayoutMode M, typename I>
+cudaError_t launch_mode_i(const RelayoutArgs &a, cudaStream_t stream)
+{
+    const long long vpl = std::min(8LL, (a.run_vec + 31) / 32);
+    switch (vpl) {
+    case 1: return launch_vpl<M, 1, I>(a, stream);
+    case 2: return launch_vpl<M, 2, I>(a, stream);
+    case 3: return launch_vpl<M, 3, I>(a, stream);
+    case 4: return launch_vpl<M, 4, I>(a, stream);
+    case 5: return launch_vpl<M, 5, I>(a, stream);
+    case 6: return launch_vpl<M, 6, I>(a, stream);
+    case 7: return launch_vpl<M, 7, I>(a, stream);
+    default: return launch_vpl<M, 8, I>(a, stream);
+    }
 }
 
 template <RelayoutMode M>
 cudaError_t launch_mode(const RelayoutArgs &a, cudaStream_t stream)
 {
-    const long long vpl = std::min(8LL, (a.run_vec + 31) / 32);
-    switch (vpl) {
-    case 1: return launch_vpl<M, 1>(a, stream);
-    case 2: return launch_vpl<M, 2>(a, stream);
-    case 3: return launch_vpl<M, 3>(a, stream);
-    case 4: return launch_vpl<M, 4>(a, stream);
-    case 5: return launch_vpl<M, 5>(a, stream);
-    case 6: return launch_vpl<M, 6>(a, stream);
-    case 7: return launch_vpl<M, 7>(a, stream);
-    default: return launch_vpl<M, 8>(a, stream);
-    }
+    // 32-bit decomposition when every item index (runs x segments, plus a
+    // pass's stride over the grid) and every shape factor fits
+    const long long n_segs = (a.run_vec + 255) / 256;  // upper bound over VPL
+    const long long lim = 0xffffffffLL / 2;
+    const bool i32 = a.n_runs * std::max(1LL, n_segs) <= lim && a.S_l <= lim && a.B <= lim && a.U <= lim;
+    return i32 ? launch_mode_i<M, uint32_t>(a, stream) : launch_mode_i<M, long long>(a, stream);
 }
 
 }  // namespace
