@@ -167,6 +167,29 @@ def test_running_maximum_jumps(ctx, orc, dtype, split):
     _check_full(orc, q, k, v, O, L, dtype=dtype)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("split", [False, True], ids=["per_unit", "balanced"])
+def test_running_maximum_jumps_late_in_block(ctx, orc, dtype, split):
+    """Jumps of the running maximum late in a key block (key 100 of block 5,
+    past the first 64 keys): about 17.3 log2 units on head 0 (the block sum
+    check fails and the block is redone with its exact maximum, O rescaled),
+    about 11.4 on head 1 (accepted), and on head 2 two jumps in a row, early
+    in block 5 and late in block 6, the second far above the first."""
+    gen = torch.Generator().manual_seed(24)
+    B, Sq, Sk, H, D = 1, 256, 1024, 3, 128
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
+    u = torch.where(torch.rand(D, generator=gen) < 0.5, -1.0, 1.0)
+    q = (u.view(1, 1, 1, D) + 0.05 * torch.randn((B, Sq, H, D), generator=gen)).to(tdt)
+    k = (0.1 * torch.randn((B, Sk, H, D), generator=gen))
+    v = torch.randn((B, Sk, H, D), generator=gen).to(tdt)
+    for h, j, s_nat in ((0, 5 * 128 + 100, 12.0), (1, 5 * 128 + 100, 8.0),
+                        (2, 5 * 128 + 20, 12.0), (2, 6 * 128 + 90, 20.0)):
+        k[0, j, h] = u * (s_nat / math.sqrt(D))  # natural-log score of the special key
+    k = k.to(tdt)
+    O, L = _run(ctx, q, k, v, split=split)
+    _check_full(orc, q, k, v, O, L, dtype=dtype)
+
+
 @pytest.mark.parametrize("masked", [False, True])
 def test_one_unit_cut_over_every_sm(ctx, orc, masked):
     """One work unit (256 query rows of one head) against 304 key blocks: the
