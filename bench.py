@@ -946,7 +946,7 @@ def main():
     ap.add_argument("--no-pack", action="store_true", help="skip the layout-only pack workload line")
     ap.add_argument("--per-rank", action="store_true",
                     help="one process per rank of the workload's U x A job (torchrun with U*A GPUs), NCCL between")
-    ap.add_argument("--unbalanced", action="store_true", help="attention without workspace: one CTA per unit")
+    ap.add_argument("--unbalanced", action="store_true", help="attention without a workspace (no unit split between CTAs)")
     ap.add_argument("--eager", action="store_true", help="launch every kernel from Python instead of CUDA graphs")
     ap.add_argument("--kernel", default=None, choices=["lse_merge", "varlen", "attn"], help="time one kernel alone")
     ap.add_argument("--attn-shape", default="1,4095,32760,12,128",

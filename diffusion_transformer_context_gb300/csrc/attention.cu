@@ -35,7 +35,10 @@
 //   * schedules: one CTA per work unit, or (given a workspace) a persistent
 //     grid of one CTA per SM that cuts units' key ranges between SMs and
 //     merges the pieces by log-sum-exp; for packed varlen documents the
-//     split iteration space is planned on the device (varlen.cu).
+//     split iteration space is planned on the device (varlen.cu). Without a
+//     workspace, where a last wave of 256-row units would leave SMs idle, a
+//     unit is one 128-row tile whose key range the two tile slots share out
+//     in halves (warp 2 then loads V), merged inside the CTA.
 // Every wait is bounded (%globaltimer); on expiry the kernel records a
 // timeout in the device status word, drains its own TMA loads and MMAs, frees
 // TMEM and returns.
@@ -53,7 +56,7 @@ namespace {
 constexpr int kBM = 128;      // query rows per tile (= TMEM lanes)
 constexpr int kBN = kAttnKeyBlock;  // keys per block (128)
 constexpr int kTiles = 2;     // query tiles per CTA
-constexpr int kStages = 2;    // depth of the K ring and of the V ring
+constexpr int kStages = 2;    // depth of the K ring (two-tile units) and of the V ring
 constexpr int kThreads = 384; // 12 warps: TMA, MMA, two idle, 4 + 4 softmax
 // Registers: the kernel is launched with kRegsLaunch per thread (the compiler's
 // figure for 384 threads, checked on the host before the first launch); the
@@ -94,20 +97,26 @@ struct Params {
     float4 *part_o;        // [2*grid][D/4][kTiles*kBM] unnormalised O of partial segments
 };
 
-template <int D>
+// kHalves: units of one 128-row tile whose key range the two tile slots share
+// out in halves (one Q tile in shared memory; the room of the other holds a
+// third K stage, since the two slots draw two K blocks per step).
+template <int D, bool kHalves = false>
 struct Layout {
     static constexpr int kPanels = D / 64;          // 64-element (128-byte) swizzle panels
     static constexpr int kQBytes = kBM * D * 2;     // one Q tile
     static constexpr int kKVBytes = kBN * D * 2;    // one K or V block
     static constexpr int kQPanel = kBM * 128;       // bytes of one panel of a Q tile
     static constexpr int kKVPanel = kBN * 128;
+    static constexpr int kQTiles = kHalves ? 1 : kTiles;
+    static constexpr int kKStages = kHalves ? 3 : kStages;
+    static constexpr int kVStages = kStages;
     static constexpr int kQOff = 0;
-    static constexpr int kKOff = kQOff + kTiles * kQBytes;
-    static constexpr int kVOff = kKOff + kStages * kKVBytes;
-    static constexpr int kBarOff = kVOff + kStages * kKVBytes;
-    // q_full, q_empty, k_full[S], k_empty[S], v_full[S], v_empty[S],
+    static constexpr int kKOff = kQOff + kQTiles * kQBytes;
+    static constexpr int kVOff = kKOff + kKStages * kKVBytes;
+    static constexpr int kBarOff = kVOff + kVStages * kKVBytes;
+    // q_full, q_empty, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS],
     // s_full[T], p_full[T], o_full[T], o_empty[T], seg_done[T], merge_go[T], written_go[T], mma_done
-    static constexpr int kNumBars = 2 + 4 * kStages + 7 * kTiles + 1;
+    static constexpr int kNumBars = 2 + 2 * kKStages + 2 * kVStages + 7 * kTiles + 1;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     // per softmax warp: its 32 rows x 64 output columns, staged so that the
     // output rows leave as whole 128-byte lines
@@ -127,8 +136,9 @@ struct Segment {
     int nb;
 };
 
-// Geometry of one work unit: 256 query rows [q0, min(q0 + 256, q_end)) of
-// head h and batch b, against keys [k0, k0 + k_len) in key blocks of 128.
+// Geometry of one work unit: kRows (256, or 128 in the halves mode) query
+// rows [q0, min(q0 + kRows, q_end)) of head h and batch b, against keys
+// [k0, k0 + k_len) in key blocks of 128.
 // Packed varlen: the unit's document d gives q0 = cu_q[d] + 256*qp,
 // q_end = cu_q[d+1], keys [cu_k[d], cu_k[d+1]) (vllm-omni PR #7641: local
 // query boundaries, global key boundaries). nblk = 0 means nothing to compute.
@@ -136,6 +146,7 @@ struct Geom {
     int b, h, q0, q_end, k0, k_len, nblk;
 };
 
+template <int kRows = kTiles * kBM>
 __device__ __forceinline__ void unit_geom(const Params &p, int unit, Geom &g)
 {
     const int qp = unit % p.n_qpairs, bh = unit / p.n_qpairs;
@@ -143,7 +154,7 @@ __device__ __forceinline__ void unit_geom(const Params &p, int unit, Geom &g)
     const int x = bh / p.H;
     if (!p.varlen) {
         g.b = x;
-        g.q0 = qp * (kTiles * kBM);
+        g.q0 = qp * kRows;
         g.q_end = p.Sq;
         g.k0 = 0;
         g.k_len = p.Sk;
@@ -441,22 +452,24 @@ __device__ __forceinline__ float add_piece(float acc, float w, float v)
 // merges them all from the workspace (false). The first shortens the end of
 // a short call; the second is kept for long calls, where the kernel built
 // without the ticket code runs its key-block loop faster.
-template <int D, bool BF16, bool kTicketMerge>
+template <int D, bool BF16, bool kTicketMerge, bool kHalves>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const Params p)
 {
-    using L = Layout<D>;
+    static_assert(!(kTicketMerge && kHalves), "halves units are never split between CTAs");
+    using L = Layout<D, kHalves>;
+    constexpr int kUnitRows = kHalves ? kBM : kTiles * kBM;  // query rows of a work unit
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
     uint64_t *q_full = bars;
     uint64_t *q_empty = q_full + 1;
     uint64_t *k_full = q_empty + 1;
-    uint64_t *k_empty = k_full + kStages;
-    uint64_t *v_full = k_empty + kStages;
-    uint64_t *v_empty = v_full + kStages;
-    uint64_t *s_full = v_empty + kStages;
+    uint64_t *k_empty = k_full + L::kKStages;
+    uint64_t *v_full = k_empty + L::kKStages;
+    uint64_t *v_empty = v_full + L::kVStages;
+    uint64_t *s_full = v_empty + L::kVStages;
     uint64_t *p_full = s_full + kTiles;
     uint64_t *o_full = p_full + kTiles;
     uint64_t *o_empty = o_full + kTiles;
@@ -474,9 +487,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         ptx::mbar_init(q_full, 1);
         ptx::mbar_init(q_empty, 1);
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < L::kKStages; ++s) {
             ptx::mbar_init(k_full + s, 1);
             ptx::mbar_init(k_empty + s, 1);
+        }
+        for (int s = 0; s < L::kVStages; ++s) {
             ptx::mbar_init(v_full + s, 1);
             ptx::mbar_init(v_empty + s, 1);
         }
@@ -512,51 +527,74 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tma_prefetch_desc(&tmV);
             Segment sg;
             int kv = 0, act = 0;  // act: segments with work so far (phase of the per-segment barriers)
-            int last_k[kStages], last_v[kStages];
-            for (int s = 0; s < kStages; ++s)
-                last_k[s] = last_v[s] = -1;
+            int last_k[L::kKStages], last_v[L::kVStages];
+            for (int s = 0; s < L::kKStages; ++s)
+                last_k[s] = -1;
+            for (int s = 0; s < L::kVStages; ++s)
+                last_v[s] = -1;
             bool ok = true;
             for (int segi = 0; ok && segment_at(p, cta, segi, sg); ++segi) {
                 if (sg.je == sg.jb)
                     continue;
                 Geom ge;
-                unit_geom(p, sg.unit, ge);
+                unit_geom<kUnitRows>(p, sg.unit, ge);
                 const int h = ge.h, b = ge.b;
                 if (act > 0 && !(ok = wait_bar(q_empty, (act - 1) & 1, abort_flag, p)))
                     break;
-                ptx::mbar_arrive_expect_tx(q_full, kTiles * L::kQBytes);
-                for (int t = 0; t < kTiles; ++t)
+                ptx::mbar_arrive_expect_tx(q_full, L::kQTiles * L::kQBytes);
+                for (int t = 0; t < L::kQTiles; ++t)
                     for (int pn = 0; pn < L::kPanels; ++pn)
                         ptx::tma_load_4d(&tmQ, q_full, smem + L::kQOff + t * L::kQBytes + pn * L::kQPanel, pn * 64,
                                          h, ge.q0 + t * kBM, b);
                 ++act;
-                for (int j = sg.jb; j < sg.je; ++j, ++kv) {
-                    const int s = kv % kStages, u = kv / kStages;
-                    if (u > 0 && !(ok = wait_bar(k_empty + s, (u - 1) & 1, abort_flag, p)))
-                        break;
-                    ptx::mbar_arrive_expect_tx(k_full + s, L::kKVBytes);
-                    for (int pn = 0; pn < L::kPanels; ++pn)
-                        ptx::tma_load_4d(&tmK, k_full + s, smem + L::kKOff + s * L::kKVBytes + pn * L::kKVPanel,
-                                         pn * 64, h, ge.k0 + j * kBN, b);
-                    last_k[s] = u;
-                    if (u > 0 && !(ok = wait_bar(v_empty + s, (u - 1) & 1, abort_flag, p)))
-                        break;
-                    ptx::mbar_arrive_expect_tx(v_full + s, L::kKVBytes);
-                    for (int pn = 0; pn < L::kPanels; ++pn)
-                        ptx::tma_load_4d(&tmV, v_full + s, smem + L::kVOff + s * L::kKVBytes + pn * L::kKVPanel,
-                                         pn * 64, h, ge.k0 + j * kBN, b);
-                    last_v[s] = u;
+                if constexpr (kHalves) {
+                    // Slot t takes key blocks [t*nh, t*nh + nh) of the unit's nb (the
+                    // second slot one fewer when nb is odd), loaded in the order the MMA
+                    // warp consumes them: block kv is step kv >> 1 of slot kv & 1 (only
+                    // the last step can lack the second slot's block). This thread
+                    // loads K; warp 2 loads V, so that a V stage waiting for its slot's
+                    // previous PV never holds back the next K block.
+                    const int nb = sg.je - sg.jb, nh = (nb + 1) / 2;
+                    for (kv = 0; kv < nb; ++kv) {
+                        const int j = sg.jb + (kv & 1) * nh + (kv >> 1);
+                        const int sk = kv % L::kKStages, uk = kv / L::kKStages;
+                        if (uk > 0 && !(ok = wait_bar(k_empty + sk, (uk - 1) & 1, abort_flag, p)))
+                            break;
+                        ptx::mbar_arrive_expect_tx(k_full + sk, L::kKVBytes);
+                        for (int pn = 0; pn < L::kPanels; ++pn)
+                            ptx::tma_load_4d(&tmK, k_full + sk, smem + L::kKOff + sk * L::kKVBytes + pn * L::kKVPanel,
+                                             pn * 64, h, ge.k0 + j * kBN, b);
+                        last_k[sk] = uk;
+                    }
+                } else {
+                    for (int j = sg.jb; j < sg.je; ++j, ++kv) {
+                        const int s = kv % kStages, u = kv / kStages;
+                        if (u > 0 && !(ok = wait_bar(k_empty + s, (u - 1) & 1, abort_flag, p)))
+                            break;
+                        ptx::mbar_arrive_expect_tx(k_full + s, L::kKVBytes);
+                        for (int pn = 0; pn < L::kPanels; ++pn)
+                            ptx::tma_load_4d(&tmK, k_full + s, smem + L::kKOff + s * L::kKVBytes + pn * L::kKVPanel,
+                                             pn * 64, h, ge.k0 + j * kBN, b);
+                        last_k[s] = u;
+                        if (u > 0 && !(ok = wait_bar(v_empty + s, (u - 1) & 1, abort_flag, p)))
+                            break;
+                        ptx::mbar_arrive_expect_tx(v_full + s, L::kKVBytes);
+                        for (int pn = 0; pn < L::kPanels; ++pn)
+                            ptx::tma_load_4d(&tmV, v_full + s, smem + L::kVOff + s * L::kKVBytes + pn * L::kKVPanel,
+                                             pn * 64, h, ge.k0 + j * kBN, b);
+                        last_v[s] = u;
+                    }
                 }
             }
             // Drain: every issued load has landed before the CTA can exit.
             if (act > 0)
                 wait_bar(q_full, (act - 1) & 1, abort_flag, p, false);
-            for (int s = 0; s < kStages; ++s) {
+            for (int s = 0; s < L::kKStages; ++s)
                 if (last_k[s] >= 0)
                     wait_bar(k_full + s, last_k[s] & 1, abort_flag, p, false);
+            for (int s = 0; s < L::kVStages; ++s)
                 if (last_v[s] >= 0)
                     wait_bar(v_full + s, last_v[s] & 1, abort_flag, p, false);
-            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issue
@@ -573,67 +611,111 @@ __global__ void __launch_bounds__(kThreads, 1)
             Segment sg;
             int kv = 0, g = 0, act = 0;
             bool ok = true;
-            for (int segi = 0; ok && segment_at(p, cta, segi, sg); ++segi) {
-                const int n = sg.je - sg.jb;
-                if (n == 0)
-                    continue;
-                if (!(ok = wait_bar_warp(q_full, act & 1, abort_flag, p)))
-                    break;
-                ptx::tc_fence_after();
-                for (int i = 0; i < n; ++i) {
-                    const int cur = kv + i, s = cur % kStages, u = cur / kStages;
-                    if (!(ok = wait_bar_warp(k_full + s, u & 1, abort_flag, p)))
+            if constexpr (kHalves) {
+                // One unit per CTA (one segment). Step i: slot 0's PV of block i-1 and
+                // QK^T of block i, then slot 1's; every K and V block belongs to one slot.
+                // Block kv is step i = kv >> 1 of slot t = kv & 1, whose V stage is t.
+                if (segment_at(p, cta, 0, sg) && sg.je > sg.jb) {
+                    const int nb = sg.je - sg.jb;
+                    ok = wait_bar_warp(q_full, 0, abort_flag, p);
+                    ptx::tc_fence_after();
+                    for (kv = 0; ok && kv < nb; ++kv) {
+                        const int i = kv >> 1, t = kv & 1;
+                        const int sk = kv % L::kKStages, uk = kv / L::kKStages;
+                        if (!(ok = wait_bar_warp(k_full + sk, uk & 1, abort_flag, p)))
+                            break;
+                        ptx::tc_fence_after();
+                        const uint32_t tS = tmem + t * kBN;
+                        if (i > 0) {  // this slot's PV of block i - 1 (V stage t, its use i - 1)
+                            if (!(ok = wait_bar_warp(v_full + t, (i - 1) & 1, abort_flag, p) &&
+                                       wait_bar_warp(p_full + t, (i - 1) & 1, abort_flag, p)))
+                                break;
+                            ptx::tc_fence_after();
+                            issue_pv<D, BF16>(tmem + 2 * kBN + t * D, tS, vbase + t * L::kKVBytes, i > 1);
+                            ptx::tc_commit(v_empty + t);
+                        }
+                        issue_qk<D, BF16>(tS, qa0, kbase + sk * L::kKVBytes);
+                        ptx::tc_commit(s_full + t);
+                        ptx::tc_commit(k_empty + sk);
+                    }
+                    if (ok)
+                        ptx::tc_commit(q_empty);
+                    for (int t = 0; ok && t < 2; ++t) {  // each slot's last PV
+                        const int nt = t ? nb / 2 : (nb + 1) / 2;
+                        if (nt == 0)
+                            break;
+                        if (!(ok = wait_bar_warp(v_full + t, (nt - 1) & 1, abort_flag, p) &&
+                                   wait_bar_warp(p_full + t, (nt - 1) & 1, abort_flag, p)))
+                            break;
+                        ptx::tc_fence_after();
+                        issue_pv<D, BF16>(tmem + 2 * kBN + t * D, tmem + t * kBN, vbase + t * L::kKVBytes, nt > 1);
+                        ptx::tc_commit(o_full + t);
+                        ptx::tc_commit(v_empty + t);
+                    }
+                }
+            } else {
+                for (int segi = 0; ok && segment_at(p, cta, segi, sg); ++segi) {
+                    const int n = sg.je - sg.jb;
+                    if (n == 0)
+                        continue;
+                    if (!(ok = wait_bar_warp(q_full, act & 1, abort_flag, p)))
                         break;
                     ptx::tc_fence_after();
-                    const int prv = cur - 1, sp = (cur + kStages - 1) % kStages, up = prv / kStages;
-                    if (i > 0) {
-                        if (!(ok = wait_bar_warp(v_full + sp, up & 1, abort_flag, p)))
-                            break;
-                        if (!(ok = wait_bar_warp(p_full + 0, (g + i - 1) & 1, abort_flag, p)))
-                            break;
-                        if (i == 1 && act > 0 && !(ok = wait_bar_warp(o_empty + 0, (act - 1) & 1, abort_flag, p)))
+                    for (int i = 0; i < n; ++i) {
+                        const int cur = kv + i, s = cur % kStages, u = cur / kStages;
+                        if (!(ok = wait_bar_warp(k_full + s, u & 1, abort_flag, p)))
                             break;
                         ptx::tc_fence_after();
-                        issue_pv<D, BF16>(tO0, tS0, vbase + sp * L::kKVBytes, i > 1);
+                        const int prv = cur - 1, sp = (cur + kStages - 1) % kStages, up = prv / kStages;
+                        if (i > 0) {
+                            if (!(ok = wait_bar_warp(v_full + sp, up & 1, abort_flag, p)))
+                                break;
+                            if (!(ok = wait_bar_warp(p_full + 0, (g + i - 1) & 1, abort_flag, p)))
+                                break;
+                            if (i == 1 && act > 0 && !(ok = wait_bar_warp(o_empty + 0, (act - 1) & 1, abort_flag, p)))
+                                break;
+                            ptx::tc_fence_after();
+                            issue_pv<D, BF16>(tO0, tS0, vbase + sp * L::kKVBytes, i > 1);
+                        }
+                        issue_qk<D, BF16>(tS0, qa0, kbase + s * L::kKVBytes);
+                        ptx::tc_commit(s_full + 0);
+                        if (i > 0) {
+                            if (!(ok = wait_bar_warp(p_full + 1, (g + i - 1) & 1, abort_flag, p)))
+                                break;
+                            if (i == 1 && act > 0 && !(ok = wait_bar_warp(o_empty + 1, (act - 1) & 1, abort_flag, p)))
+                                break;
+                            ptx::tc_fence_after();
+                            issue_pv<D, BF16>(tO1, tS1, vbase + sp * L::kKVBytes, i > 1);
+                            ptx::tc_commit(v_empty + sp);
+                        }
+                        issue_qk<D, BF16>(tS1, qa1, kbase + s * L::kKVBytes);
+                        ptx::tc_commit(s_full + 1);
+                        ptx::tc_commit(k_empty + s);
                     }
-                    issue_qk<D, BF16>(tS0, qa0, kbase + s * L::kKVBytes);
-                    ptx::tc_commit(s_full + 0);
-                    if (i > 0) {
-                        if (!(ok = wait_bar_warp(p_full + 1, (g + i - 1) & 1, abort_flag, p)))
-                            break;
-                        if (i == 1 && act > 0 && !(ok = wait_bar_warp(o_empty + 1, (act - 1) & 1, abort_flag, p)))
-                            break;
-                        ptx::tc_fence_after();
-                        issue_pv<D, BF16>(tO1, tS1, vbase + sp * L::kKVBytes, i > 1);
-                        ptx::tc_commit(v_empty + sp);
-                    }
-                    issue_qk<D, BF16>(tS1, qa1, kbase + s * L::kKVBytes);
-                    ptx::tc_commit(s_full + 1);
-                    ptx::tc_commit(k_empty + s);
+                    if (!ok)
+                        break;
+                    ptx::tc_commit(q_empty);  // the segment's QK^T products are all issued
+                    const int lst = kv + n - 1, sl = lst % kStages, ul = lst / kStages;
+                    ok = wait_bar_warp(v_full + sl, ul & 1, abort_flag, p) &&
+                         wait_bar_warp(p_full + 0, (g + n - 1) & 1, abort_flag, p) &&
+                         (n > 1 || act == 0 || wait_bar_warp(o_empty + 0, (act - 1) & 1, abort_flag, p));
+                    if (!ok)
+                        break;
+                    ptx::tc_fence_after();
+                    issue_pv<D, BF16>(tO0, tS0, vbase + sl * L::kKVBytes, n > 1);
+                    ptx::tc_commit(o_full + 0);
+                    ok = wait_bar_warp(p_full + 1, (g + n - 1) & 1, abort_flag, p) &&
+                         (n > 1 || act == 0 || wait_bar_warp(o_empty + 1, (act - 1) & 1, abort_flag, p));
+                    if (!ok)
+                        break;
+                    ptx::tc_fence_after();
+                    issue_pv<D, BF16>(tO1, tS1, vbase + sl * L::kKVBytes, n > 1);
+                    ptx::tc_commit(o_full + 1);
+                    ptx::tc_commit(v_empty + sl);
+                    kv += n;
+                    g += n;
+                    ++act;
                 }
-                if (!ok)
-                    break;
-                ptx::tc_commit(q_empty);  // the segment's QK^T products are all issued
-                const int lst = kv + n - 1, sl = lst % kStages, ul = lst / kStages;
-                ok = wait_bar_warp(v_full + sl, ul & 1, abort_flag, p) &&
-                     wait_bar_warp(p_full + 0, (g + n - 1) & 1, abort_flag, p) &&
-                     (n > 1 || act == 0 || wait_bar_warp(o_empty + 0, (act - 1) & 1, abort_flag, p));
-                if (!ok)
-                    break;
-                ptx::tc_fence_after();
-                issue_pv<D, BF16>(tO0, tS0, vbase + sl * L::kKVBytes, n > 1);
-                ptx::tc_commit(o_full + 0);
-                ok = wait_bar_warp(p_full + 1, (g + n - 1) & 1, abort_flag, p) &&
-                     (n > 1 || act == 0 || wait_bar_warp(o_empty + 1, (act - 1) & 1, abort_flag, p));
-                if (!ok)
-                    break;
-                ptx::tc_fence_after();
-                issue_pv<D, BF16>(tO1, tS1, vbase + sl * L::kKVBytes, n > 1);
-                ptx::tc_commit(o_full + 1);
-                ptx::tc_commit(v_empty + sl);
-                kv += n;
-                g += n;
-                ++act;
             }
             // Every MMA issued above has retired before TMEM is released.
             ptx::tc_commit(mma_done);
@@ -642,13 +724,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp < 4) {
         ptx::setmaxnreg_dec<kRegsControl>();  // warps 2-3: registers only
+        if constexpr (kHalves) {
+            // ------------------------------------------------ V loads (halves units)
+            // Block kv is step kv >> 1 of slot kv & 1; V stage t belongs to slot t
+            // and is reused once that slot's PV of the previous step has retired.
+            static_assert(L::kVStages == 2, "V stage t belongs to slot t");
+            Segment sg;
+            if (warp == 2 && lane == 0 && segment_at(p, cta, 0, sg) && sg.je > sg.jb) {
+                ptx::tma_prefetch_desc(&tmV);
+                Geom ge;
+                unit_geom<kUnitRows>(p, sg.unit, ge);
+                const int nb = sg.je - sg.jb, nh = (nb + 1) / 2;
+                int last_v[2] = {-1, -1};
+                for (int kv = 0; kv < nb; ++kv) {
+                    const int sv = kv & 1, uv = kv >> 1;
+                    if (uv > 0 && !wait_bar(v_empty + sv, (uv - 1) & 1, abort_flag, p))
+                        break;
+                    ptx::mbar_arrive_expect_tx(v_full + sv, L::kKVBytes);
+                    for (int pn = 0; pn < L::kPanels; ++pn)
+                        ptx::tma_load_4d(&tmV, v_full + sv, smem + L::kVOff + sv * L::kKVBytes + pn * L::kKVPanel,
+                                         pn * 64, ge.h, ge.k0 + (sg.jb + sv * nh + uv) * kBN, ge.b);
+                    last_v[sv] = uv;
+                }
+                // Drain: every issued load has landed before the CTA can exit.
+                for (int s = 0; s < 2; ++s)
+                    if (last_v[s] >= 0)
+                        wait_bar(v_full + s, last_v[s] & 1, abort_flag, p, false);
+            }
+        }
     } else {
         // ------------------------------------------------------------ softmax
         ptx::setmaxnreg_inc<kRegsSoftmax>();
         const int t = (warp - 4) >> 2;  // query tile
         const int quad = warp & 3;      // TMEM lane quadrant this warp may access
         const int row = quad * 32 + lane;
-        const int prow = t * kBM + row;  // row inside the unit's 256 query rows
+        const int prow = kHalves ? row : t * kBM + row;  // row inside the unit's query rows
         const bool tile_leader = ((warp - 4) & 3) == 0 && lane == 0;
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t tS = tmem + lane_off + t * kBN;
@@ -669,11 +779,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if constexpr (kTicketMerge)
                     tix = sg.full ? -1 : sg.unit;
                 Geom ge;
-                unit_geom(p, sg.unit, ge);
+                unit_geom<kUnitRows>(p, sg.unit, ge);
                 // the key mask is indexed by the key's global position: batch row, then k0 + offset
                 mrow = p.mask ? p.mask + static_cast<size_t>(ge.b) * p.Sk + ge.k0 : nullptr;
                 n = sg.je - sg.jb;
                 jb = sg.jb;
+                if constexpr (kHalves) {
+                    // this slot's half of the unit's key blocks: [jb + t*nh, ...)
+                    const int nh = (n + 1) / 2;
+                    jb += t * nh;
+                    n = t ? n - nh : nh;
+                    if (n == 0 && t == 1)
+                        continue;  // nothing for the second slot (at most one key block)
+                }
                 k_len = ge.k_len;
                 if (n == 0) {
                     // query rows with no key at all (a packed document without keys): O = 0, LSE = -inf
@@ -874,11 +992,68 @@ __global__ void __launch_bounds__(kThreads, 1)
             Segment sg;
             segment_at(p, cta, opaque(segi), sg);
             Geom ge;
-            unit_geom(p, sg.unit, ge);
+            unit_geom<kUnitRows>(p, sg.unit, ge);
             const int h = ge.h, b = ge.b;
             const int qrow = ge.q0 + prow;
             const int q_end = ge.q_end;
-            if (sg.full) {
+            if constexpr (kHalves) {
+                // The second slot hands its rows' (m, l) to the first through its unused
+                // staging area; the first merges the two halves by log-sum-exp with
+                // both O read from TMEM (the same lanes, the second half's columns).
+                float2 *const ml_half = reinterpret_cast<float2 *>(reinterpret_cast<uint8_t *>(bars) +
+                                                                   (L::kEpiOff - L::kBarOff) + 4 * L::kEpiWarpBytes);
+                if (t == 1) {
+                    ml_half[row] = make_float2(m_run, l_run);
+                    ptx::mbar_arrive(seg_done + 1);
+                } else {
+                    const int nb = sg.je - sg.jb;
+                    const bool has1 = nb - (nb + 1) / 2 > 0;
+                    float2 ml1 = make_float2(-INFINITY, 0.f);
+                    if (has1) {
+                        if (!(ok = wait_bar_warp(seg_done + 1, 0, abort_flag, p) &&
+                                   wait_bar_warp(o_full + 1, 0, abort_flag, p)))
+                            break;
+                        ptx::tc_fence_after();
+                        ml1 = ml_half[row];
+                    }
+                    const float M = fmaxf(m_run, ml1.x);
+                    const float w0 = m_run == -INFINITY ? 0.f : ptx::ex2_approx(m_run - M);
+                    const float w1 = ml1.x == -INFINITY ? 0.f : ptx::ex2_approx(ml1.x - M);
+                    const float lsum = fmaf(w1, ml1.y, w0 * l_run);
+                    const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
+                    const unsigned long long orow =
+                        qrow < q_end ? reinterpret_cast<unsigned long long>(out_row<D>(p, b, h, qrow)) : 0ull;
+                    uint4 *const stg = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(bars) +
+                                                                 (L::kEpiOff - L::kBarOff) + (warp - 4) * L::kEpiWarpBytes);
+#pragma unroll
+                    for (int hf = 0; hf < D / 64; ++hf) {
+#pragma unroll
+                        for (int qq = 0; qq < 2; ++qq) {
+                            uint32_t o[32];
+                            ptx::tmem_ld32(tO + hf * 64 + qq * 32, o);
+                            ptx::tmem_ld_wait();
+                            ptx::reg_fence32(o);
+                            float of[32];
+#pragma unroll
+                            for (int k = 0; k < 32; ++k)
+                                of[k] = w0 * __uint_as_float(o[k]);
+                            if (has1) {
+                                ptx::tmem_ld32(tO + D + hf * 64 + qq * 32, o);
+                                ptx::tmem_ld_wait();
+                                ptx::reg_fence32(o);
+#pragma unroll
+                                for (int k = 0; k < 32; ++k)
+                                    of[k] = fmaf(w1, __uint_as_float(o[k]), of[k]);
+                            }
+                            stage32<BF16>(stg, lane, qq, of, inv);
+                        }
+                        store_staged(stg, lane, orow, hf * 8);
+                    }
+                    if (p.lse && qrow < q_end)
+                        p.lse[(static_cast<size_t>(b) * p.H + h) * p.Sq + qrow] =
+                            lsum > 0.f ? (M + log2f(lsum)) * kLn2 : -INFINITY;
+                }
+            } else if (sg.full) {
                 const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
                 const float lse_val = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
                 // Each thread converts its own row into the warp's staging
@@ -1272,6 +1447,7 @@ struct Schedule {
     int n_units, n_kblocks, grid, dp_waves;
     long long tail_iters;
     bool ticket_merge;  // merge split units with the ticket-first protocol
+    bool halves;        // units of one 128-row tile, key range shared out between the CTA's two slots
 };
 
 // Calls whose CTAs each run at most this many key blocks (about 250 us at the
@@ -1295,6 +1471,13 @@ constexpr long long kTicketMergeMaxBlocks = 160;
 // blocks) is faster with the second.
 constexpr long long kMinTailBlocks = 32;
 
+// Cost of one halves-mode key-block step against a two-tile step, in
+// percent. Measured on GB300 without a workspace: one Wan-like 480p rank
+// (Q 4095 x K/V 32760, 12 heads: 512 -> 384 steps) 1.45 -> 1.54 us per step,
+// 1108 -> 1391 TFLOP/s; Q 9450 x K/V 75600, 10 heads (1773 -> 1480 steps)
+// 1.44 -> 1.51 us, 1435 -> 1637 TFLOP/s.
+constexpr long long kHalvesStepCost = 107;
+
 Schedule plan(int B, int Sq, int Sk, int H, int sms, bool split)
 {
     Schedule s{};
@@ -1303,6 +1486,19 @@ Schedule plan(int B, int Sq, int Sk, int H, int sms, bool split)
     s.n_units = static_cast<int>(attention_units(B, Sq, H));
     s.n_kblocks = (Sk + kBN - 1) / kBN;
     if (!split) {
+        // Without a workspace no unit can be cut between CTAs. When the last
+        // wave of 256-row units leaves many SMs idle, 128-row units whose two
+        // halves of the key range run side by side in one CTA (merged inside
+        // it) end sooner: the makespan in key-block steps, waves x blocks, is
+        // compared, the halves steps counted kHalvesStepCost times (two K/V
+        // streams per CTA instead of one shared).
+        const long long n_h = (static_cast<long long>(Sq) + kBM - 1) / kBM * H * B;  // 128-row units
+        const long long steps_t = (s.n_units + sms - 1) / sms * static_cast<long long>(s.n_kblocks);
+        const long long steps_h = (n_h + sms - 1) / sms * ((s.n_kblocks + 1) / 2);
+        if (s.n_kblocks >= 2 && n_h <= INT_MAX && steps_h * kHalvesStepCost < steps_t * 100) {
+            s.halves = true;
+            s.n_units = static_cast<int>(n_h);
+        }
         s.grid = s.n_units;
         s.dp_waves = 1;
         s.tail_iters = 0;
@@ -1361,7 +1557,7 @@ long long ws_bytes(const Schedule &s, int D)
 // count differs from kRegsLaunch (the warpgroups' register budgets add up to
 // the launch's total only then; a larger split would never be granted), and
 // raise the kernel's dynamic shared memory limit.
-template <int D, bool BF16, bool TM>
+template <int D, bool BF16, bool TM, bool HV>
 cudaError_t prepare_kernel()
 {
     static bool attr_set[64] = {false};
@@ -1374,13 +1570,13 @@ cudaError_t prepare_kernel()
     if (dev < 64 && attr_set[dev])
         return cudaSuccess;
     cudaFuncAttributes fa{};
-    err = cudaFuncGetAttributes(&fa, attn_fwd_kernel<D, BF16, TM>);
+    err = cudaFuncGetAttributes(&fa, attn_fwd_kernel<D, BF16, TM, HV>);
     if (err != cudaSuccess)
         return err;
     if (fa.numRegs != kRegsLaunch || fa.maxThreadsPerBlock < kThreads)
         return cudaErrorInvalidDeviceFunction;
-    err = cudaFuncSetAttribute(attn_fwd_kernel<D, BF16, TM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               Layout<D>::kAlloc);
+    err = cudaFuncSetAttribute(attn_fwd_kernel<D, BF16, TM, HV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               Layout<D, HV>::kAlloc);
     if (err != cudaSuccess)
         return err;
     if (dev < 64)
@@ -1419,7 +1615,8 @@ cudaError_t launch_typed(const AttnArgs &a, cudaStream_t stream)
     p.Sq = a.Sq;
     p.Sk = a.Sk;
     p.H = a.H;
-    p.n_qpairs = ((varlen ? a.max_seqlen_q : a.Sq) + kTiles * kBM - 1) / (kTiles * kBM);
+    const int unit_rows = sc.halves ? kBM : kTiles * kBM;
+    p.n_qpairs = ((varlen ? a.max_seqlen_q : a.Sq) + unit_rows - 1) / unit_rows;
     p.n_kblocks = sc.n_kblocks;
     p.cu_q = a.cu_q;
     p.cu_k = a.cu_k;
@@ -1450,15 +1647,21 @@ cudaError_t launch_typed(const AttnArgs &a, cudaStream_t stream)
             return err;
         p.var_prefix = prefix;
     }
-    if (sc.ticket_merge) {
-        if ((err = prepare_kernel<D, BF16, true>()) != cudaSuccess)
+    if (sc.halves) {
+        if ((err = prepare_kernel<D, BF16, false, true>()) != cudaSuccess)
             return err;
-        attn_fwd_kernel<D, BF16, true><<<static_cast<unsigned>(sc.grid), kThreads, L::kAlloc, stream>>>(mq, mk, mv, p);
+        attn_fwd_kernel<D, BF16, false, true>
+            <<<static_cast<unsigned>(sc.grid), kThreads, Layout<D, true>::kAlloc, stream>>>(mq, mk, mv, p);
+    } else if (sc.ticket_merge) {
+        if ((err = prepare_kernel<D, BF16, true, false>()) != cudaSuccess)
+            return err;
+        attn_fwd_kernel<D, BF16, true, false><<<static_cast<unsigned>(sc.grid), kThreads, L::kAlloc, stream>>>(mq, mk,
+                                                                                                                mv, p);
     } else {
-        if ((err = prepare_kernel<D, BF16, false>()) != cudaSuccess)
+        if ((err = prepare_kernel<D, BF16, false, false>()) != cudaSuccess)
             return err;
-        attn_fwd_kernel<D, BF16, false><<<static_cast<unsigned>(sc.grid), kThreads, L::kAlloc, stream>>>(mq, mk, mv,
-                                                                                                          p);
+        attn_fwd_kernel<D, BF16, false, false><<<static_cast<unsigned>(sc.grid), kThreads, L::kAlloc, stream>>>(mq, mk,
+                                                                                                                 mv, p);
     }
     return cudaGetLastError();
 }

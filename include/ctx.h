@@ -223,14 +223,18 @@ ctx_status ctx_merge_joint_attn_mask(const unsigned char *image_mask, int image_
  * out      : [B, Sq, H, D], device, same dtype as q.
  * lse      : NULL or [B, H, Sq] float32, device (natural log).
  * workspace, workspace_bytes :
- *            NULL / 0: one CTA per (256 query rows, head, batch) unit. This
- *            form is slower whenever the unit count leaves a partial last
- *            wave on the GPU's SMs: on a 152-SM GB300, one rank of a 480p
- *            video layer (Q [1,4095,12,128], 192 units) runs at about 0.69 of
- *            the balanced schedule's speed, and small calls (fewer units than
- *            SMs) leave SMs idle. Callers that can should pass a workspace
- *            (size from ctx_attn_lq_gkv_workspace_size; callers that cannot
- *            allocate have ctx_attn_lq_gkv_noalloc).
+ *            NULL / 0: no unit is split between CTAs. One CTA per (256 query
+ *            rows, head, batch) unit, or, where that leaves a partial last
+ *            wave on the SMs and it ends sooner, one CTA per (128 query rows,
+ *            head, batch) unit whose two halves of the key range run side by
+ *            side in the CTA and are merged inside it. Still slower than a
+ *            workspace whenever the units do not fill the SMs evenly: on a
+ *            152-SM GB300, one rank of a 480p video layer
+ *            (Q [1,4095,12,128]) runs at about 0.85 of the balanced
+ *            schedule's speed, and small calls (fewer units than SMs) leave
+ *            SMs idle. Callers that can should pass a workspace (size from
+ *            ctx_attn_lq_gkv_workspace_size; callers that cannot allocate
+ *            have ctx_attn_lq_gkv_noalloc).
  *            Otherwise device memory of at least
  *            ctx_attn_lq_gkv_workspace_size(B, Sq, Sk, H, D) bytes, 256-byte
  *            aligned, filled with zeros before its first use: a persistent

@@ -93,7 +93,8 @@ def test_fp16(ctx, orc):
 
 
 @pytest.mark.parametrize("split", [False, True], ids=["per_unit", "balanced"])
-@pytest.mark.parametrize("kind", ["random", "rear_text", "front_text", "first_block_empty", "row_empty"])
+@pytest.mark.parametrize("kind", ["random", "rear_text", "front_text", "first_block_empty", "first_half_empty",
+                                  "row_empty"])
 def test_key_mask(ctx, orc, kind, split):
     gen = torch.Generator().manual_seed(11)
     B, Sq, Sk, H, D = 2, 200, 600, 2, 128
@@ -110,6 +111,8 @@ def test_key_mask(ctx, orc, kind, split):
         mask[1, 180:256] = 0
     elif kind == "first_block_empty":
         mask[:, :300] = 0
+    elif kind == "first_half_empty":  # 5 key blocks: without a workspace the first 3 (one slot's half) are all masked
+        mask[:, :384] = 0
     elif kind == "row_empty":
         mask[1, :] = 0
     O, L = _run(ctx, q, k, v, mask=mask, guard=True, split=split)
