@@ -7,9 +7,10 @@
 //
 // How (GB300-first design):
 //   * one CTA = two 128-row query tiles of one (b, h) sharing one K/V stream;
-//   * warp 0 issues TMA loads: both Q tiles once, then K and V blocks of 128
-//     keys into a two-stage ring (128-byte swizzled tiles, mbarrier
-//     complete_tx accounting);
+//   * warp 0 issues TMA loads: both Q tiles once, then K blocks of 128 keys
+//     into a two-stage ring (128-byte swizzled tiles, mbarrier complete_tx
+//     accounting), and warp 2 the V blocks into their own two-stage ring (in
+//     the ticket-merge instantiation for short calls warp 0 loads V too);
 //   * warp 1 allocates 512 TMEM columns and runs the MMA loop as a whole warp
 //     (warp-uniform descriptors), one elected lane issuing every tcgen05.mma:
 //     S_t = Q_t K^T (A and B from shared memory, K-major) into
@@ -17,8 +18,8 @@
 //     (it overwrites S_t as 16-bit pairs) and V from shared memory (MN-major)
 //     into columns [256 + Dt, 256 + D(t+1));
 //   * warps 4-7 and 8-11 are the softmax of tile 0 and tile 1 (warps 2-3
-//     only hand their registers over: the first warpgroup runs with 104
-//     registers per thread, the softmax warpgroups with 200): each thread
+//     hand registers over, and warp 2 then loads V: the first warpgroup runs
+//     with 104 registers per thread, the softmax warpgroups with 200): each thread
 //     owns one query row (its TMEM lane), reads its 128 scores with
 //     tcgen05.ld, does the online softmax in the log2 domain with exp2, writes
 //     P back with tcgen05.st and signals the MMA warp. The MMA warp issues
@@ -576,13 +577,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ptx::tma_load_4d(&tmK, k_full + s, smem + L::kKOff + s * L::kKVBytes + pn * L::kKVPanel,
                                              pn * 64, h, ge.k0 + j * kBN, b);
                         last_k[s] = u;
-                        if (u > 0 && !(ok = wait_bar(v_empty + s, (u - 1) & 1, abort_flag, p)))
-                            break;
-                        ptx::mbar_arrive_expect_tx(v_full + s, L::kKVBytes);
-                        for (int pn = 0; pn < L::kPanels; ++pn)
-                            ptx::tma_load_4d(&tmV, v_full + s, smem + L::kVOff + s * L::kKVBytes + pn * L::kKVPanel,
-                                             pn * 64, h, ge.k0 + j * kBN, b);
-                        last_v[s] = u;
+                        if constexpr (kTicketMerge) {  // other instantiations: warp 2 loads V
+                            if (u > 0 && !(ok = wait_bar(v_empty + s, (u - 1) & 1, abort_flag, p)))
+                                break;
+                            ptx::mbar_arrive_expect_tx(v_full + s, L::kKVBytes);
+                            for (int pn = 0; pn < L::kPanels; ++pn)
+                                ptx::tma_load_4d(&tmV, v_full + s,
+                                                 smem + L::kVOff + s * L::kKVBytes + pn * L::kKVPanel, pn * 64, h,
+                                                 ge.k0 + j * kBN, b);
+                            last_v[s] = u;
+                        }
                     }
                 }
             }
@@ -748,6 +752,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // Drain: every issued load has landed before the CTA can exit.
                 for (int s = 0; s < 2; ++s)
+                    if (last_v[s] >= 0)
+                        wait_bar(v_full + s, last_v[s] & 1, abort_flag, p, false);
+            }
+        } else if constexpr (!kTicketMerge) {
+            // ------------------------------------------------ V loads (long calls)
+            // Warp 0 loads Q and K; this thread loads V, so that a V stage waiting
+            // for its PV never holds back the next K block (same-box A/B on GB300:
+            // the batched Wan-like 480p call 1655 -> 1669-1671 TFLOP/s, one 480p rank
+            // 1637-1641 -> 1647; the short calls of the ticket-merge instantiation
+            // measured no better and keep V in the producer). Block kv of the load
+            // order is the kv-th key block of the CTA's segments.
+            if (warp == 2 && lane == 0) {
+                ptx::tma_prefetch_desc(&tmV);
+                int last_v[L::kVStages];
+                for (int s = 0; s < L::kVStages; ++s)
+                    last_v[s] = -1;
+                Segment sg;
+                int kv = 0;
+                bool ok = true;
+                for (int segi = 0; ok && segment_at(p, cta, segi, sg); ++segi) {
+                    if (sg.je == sg.jb)
+                        continue;
+                    Geom ge;
+                    unit_geom<kUnitRows>(p, sg.unit, ge);
+                    for (int j = sg.jb; j < sg.je; ++j, ++kv) {
+                        const int s = kv % L::kVStages, u = kv / L::kVStages;
+                        if (u > 0 && !(ok = wait_bar(v_empty + s, (u - 1) & 1, abort_flag, p)))
+                            break;
+                        ptx::mbar_arrive_expect_tx(v_full + s, L::kKVBytes);
+                        for (int pn = 0; pn < L::kPanels; ++pn)
+                            ptx::tma_load_4d(&tmV, v_full + s, smem + L::kVOff + s * L::kKVBytes + pn * L::kKVPanel,
+                                             pn * 64, ge.h, ge.k0 + j * kBN, ge.b);
+                        last_v[s] = u;
+                    }
+                }
+                // Drain: every issued load has landed before the CTA can exit.
+                for (int s = 0; s < L::kVStages; ++s)
                     if (last_v[s] >= 0)
                         wait_bar(v_full + s, last_v[s] & 1, abort_flag, p, false);
             }
