@@ -608,6 +608,19 @@ def run_merge_bench(args):
     clocks = sampler.stop() if sampler else None
     ms = e0.elapsed_time(e1) / args.steps
     gbs = nbytes / (ms * 1e-3) / 1e9
+    # the same traffic mix without the merge arithmetic: an elementwise add of
+    # the two segments' O (two reads and one write of the same O bytes), timed
+    # the same way, as the reference for what this mix reaches on the device
+    add_out = torch.empty_like(out)
+    for _ in range(args.warmup):
+        torch.add(o[0], o[1], out=add_out)
+    e0.record()
+    for _ in range(args.steps):
+        torch.add(o[0], o[1], out=add_out)
+    e1.record()
+    torch.cuda.synchronize()
+    add_bytes = 3 * rows * D * 2
+    add_gbs = add_bytes / (e0.elapsed_time(e1) / args.steps * 1e-3) / 1e9
     # e2e: parts in from pinned host memory, merged output back
     oh, lh = o_host.pin_memory(), l_host.pin_memory()
     outh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -629,7 +642,9 @@ def run_merge_bench(args):
             "roofline": {"bound": "hbm", "kernel": "lse_merge_kernel", "achieved": round(gbs, 1),
                          "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
                          "peak_source": f"{kind} hbm_gbs", "algorithmic_bytes_per_launch": nbytes,
-                         "traffic": None},
+                         "traffic": None, "add_gbs": round(add_gbs, 1),
+                         "add_note": "torch.add of the two segments' O (2 reads + 1 write of the same O bytes), "
+                                     "timed the same way"},
             "gpu_launches": args.steps, "clocks": clocks,
             "e2e": {"value": round(nbytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                     "h2d_bytes_per_step": oh.numel() * 2 + lh.numel() * 4,

@@ -39,12 +39,14 @@ __device__ __forceinline__ void widen8(const uint4 &v, float *f)
 }
 
 // DV = D/8 lanes own one row (a "lane group"); a warp holds 32/DV groups and
-// every group merges kUnr rows per iteration. All PT segment LSEs and all PT
-// 16-byte chunks of those rows are loaded before any of them is used, so a
-// lane keeps PT*kUnr loads in flight and an iteration waits for one DRAM
-// round trip. Row indices are decomposed once per row, in 32-bit arithmetic
-// when every row index fits (I32); with 64 registers a thread, four blocks
-// stay resident on an SM (three for four segments).
+// every group merges kUnr rows per pass. All PT 16-byte chunks of those rows
+// are loaded before any of them is used, so a lane keeps PT*kUnr loads in
+// flight and a pass waits for one DRAM round trip. The pass's rows' weights
+// are computed once per row by one lane each (its LSE loads, the row index
+// decomposed in 32-bit arithmetic when every index fits, I32) and handed to
+// the row's lanes by shuffle; the weighted sum runs as packed fp32 pairs.
+// With 64 registers a thread, four blocks stay resident on an SM (three for
+// four segments).
 __host__ __device__ constexpr int merge_unroll(int pt) { return pt <= 2 ? 4 : 2; }
 __host__ __device__ constexpr int merge_min_blocks(int pt) { return pt <= 3 ? 4 : 3; }
 
@@ -59,68 +61,89 @@ __global__ void __launch_bounds__(256, merge_min_blocks(PT)) lse_merge_kernel(co
     const int grp = lane / DV, c = lane % DV;
     const long long warp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const long long n_warps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
-    for (long long r0 = warp * kGroups * kUnr; r0 < rows; r0 += n_warps * kGroups * kUnr) {
-        long long r[kUnr], lrow[kUnr];
-        float lv[kUnr][PT];
+    constexpr int kRows = kGroups * kUnr;  // rows of one pass of the warp
+    static_assert(kRows <= 32, "one lane per row computes the weights");
+    for (long long r0 = warp * kRows; r0 < rows; r0 += n_warps * kRows) {
+        // rows are walked in output order r = (b*Sq + i)*H + h of [B, Sq, H, D], so a
+        // warp's rows are one contiguous stretch of every part (the bulk of the bytes)
         uint4 ov[kUnr][PT];
 #pragma unroll
         for (int u = 0; u < kUnr; ++u) {
-            // rows are walked in output order r = (b*Sq + i)*H + h of [B, Sq, H, D], so a
-            // warp's rows are one contiguous stretch of every part (the bulk of the bytes);
-            // the LSE of a row sits at lrow = (b*H + h)*Sq + i of [B, H, Sq] (small, L2-resident)
             const long long l0 = r0 + static_cast<long long>(u) * kGroups + grp;
             const long long rr = l0 < rows ? l0 : rows - 1;  // clamp: loads stay in bounds
+#pragma unroll
+            for (int p = 0; p < PT; ++p)
+                ov[u][p] = __ldg(o_parts + (p * rows + rr) * DV + c);
+        }
+        // The weights of the pass's rows, once per row: lane j < kRows takes row
+        // r0 + j (pass order u*kGroups + grp), whose LSE sits at
+        // lrow = (b*H + h)*Sq + i of [B, H, Sq] (small, L2-resident). With
+        // m = max_p lse_p, e_p = 2^((lse_p - m) log2 e) (0 for an empty segment,
+        // 1 for the largest), l = sum_p e_p: w_p = e_p / l, lse = m + ln l.
+        float w[PT];
+#pragma unroll
+        for (int p = 0; p < PT; ++p)
+            w[p] = 0.f;
+        if (lane < kRows) {
+            const long long l0 = r0 + lane;
+            const long long rr = l0 < rows ? l0 : rows - 1;
+            long long lrow;
             if constexpr (I32) {
                 const unsigned r32 = static_cast<unsigned>(rr), hu = static_cast<unsigned>(H);
                 const unsigned bi = r32 / hu, h = r32 - bi * hu;
                 const unsigned b = bi / static_cast<unsigned>(Sq), i = bi - b * static_cast<unsigned>(Sq);
-                lrow[u] = static_cast<long long>((b * hu + h) * static_cast<unsigned>(Sq) + i);
+                lrow = static_cast<long long>((b * hu + h) * static_cast<unsigned>(Sq) + i);
             } else {
                 const long long bi = rr / H, h = rr - bi * H;
                 const long long b = bi / Sq, i = bi - b * Sq;
-                lrow[u] = (b * H + h) * Sq + i;
+                lrow = (b * H + h) * Sq + i;
             }
-            r[u] = l0 < rows ? rr : rows;
+            float lv[PT];
 #pragma unroll
-            for (int p = 0; p < PT; ++p) {
-                lv[u][p] = __ldg(lse_parts + p * rows + lrow[u]);
-                ov[u][p] = __ldg(o_parts + (p * rows + rr) * DV + c);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kUnr; ++u) {
-            float m = lv[u][0];
+            for (int p = 0; p < PT; ++p)
+                lv[p] = __ldg(lse_parts + p * rows + lrow);
+            float m = lv[0];
 #pragma unroll
             for (int p = 1; p < PT; ++p)
-                m = fmaxf(m, lv[u][p]);
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                m = fmaxf(m, lv[p]);
             float total = -INFINITY;
             if (m != -INFINITY) {
-                // e_p = 2^((lse_p - m) log2 e): 0 for an empty segment (lse_p = -inf), 1 for the largest
                 float e[PT], l = 0.f;
 #pragma unroll
                 for (int p = 0; p < PT; ++p) {
-                    e[p] = ptx::ex2_approx((lv[u][p] - m) * kLog2e);
+                    e[p] = ptx::ex2_approx((lv[p] - m) * kLog2e);
                     l += e[p];
                 }
                 const float inv = __frcp_rn(l);  // l >= 1
                 total = m + kLn2 * ptx::lg2_approx(l);
 #pragma unroll
-                for (int p = 0; p < PT; ++p) {
-                    const float w = e[p] * inv;
-                    float f[8];
-                    widen8<BF16>(ov[u][p], f);
+                for (int p = 0; p < PT; ++p)
+                    w[p] = e[p] * inv;
+            }
+            if (lse_out && l0 < rows)
+                lse_out[lrow] = total;
+        }
 #pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        acc[k] = fmaf(w, f[k], acc[k]);
-                }
+        for (int u = 0; u < kUnr; ++u) {
+            const int src = u * kGroups + grp;  // the lane that holds this row's weights
+            uint64_t acc[4] = {0, 0, 0, 0};     // (fp32, fp32) pairs of the lane's 8 columns
+#pragma unroll
+            for (int p = 0; p < PT; ++p) {
+                const float wp = __shfl_sync(0xffffffffu, w[p], src);
+                const uint64_t w2 = ptx::f2_pack(wp, wp);
+                float f[8];
+                widen8<BF16>(ov[u][p], f);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    acc[k] = ptx::f2_fma(w2, ptx::f2_pack(f[2 * k], f[2 * k + 1]), acc[k]);
             }
-            if (r[u] < rows) {
-                out[r[u] * DV + c] = make_uint4(ptx::pack2<BF16>(acc[0], acc[1]), ptx::pack2<BF16>(acc[2], acc[3]),
-                                                ptx::pack2<BF16>(acc[4], acc[5]), ptx::pack2<BF16>(acc[6], acc[7]));
-                if (lse_out && c == 0)
-                    lse_out[lrow[u]] = total;
-            }
+            const long long l0 = r0 + static_cast<long long>(u) * kGroups + grp;
+            if (l0 < rows)
+                out[l0 * DV + c] =
+                    make_uint4(ptx::pack2<BF16>(ptx::f2_lo(acc[0]), ptx::f2_hi(acc[0])),
+                               ptx::pack2<BF16>(ptx::f2_lo(acc[1]), ptx::f2_hi(acc[1])),
+                               ptx::pack2<BF16>(ptx::f2_lo(acc[2]), ptx::f2_hi(acc[2])),
+                               ptx::pack2<BF16>(ptx::f2_lo(acc[3]), ptx::f2_hi(acc[3])));
         }
     }
 }
