@@ -300,10 +300,22 @@ def run_pack_line(args, dev, peaks, peak_kind):
                 fn(i)
         return g
 
+    def copy_ranks(i):
+        # the same bytes as four per-rank copies on the rank streams, as the packs run
+        R = wl.ranks
+
+        def one(g, s):
+            n = src[i].numel() // R
+            with torch.cuda.stream(s):
+                dst[i][g * n:(g + 1) * n].copy_(src[i][g * n:(g + 1) * n])
+
+        sims[i]._per_rank(None, one)
+
     graphs = {"pack": capture(lambda i: sims[i].pack_ranks()),
               "unpack": capture(lambda i: sims[i].unpack_ranks()),
               "step": capture(lambda i: sims[i].exchange_in()),
-              "copy": capture(lambda i: dst[i].copy_(src[i]))}
+              "copy": capture(lambda i: dst[i].copy_(src[i])),
+              "copy_ranks": capture(copy_ranks)}
     torch.cuda.synchronize(dev)
     stream = torch.cuda.current_stream(dev)
     reps = max(args.steps, 20)
@@ -322,6 +334,7 @@ def run_pack_line(args, dev, peaks, peak_kind):
         return e0.elapsed_time(e1) / (reps * n_sets)  # per set
 
     ms_pack, ms_unpack, ms_step, ms_copy = timed("pack"), timed("unpack"), timed("step"), timed("copy")
+    ms_copy_ranks = timed("copy_ranks")
     gbs = (b_pack + b_unpack) / ((ms_pack + ms_unpack) * 1e-3) / 1e9
 
     def rate(b, ms):
@@ -336,6 +349,9 @@ def run_pack_line(args, dev, peaks, peak_kind):
             "pack_ms": round(ms_pack, 4), "unpack_ms": round(ms_unpack, 4),
             "algorithmic_bytes": {"pack": b_pack, "unpack": b_unpack},
             "copy_gbs": rate(b_pack, ms_copy),
+            "copy_per_rank_gbs": rate(b_pack, ms_copy_ranks),
+            "copy_note": "copy_gbs: one device copy of a set's bytes; copy_per_rank_gbs: the same bytes as one "
+                         "copy per rank on the rank streams (the packs' launch pattern)",
             "timing": f"one CUDA graph over {n_sets} buffer sets of {set_bytes >> 20} MiB (L2 {l2_bytes >> 20} MiB), "
                       f"replayed {reps} times back to back: reads from HBM, write-back inside the timed region",
             "gpu_launches_per_set": {"pack": wl.ranks, "unpack": wl.ranks},

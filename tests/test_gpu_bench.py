@@ -43,6 +43,7 @@ def test_attention_workload_line():
     assert p["algorithmic_bytes"] == {"pack": 2 * 3 * 4 * 1024 * 24 * 128 * 2, "unpack": 2 * 3 * 4 * 1024 * 24 * 128 * 2}
     assert p["gpu_launches_per_set"] == {"pack": 4, "unpack": 4}
     assert p["pack_gbs"] > 0 and p["unpack_gbs"] > 0 and p["step_gbs"] > 0 and p["copy_gbs"] > 0
+    assert p["copy_per_rank_gbs"] > 0
 
 
 @pytest.mark.gpu
