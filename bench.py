@@ -249,7 +249,7 @@ def run_gpu(args, rank, world, local_rank):
     # ---------------------------------------------------------- e2e (host buffers)
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(sim, inp, args, world, dev, run_phase, barrier)
+        e2e = run_e2e(sim, inp, args, world, dev, barrier)
     sim.l2_flushed = flush
     return sim, inp, total_ms, parts, clocks, e2e
 
@@ -360,72 +360,80 @@ def run_pack_line(args, dev, peaks, peak_kind):
             "traffic": recorded_traffic("pack_kernels", "relayout")}
 
 
-def run_e2e(sim, inp, args, world, dev, run_phase, barrier):
+def run_e2e(sim, inp, args, world, dev, barrier):
     """The same steps with every step's inputs copied in from pinned host
     memory and its result copied back, all inside the timed region.
 
-    Three streams pipeline the copies the way a serving loop would: the
-    host->device copy of step i+1 runs on its own stream as soon as step i's
-    exchange has read the input buffer (during step i's attention), and the
-    device->host copy of step i runs on a third stream while step i+1
-    computes. Where the result buffer is written again early in the next
-    step (the attention output at U = 1), it is first snapshotted on the
-    device (one D2D copy per step, inside the timed region) so the read-back
-    never races the next step's kernels."""
+    Two copies of the layer (input, gathered and output buffers, graphs)
+    take the steps in turn, the way a serving loop double-buffers: step i's
+    input is copied in on its own stream while step i-1 computes (its buffer
+    was last read by step i-2's exchange), and step i's result is read back
+    on a third stream while the following steps compute (its buffer is next
+    rewritten by step i+2, after that read-back)."""
     import torch
+
+    from diffusion_transformer_context_gb300.simulate import SimLayer
 
     cs = torch.cuda.current_stream(dev)
     hs, ds = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    other = SimLayer(sim.wl, device=dev, balanced=not args.unbalanced)
+    other.load(inp)
+    if not args.eager:
+        other.capture()
+    sims = [sim, other]
     host_x = torch.empty(sim.x.shape, dtype=sim.x.dtype).pin_memory()
     host_x.copy_(sim.x.cpu())
-    # the step's result and the phase of the next step that rewrites it
-    if not sim.attention:
-        results, rewrite = [sim.qg, sim.kg, sim.vg], "exchange_in"   # the unpacked Q/K/V
-    elif sim.wl.U > 1:
-        results, rewrite = [sim.y], "exchange_out"                   # after the reverse exchange
-    else:
-        results, rewrite = [sim.out], "attend"
-    host_y = [torch.empty(r.shape, dtype=r.dtype).pin_memory() for r in results]
-    # the attention output is rewritten by the next step's attention, which starts
-    # right after the next exchange: read it back from a snapshot instead
-    stage = [torch.empty_like(r) for r in results] if rewrite == "attend" else None
+
+    def results_of(s):
+        if not s.attention:
+            return [s.qg, s.kg, s.vg], "exchange_in"  # the unpacked Q/K/V
+        if s.wl.U > 1:
+            return [s.y], "exchange_out"              # after the reverse exchange
+        return [s.out], "attend"
+
+    host_y = [torch.empty(r.shape, dtype=r.dtype).pin_memory() for r in results_of(sim)[0]]
+
+    def phase(s, name):
+        if args.eager:
+            getattr(s, name)(stream=cs)
+        else:
+            s.replay(name)
 
     def ev():
         return torch.cuda.Event()
 
+    x_free, out_free = [None, None], [None, None]  # per copy: its input read, its result read back
+
     def steps(n):
-        in_free, out_free = None, None
-        for _ in range(n):
+        for i in range(n):
+            k = i & 1
+            s = sims[k]
+            results, rewrite = results_of(s)
             h2d_done, x_read, out_ready, d2h_done = ev(), ev(), ev(), ev()
             with torch.cuda.stream(hs):
-                if in_free is not None:
-                    hs.wait_event(in_free)   # the previous exchange has read x
-                sim.x.copy_(host_x, non_blocking=True)
+                if x_free[k] is not None:
+                    hs.wait_event(x_free[k])   # this copy's previous exchange has read its input
+                s.x.copy_(host_x, non_blocking=True)
                 h2d_done.record(hs)
             cs.wait_event(h2d_done)
-            for name in sim.PHASES:
-                if name == rewrite and stage is None and out_free is not None:
-                    cs.wait_event(out_free)  # the previous read-back has left the result buffer
-                run_phase(name)
+            for name in s.PHASES:
+                if name == rewrite and out_free[k] is not None:
+                    cs.wait_event(out_free[k])  # this copy's previous read-back has left its result
+                phase(s, name)
                 if name == "exchange_in":
                     x_read.record(cs)
-            src = results
-            if stage is not None:
-                if out_free is not None:
-                    cs.wait_event(out_free)  # the previous read-back has left the snapshot
-                for d, r in zip(stage, results):
-                    d.copy_(r, non_blocking=True)
-                src = stage
             out_ready.record(cs)
             with torch.cuda.stream(ds):
                 ds.wait_event(out_ready)
-                for h, r in zip(host_y, src):
+                for h, r in zip(host_y, results):
                     h.copy_(r, non_blocking=True)
                 d2h_done.record(ds)
-            in_free, out_free = x_read, d2h_done
-        cs.wait_event(out_free)  # the last read-back is inside the timed region
+            x_free[k], out_free[k] = x_read, d2h_done
+        for k in range(2):
+            if out_free[k] is not None:
+                cs.wait_event(out_free[k])  # the last read-backs are inside the timed region
 
-    steps(max(1, args.warmup))
+    steps(max(2, args.warmup))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     e0.record(cs)
@@ -435,13 +443,14 @@ def run_e2e(sim, inp, args, world, dev, run_phase, barrier):
     barrier()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     # after the timed region: the host copy of the last step's result equals the device result
-    verified = all(torch.equal(h.to(dev), r) for h, r in zip(host_y, results))
+    last = sims[(args.steps - 1) & 1]
+    verified = all(torch.equal(h.to(dev), r) for h, r in zip(host_y, results_of(last)[0]))
     flops = sim.attn_flops(valid_keys(inp))
     return {"value": round(whole_job_tflops(flops * args.steps, world, e2e_ms), 3), "unit": "TFLOP/s",
             "h2d_bytes_per_step": host_x.numel() * host_x.element_size(),
             "d2h_bytes_per_step": sum(h.numel() * h.element_size() for h in host_y),
             "ms_per_step": round(e2e_ms / args.steps, 4),
-            "pipeline": "H2D / compute / D2H on three streams" + (", D2D snapshot of the output" if stage is not None else ""),
+            "pipeline": "H2D / compute / D2H on three streams; two copies of the layer take the steps in turn",
             "readback_verified": verified}
 
 
