@@ -58,7 +58,7 @@ constexpr int kBM = 128;      // query rows per tile (= TMEM lanes)
 constexpr int kBN = kAttnKeyBlock;  // keys per block (128)
 constexpr int kTiles = 2;     // query tiles per CTA
 constexpr int kStages = 2;    // depth of the K ring (two-tile units) and of the V ring
-constexpr int kThreads = 384; // 12 warps: TMA, MMA, two idle, 4 + 4 softmax
+constexpr int kThreads = 384; // 12 warps: Q/K loads, MMA, V loads, one spare, 4 + 4 softmax
 // Registers: the kernel is launched with kRegsLaunch per thread (the compiler's
 // figure for 384 threads, checked on the host before the first launch); the
 // first warpgroup (TMA, MMA) gives registers up to the two softmax warpgroups.
