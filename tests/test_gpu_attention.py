@@ -332,6 +332,23 @@ def test_wan480_one_rank_full_size_sampled(ctx, orc):
     _sampled(ctx, orc, 1, 4095, 32760, 12, 128, 512, all_heads_tail=True)
 
 
+@pytest.mark.parametrize("shape,masked", [((1, 4095, 32760, 12), True), ((1, 9450, 75600, 10), False)],
+                         ids=["wan480_rank_masked", "wan14b_rank_odd_blocks"])
+def test_no_workspace_full_size_sampled(ctx, orc, shape, masked):
+    """Calls without a workspace whose 256-row units would leave a partial
+    last wave take the halves mode (128-row units, the two halves of the key
+    range side by side in one CTA). One 480p rank (256 key blocks, a ragged
+    last tile of 127 rows; 20 % of the keys masked), and one rank of Q 9450
+    rows against 75600 keys (591 key blocks: the halves differ by one, the
+    last block holds 80 keys; a ragged tail of 106 rows)."""
+    B, Sq, Sk, H = shape
+    mask = None
+    if masked:
+        mask = (np.random.default_rng(7).random((B, Sk)) > 0.2).astype(np.uint8)
+    n = _sampled(ctx, orc, B, Sq, Sk, H, 128, 512, mask=mask, split=False, all_heads_tail=True)
+    assert n >= 512 + H * 255
+
+
 def test_wan14b_full_size_sampled(ctx, orc):
     """The Wan-14B-like call as the layer runs it (4 head groups batched, the
     local-Q of both A ranks stacked: Q [4,75600,10,128] vs K/V
