@@ -92,12 +92,13 @@ def test_fp16(ctx, orc):
     _check_full(orc, q, k, v, O, L, dtype="fp16")
 
 
+@pytest.mark.parametrize("D", [128, 64])
 @pytest.mark.parametrize("split", [False, True], ids=["per_unit", "balanced"])
 @pytest.mark.parametrize("kind", ["random", "rear_text", "front_text", "first_block_empty", "first_half_empty",
                                   "row_empty"])
-def test_key_mask(ctx, orc, kind, split):
+def test_key_mask(ctx, orc, kind, split, D):
     gen = torch.Generator().manual_seed(11)
-    B, Sq, Sk, H, D = 2, 200, 600, 2, 128
+    B, Sq, Sk, H = 2, 200, 600, 2
     q, k, v = (workloads.randn(s, gen) for s in ((B, Sq, H, D), (B, Sk, H, D), (B, Sk, H, D)))
     mask = np.ones((B, Sk), np.uint8)
     rng = np.random.default_rng(0)
@@ -121,12 +122,13 @@ def test_key_mask(ctx, orc, kind, split):
         assert (O[1] == 0).all() and np.isneginf(L[1]).all()
 
 
+@pytest.mark.parametrize("D", [128, 64])
 @pytest.mark.parametrize("scale", [1.0, 0.01, 0.35])
-def test_scale_and_rescaling(ctx, orc, scale):
-    """scale 1.0 makes the scores ~N(0, 128): row maxima keep growing across
-    key blocks, which exercises the conditional O rescaling."""
+def test_scale_and_rescaling(ctx, orc, scale, D):
+    """scale 1.0 makes the scores ~N(0, D): row maxima keep growing across
+    key blocks, which exercises the conditional O rescaling (D = 128 and 64)."""
     gen = torch.Generator().manual_seed(12)
-    B, Sq, Sk, H, D = 1, 256, 1024, 2, 128
+    B, Sq, Sk, H = 1, 256, 1024, 2
     q, k, v = (workloads.randn(s, gen) for s in ((B, Sq, H, D), (B, Sk, H, D), (B, Sk, H, D)))
     O, L = _run(ctx, q, k, v, scale=scale)
     _check_full(orc, q, k, v, O, L, scale=scale)
@@ -145,18 +147,20 @@ def test_growing_maximum_sorted_keys(ctx, orc):
     _check_full(orc, q, k, v, O, L, scale=0.5)
 
 
+@pytest.mark.parametrize("D", [128, 64])
 @pytest.mark.parametrize("split", [False, True], ids=["per_unit", "balanced"])
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
-def test_running_maximum_jumps(ctx, orc, dtype, split):
+def test_running_maximum_jumps(ctx, orc, dtype, split, D):
     """After a segment's first key block the kernel takes the exps against
     the running maximum and checks the block's probability sum (at most 2^15)
     instead of computing the block maximum. Query rows close to one direction
     u and small random keys keep the early maxima near 0; in key block 5 one
     key is a multiple of u whose score jumps by about 11.4 log2 units on head
     0 (p ~ 2^11: accepted, no rescale) and by about 17.3 on head 1 (p ~ 2^17:
-    the block is redone with its exact maximum and O rescaled)."""
+    the block is redone with its exact maximum and O rescaled). At D = 128
+    and D = 64."""
     gen = torch.Generator().manual_seed(21)
-    B, Sq, Sk, H, D = 1, 256, 1024, 2, 128
+    B, Sq, Sk, H = 1, 256, 1024, 2
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
     u = torch.where(torch.rand(D, generator=gen) < 0.5, -1.0, 1.0)
     q = (u.view(1, 1, 1, D) + 0.05 * torch.randn((B, Sq, H, D), generator=gen)).to(tdt)
@@ -170,16 +174,17 @@ def test_running_maximum_jumps(ctx, orc, dtype, split):
     _check_full(orc, q, k, v, O, L, dtype=dtype)
 
 
+@pytest.mark.parametrize("D", [128, 64])
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 @pytest.mark.parametrize("split", [False, True], ids=["per_unit", "balanced"])
-def test_running_maximum_jumps_late_in_block(ctx, orc, dtype, split):
+def test_running_maximum_jumps_late_in_block(ctx, orc, dtype, split, D):
     """Jumps of the running maximum late in a key block (key 100 of block 5,
     past the first 64 keys): about 17.3 log2 units on head 0 (the block sum
     check fails and the block is redone with its exact maximum, O rescaled),
     about 11.4 on head 1 (accepted), and on head 2 two jumps in a row, early
     in block 5 and late in block 6, the second far above the first."""
     gen = torch.Generator().manual_seed(24)
-    B, Sq, Sk, H, D = 1, 256, 1024, 3, 128
+    B, Sq, Sk, H = 1, 256, 1024, 3
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
     u = torch.where(torch.rand(D, generator=gen) < 0.5, -1.0, 1.0)
     q = (u.view(1, 1, 1, D) + 0.05 * torch.randn((B, Sq, H, D), generator=gen)).to(tdt)
