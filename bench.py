@@ -35,6 +35,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "LQ/GKV attn TFLOP/s & % GB300 bf16 peak; QKV pack/unpack GB/s & % HBM"
+# staging layouts of the exchange (values of ctx_layout in the C header)
+LAYOUTS = {"tqkv": 0, "interleaved": 1}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -186,7 +188,7 @@ def run_gpu(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     wl = workloads.WORKLOADS[args.workload]
     inp = workloads.make_inputs(wl)
-    sim = SimLayer(wl, device=dev, balanced=not args.unbalanced)
+    sim = SimLayer(wl, device=dev, balanced=not args.unbalanced, layout=LAYOUTS[args.layout])
     sim.load(inp)
     stream = torch.cuda.current_stream(dev)
 
@@ -256,8 +258,9 @@ def run_gpu(args, rank, world, local_rank):
 
 def run_pack_line(args, dev, peaks, peak_kind):
     """The layout-only workload timed beside the default line: U = 4 ranks,
-    each Q/K/V [1,1024,24,128], packed into [4,3,1,1024,6,128] staging
-    buffers and, after the exchange, unpacked to [1,4096,6,128] per rank.
+    each Q/K/V [1,1024,24,128], packed into staging buffers of the chosen
+    layout ([4,3,1,1024,6,128] or [4,1,1024,6,384]) and, after the exchange,
+    unpacked to [1,4096,6,128] per rank.
 
     `achieved` is the library's pack and unpack kernels in HBM terms. The
     work rotates over n buffer sets whose total is several times L2, so every
@@ -265,7 +268,8 @@ def run_pack_line(args, dev, peaks, peak_kind):
     timed region (all but the last replay's). One CUDA graph holds the four
     ranks' packs (launches concurrent, as ranks run) of every set in turn,
     another the unpacks; each is replayed back to back, so graph launches
-    are amortised over n sets as inside a layer's graph. `copy_gbs` is a
+    are amortised over n sets as inside a layer's graph. The other staging
+    layout is timed the same way and reported beside it. `copy_gbs` is a
     plain device copy of the same bytes per set timed the same way: the
     reference for transfers of this size. `step_gbs` is the whole simulated
     step (pack + all-to-all + unpack): there the staging buffers written by
@@ -278,13 +282,16 @@ def run_pack_line(args, dev, peaks, peak_kind):
     wl = workloads.WORKLOADS["pack"]
     inp = workloads.make_inputs(wl)
     l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
-    one = SimLayer(wl, device=dev)
+    main_layout = args.layout
+    other_layout = "interleaved" if main_layout == "tqkv" else "tqkv"
+    one = SimLayer(wl, device=dev, layout=LAYOUTS[main_layout])
     set_bytes = (one.x.numel() + one.send.numel() + one.recv.numel() + 3 * one.qg.numel()) * 2
     # a pack (or an unpack) touches half a set; between two uses of a buffer
     # the other sets' kernels move at least 4x L2 through the cache
     n_sets = 1 + -(-4 * l2_bytes // (set_bytes // 2))
-    sims = [one] + [SimLayer(wl, device=dev) for _ in range(n_sets - 1)]
-    for sim in sims:
+    sims = {main_layout: [one] + [SimLayer(wl, device=dev, layout=LAYOUTS[main_layout]) for _ in range(n_sets - 1)],
+            other_layout: [SimLayer(wl, device=dev, layout=LAYOUTS[other_layout]) for _ in range(n_sets)]}
+    for sim in sims[main_layout] + sims[other_layout]:
         sim.load(inp)
         sim.step()  # library set-up outside any capture
     b_pack, b_unpack = one.pack_bytes(), one.unpack_bytes()
@@ -309,21 +316,20 @@ def run_pack_line(args, dev, peaks, peak_kind):
             with torch.cuda.stream(s):
                 dst[i][g * n:(g + 1) * n].copy_(src[i][g * n:(g + 1) * n])
 
-        sims[i]._per_rank(None, one)
+        sims[main_layout][i]._per_rank(None, one)
 
-    graphs = {"pack": capture(lambda i: sims[i].pack_ranks()),
-              "unpack": capture(lambda i: sims[i].unpack_ranks()),
-              "step": capture(lambda i: sims[i].exchange_in()),
+    graphs = {"step": capture(lambda i: sims[main_layout][i].exchange_in()),
               "copy": capture(lambda i: dst[i].copy_(src[i])),
               "copy_ranks": capture(copy_ranks)}
+    for lay, ss in sims.items():
+        graphs["pack_" + lay] = capture(lambda i: ss[i].pack_ranks())
+        graphs["unpack_" + lay] = capture(lambda i: ss[i].unpack_ranks())
     torch.cuda.synchronize(dev)
     stream = torch.cuda.current_stream(dev)
     reps = max(args.steps, 20)
 
-    def timed(name):
+    def timed_once(name):
         g = graphs[name]
-        for _ in range(3):
-            g.replay()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize(dev)
         e0.record(stream)
@@ -333,31 +339,55 @@ def run_pack_line(args, dev, peaks, peak_kind):
         torch.cuda.synchronize(dev)
         return e0.elapsed_time(e1) / (reps * n_sets)  # per set
 
-    ms_pack, ms_unpack, ms_step, ms_copy = timed("pack"), timed("unpack"), timed("step"), timed("copy")
-    ms_copy_ranks = timed("copy_ranks")
-    gbs = (b_pack + b_unpack) / ((ms_pack + ms_unpack) * 1e-3) / 1e9
+    # every graph warmed up first, then three rounds over all of them in turn
+    # (median per graph), so that no figure depends on its place in the order
+    for g in graphs.values():
+        for _ in range(3):
+            g.replay()
+    samples = {n: [] for n in graphs}
+    for _ in range(3):
+        for n in graphs:
+            samples[n].append(timed_once(n))
+
+    def timed(name):
+        return sorted(samples[name])[1]
 
     def rate(b, ms):
         return round(b / (ms * 1e-3) / 1e9, 1)
 
-    return {"workload": "pack", "U": wl.U, "per_rank": [wl.B, wl.S_l, wl.H, wl.D],
-            "staging": [wl.U, 3, wl.B, wl.S_l, wl.h_l, wl.D], "bound": "hbm",
-            "kernel": "relayout_kernel (4 packs; 4 unpacks)", "achieved": round(gbs, 1),
-            "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+    def layout_figures(lay):
+        ms_p, ms_u = timed("pack_" + lay), timed("unpack_" + lay)
+        gbs = (b_pack + b_unpack) / ((ms_p + ms_u) * 1e-3) / 1e9
+        staging = ([wl.U, 3, wl.B, wl.S_l, wl.h_l, wl.D] if lay == "tqkv"
+                   else [wl.U, wl.B, wl.S_l, wl.h_l, 3 * wl.D])
+        return {"staging": staging, "achieved": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4),
+                "pack_gbs": rate(b_pack, ms_p), "unpack_gbs": rate(b_unpack, ms_u),
+                "pack_ms": round(ms_p, 4), "unpack_ms": round(ms_u, 4),
+                "traffic": recorded_traffic("pack_kernels" + ("" if lay == "tqkv" else "_" + lay), "relayout")}
+
+    main = layout_figures(main_layout)
+    other = layout_figures(other_layout)
+    ms_step, ms_copy, ms_copy_ranks = timed("step"), timed("copy"), timed("copy_ranks")
+    traffic = main.pop("traffic")
+    return {"workload": "pack", "U": wl.U, "per_rank": [wl.B, wl.S_l, wl.H, wl.D], "staging_layout": main_layout,
+            "staging": main["staging"], "bound": "hbm",
+            "kernel": "relayout_kernel (4 packs; 4 unpacks)", "achieved": main["achieved"],
+            "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": main["frac"],
             "peak_source": f"{peak_kind} hbm_gbs",
-            "pack_gbs": rate(b_pack, ms_pack), "unpack_gbs": rate(b_unpack, ms_unpack),
-            "pack_ms": round(ms_pack, 4), "unpack_ms": round(ms_unpack, 4),
+            **{k: main[k] for k in ("pack_gbs", "unpack_gbs", "pack_ms", "unpack_ms")},
             "algorithmic_bytes": {"pack": b_pack, "unpack": b_unpack},
             "copy_gbs": rate(b_pack, ms_copy),
             "copy_per_rank_gbs": rate(b_pack, ms_copy_ranks),
             "copy_note": "copy_gbs: one device copy of a set's bytes; copy_per_rank_gbs: the same bytes as one "
                          "copy per rank on the rank streams (the packs' launch pattern)",
             "timing": f"one CUDA graph over {n_sets} buffer sets of {set_bytes >> 20} MiB (L2 {l2_bytes >> 20} MiB), "
-                      f"replayed {reps} times back to back: reads from HBM, write-back inside the timed region",
+                      f"replayed {reps} times back to back: reads from HBM, write-back inside the timed region; "
+                      f"median of 3 rounds over all graphs in turn",
             "gpu_launches_per_set": {"pack": wl.ranks, "unpack": wl.ranks},
+            other_layout: other,
             "step_gbs": rate(b_step, ms_step), "step_ms": round(ms_step, 4),
             "step_note": "pack + simulated all-to-all + unpack; staging buffers re-read from L2",
-            "traffic": recorded_traffic("pack_kernels", "relayout")}
+            "traffic": traffic}
 
 
 def run_e2e(sim, inp, args, world, dev, barrier):
@@ -376,7 +406,7 @@ def run_e2e(sim, inp, args, world, dev, barrier):
 
     cs = torch.cuda.current_stream(dev)
     hs, ds = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    other = SimLayer(sim.wl, device=dev, balanced=not args.unbalanced)
+    other = SimLayer(sim.wl, device=dev, balanced=not args.unbalanced, layout=sim.layout)
     other.load(inp)
     if not args.eager:
         other.capture()
@@ -575,10 +605,12 @@ def run_reference_layout(args, wl, inp):
     u16 = workloads.as_u16
     shards = [[u16(inp.shard(t, g)) for t in (inp.q, inp.k, inp.v)] for g in range(wl.U * wl.A)]
 
+    layout = LAYOUTS[args.layout]
+
     def one_step(g):
         t = time.perf_counter()
-        st = oracle.pack_qkv(*shards[g], wl.U)
-        oracle.unpack_qkv(st, wl.U)
+        st = oracle.pack_qkv_ex(*shards[g], wl.U, layout)
+        oracle.unpack_qkv_ex(st, wl.U, layout)
         return 2 * 2 * st.nbytes, time.perf_counter() - t
 
     for i in range(args.warmup):
@@ -593,7 +625,8 @@ def run_reference_layout(args, wl, inp):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 * dt / args.steps, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "u16 (bit copy)", "data": "synthetic",
-            "config": {**shape_config(wl), "sample": "pack + unpack of one rank per step"},
+            "config": {**shape_config(wl), "sample": "pack + unpack of one rank per step",
+                       **({"staging_layout": args.layout} if args.layout != "tqkv" else {})},
             "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": oracle.num_threads(),
                              "kind": "oracle", "sample": "pack + unpack of one rank per step"},
             "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -984,6 +1017,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-pack", action="store_true", help="skip the layout-only pack workload line")
+    ap.add_argument("--layout", default="tqkv", choices=sorted(LAYOUTS),
+                    help="staging layout of the exchange: [U,3,B,S_l,h_l,D] or [U,B,S_l,h_l,3D]")
     ap.add_argument("--per-rank", action="store_true",
                     help="one process per rank of the workload's U x A job (torchrun with U*A GPUs), NCCL between")
     ap.add_argument("--unbalanced", action="store_true", help="attention without a workspace (no unit split between CTAs)")
@@ -1046,13 +1081,16 @@ def main():
                 "frac": round(relayout_gbs / peaks["hbm_gbs"], 4), "peak_source": f"{peak_kind} hbm_gbs",
                 "ms": round(relayout_ms, 4), "algorithmic_bytes": relayout_bytes,
                 "reverse_ms": round(reverse_ms, 4), "reverse_bytes": sim.reverse_bytes(),
-                "traffic": recorded_traffic(args.workload, "relayout"),
+                "traffic": recorded_traffic(args.workload + ("" if args.layout == "tqkv" else "_" + args.layout),
+                                            "relayout"),
                 "note": "inside the step: written rows drain from L2 during the next kernel, so an upper bound; "
                         "the `pack` object times the layout kernels with reads from HBM and timed write-backs"}
     config = {**shape_config(sim.wl),
               "l2": "flushed_between_steps" if sim.l2_flushed else "inputs_larger_than_l2",
               "parallelism": f"replicas{world}",
               "launch": "eager" if args.eager else "cuda graphs (one per phase)"}
+    if args.layout != "tqkv":
+        config["staging_layout"] = args.layout
     line = {"metric": METRIC, "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic", "config": config}

@@ -385,8 +385,9 @@ ctx_status ctx_pack_qkv_ex(const void *q, const void *k, const void *v, void *st
         a.n_runs = 3LL * U * B * S_l;
         return run_relayout(H % U == 0 ? RelayoutMode::PackQKV : RelayoutMode::PackQKVPad, a, stream);
     }
-    a.run_vec = D / 8;
-    a.n_runs = static_cast<long long>(U) * B * S_l * h_l;
+    a.run_vec = h_l * D / 8;
+    a.head_vec = D / 8;
+    a.n_runs = 3LL * U * B * S_l;
     return run_relayout(RelayoutMode::PackInter, a, stream);
 }
 
@@ -432,8 +433,9 @@ ctx_status ctx_unpack_qkv_ex(const void *recv, void *q, void *k, void *v, long l
     a.U = U;
     a.q_batch_stride_rows = q_batch_stride_rows;
     a.kv_batch_stride_rows = kv_batch_stride_rows;
-    a.run_vec = D / 8;
-    a.n_runs = static_cast<long long>(U) * B * S_l * h_l;
+    a.run_vec = static_cast<long long>(h_l) * D / 8;
+    a.head_vec = D / 8;
+    a.n_runs = 3LL * U * B * S_l;
     return run_relayout(RelayoutMode::UnpackInter, a, stream);
 }
 

@@ -41,8 +41,8 @@ enum class RelayoutMode : int {
     AllToAll = 4,
     PackQKVPad = 5,    // heads padded with zeros to U*h_l
     UnpackOutPad = 6,  // keeps the first H of the U*h_l heads
-    PackInter = 7,     // interleaved staging [U][B][S_l][h_l][3][D] (cells of 3*D)
-    UnpackInter = 8,
+    PackInter = 7,     // interleaved staging [U][B][S_l][h_l][3][D] (cells of 3*D), heads padded
+    UnpackInter = 8,   // interleaved staging back to Q', K', V'
 };
 
 // Every relayout step moves "runs": contiguous groups of 16-byte vectors that
@@ -60,6 +60,7 @@ struct RelayoutArgs {
     // shape parameters (meaning depends on the mode)
     long long B, S_l, H, h_l, U, G;
     long long H_real;                // padded modes: heads that exist (< U*h_l)
+    long long head_vec;              // interleaved modes: 16-byte vectors per head (D/8)
     long long q_batch_stride_rows;   // unpack: Q' batch stride; pack_out: O batch stride
     long long kv_batch_stride_rows;  // unpack: K'/V' batch stride
 };

@@ -42,6 +42,10 @@ def test_attention_workload_line():
     # the packs and the unpacks each read and write the 75.5 MB of all ranks' Q/K/V once
     assert p["algorithmic_bytes"] == {"pack": 2 * 3 * 4 * 1024 * 24 * 128 * 2, "unpack": 2 * 3 * 4 * 1024 * 24 * 128 * 2}
     assert p["gpu_launches_per_set"] == {"pack": 4, "unpack": 4}
+    # the interleaved staging layout, timed the same way
+    assert p["staging_layout"] == "tqkv" and p["staging"] == [4, 3, 1, 1024, 6, 128]
+    pi = p["interleaved"]
+    assert pi["staging"] == [4, 1, 1024, 6, 384] and pi["achieved"] > 0 and pi["pack_gbs"] > 0
     assert p["pack_gbs"] > 0 and p["unpack_gbs"] > 0 and p["step_gbs"] > 0 and p["copy_gbs"] > 0
     assert p["copy_per_rank_gbs"] > 0
 
@@ -68,6 +72,17 @@ def test_layout_workload_line():
     assert d["config"]["l2"] == "flushed_between_steps"
     assert d["e2e"]["readback_verified"] is True
     assert d["e2e"]["unit"] == "GB/s"
+
+
+@pytest.mark.gpu
+def test_layout_workload_line_interleaved():
+    d = run_bench("--workload", "pack", "--layout", "interleaved", "--steps", "3", "--warmup", "3",
+                  "--no-cpu-baseline", "--no-clocks")
+    r = d["roofline"]
+    assert d["config"]["staging_layout"] == "interleaved"
+    assert r["staging_layout"] == "interleaved" and r["staging"] == [4, 1, 1024, 6, 384]
+    assert d["value"] == r["achieved"] > 0 and r["tqkv"]["staging"] == [4, 3, 1, 1024, 6, 128]
+    assert d["e2e"]["readback_verified"] is True
 
 
 @pytest.mark.gpu

@@ -136,7 +136,14 @@ def test_host_pointer_is_rejected(ctx):
 
 
 @pytest.mark.parametrize("layout", [0, 1])
-@pytest.mark.parametrize("B,S_l,H,D,U", [(1, 16, 14, 128, 4), (2, 5, 7, 64, 3), (1, 9, 8, 128, 4), (1, 3, 3, 8, 2)])
+@pytest.mark.parametrize("B,S_l,H,D,U", [
+    (1, 16, 14, 128, 4), (2, 5, 7, 64, 3), (1, 9, 8, 128, 4), (1, 3, 3, 8, 2),
+    # heads of 9 and 17 vectors (D = 72, 136): the interleaved offsets carry a
+    # remainder that is not a power of two
+    (2, 3, 5, 72, 2), (1, 4, 33, 136, 2),
+    # runs longer than one warp pass (40 x 128 and 33 x 136 elements per rank and part)
+    (1, 6, 40, 128, 1), (1, 5, 33, 136, 1),
+])
 def test_pack_ex_bit_exact(ctx, orc, B, S_l, H, D, U, layout):
     gen = torch.Generator().manual_seed(71)
     q, k, v = (_bits((B, S_l, H, D), gen) for _ in range(3))
@@ -152,6 +159,31 @@ def test_pack_ex_bit_exact(ctx, orc, B, S_l, H, D, U, layout):
     torch.cuda.synchronize()
     for o, e in zip(outs, orc.unpack_qkv_ex(expect, U, layout)):
         assert o.intact() and np.array_equal(u16(o.t), e)
+
+
+@pytest.mark.parametrize("B,S_l,H,D,U", [(2, 7, 14, 128, 4), (2, 3, 40, 64, 1), (3, 5, 10, 72, 2)])
+def test_interleaved_unpack_strided(ctx, orc, B, S_l, H, D, U):
+    """The interleaved unpack placing every rank's rows inside larger gathered
+    buffers (batch strides of U*S_l + 3 and U*S_l + 5 rows): placed rows equal
+    the oracle's unpack, every other row stays untouched."""
+    gen = torch.Generator().manual_seed(73)
+    q, k, v = (_bits((B, S_l, H, D), gen) for _ in range(3))
+    h_l = -(-H // U)
+    staging = orc.pack_qkv_ex(u16(q), u16(k), u16(v), U, 1)
+    st = torch.from_numpy(staging.view(np.int16)).view(torch.bfloat16).cuda()
+    rows = U * S_l
+    qs, ks = rows + 3, rows + 5
+    outs = [Guarded((B, n, h_l, D), torch.bfloat16) for n in (qs, ks, ks)]
+    for o in outs:
+        o.t.view(torch.int16).fill_(-12345)
+    ctx.ctx_unpack_qkv_ex(st, outs[0].t, outs[1].t, outs[2].t, U, B, S_l, h_l, D, 1,
+                          q_batch_stride_rows=qs, kv_batch_stride_rows=ks)
+    torch.cuda.synchronize()
+    for o, e in zip(outs, orc.unpack_qkv_ex(staging, U, 1)):
+        got = u16(o.t)
+        assert o.intact()
+        assert np.array_equal(got[:, :rows], e)
+        assert (got[:, rows:] == np.uint16(np.int16(-12345).view(np.uint16))).all()
 
 
 @pytest.mark.parametrize("B,S_l,h_l,H,D,U", [(1, 16, 4, 14, 128, 4), (2, 5, 3, 7, 64, 3), (1, 4, 2, 8, 8, 4)])
