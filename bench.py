@@ -62,6 +62,7 @@ TRAFFIC_RECORDS = {
     # roofline object -> (committed ncu summary, kernel sources it was taken on)
     "attention": ("attn_traffic.json", ("attention.cu", "ptx.cuh")),
     "relayout": ("relayout_traffic.json", ("relayout.cu",)),
+    "merge": ("merge_traffic.json", ("merge.cu", "ptx.cuh")),
 }
 
 
@@ -700,7 +701,7 @@ def run_merge_bench(args):
             "roofline": {"bound": "hbm", "kernel": "lse_merge_kernel", "achieved": round(gbs, 1),
                          "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
                          "peak_source": f"{kind} hbm_gbs", "algorithmic_bytes_per_launch": nbytes,
-                         "traffic": None, "add_gbs": round(add_gbs, 1),
+                         "traffic": recorded_traffic("wan480_two_segments", "merge"), "add_gbs": round(add_gbs, 1),
                          "add_note": "torch.add of the two segments' O (2 reads + 1 write of the same O bytes), "
                                      "timed the same way"},
             "gpu_launches": args.steps, "clocks": clocks,
@@ -899,18 +900,60 @@ def run_varlen_bench(args):
     one_rank_line = {"rank": 0, "flops": flops0,
                      "balanced_tflops": round(flops0 / (ms_bal * 1e-3) / 1e12, 1),
                      "one_cta_per_unit_tflops": round(flops0 / (ms_unit * 1e-3) / 1e12, 1)}
-    # e2e: the packed Q/K/V in from pinned host memory, every rank's output back
+    # e2e: the packed Q/K/V in from pinned host memory, every rank's output back.
+    # Two buffer sets take the steps in turn (double-buffered as in the layer's
+    # e2e): step i's input is copied in on its own stream while step i-1
+    # computes, its output read back on a third stream while later steps compute.
     qh, kh, vh = (t.pin_memory() for t in (q_h, k_h, v_h))
     outh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    sets = [(q, k, v, out, lse, cu_loc)] + [
+        (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(out),
+         torch.empty_like(lse), [torch.empty_like(c) for c in cu_loc])]
+    cs = torch.cuda.current_stream()
+    hs, ds = torch.cuda.Stream(), torch.cuda.Stream()
+    x_free, out_free = [None, None], [None, None]
+
+    def e2e_steps(n):
+        for i in range(n):
+            b = i & 1
+            sq, sk, sv, so, sl, sc = sets[b]
+            h2d_done, x_read, d2h_done = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
+            with torch.cuda.stream(hs):
+                if x_free[b] is not None:
+                    hs.wait_event(x_free[b])  # this set's previous step has read its inputs
+                for dst, src in ((sq, qh), (sk, kh), (sv, vh)):
+                    dst.copy_(src, non_blocking=True)
+                h2d_done.record(hs)
+            cs.wait_event(h2d_done)
+            if out_free[b] is not None:
+                cs.wait_event(out_free[b])  # this set's previous output has been read back
+            fork = torch.cuda.Event()
+            fork.record(cs)
+            for r, st_ in enumerate(lanes):
+                st_.wait_event(fork)
+                ctx.ctx_varlen_remap(cu, r * S_l, S_l, sc[r], stream=st_)
+                ctx.ctx_attn_varlen(sq[r * S_l:(r + 1) * S_l], sk, sv, sc[r], cu, S_l, so[r], sl[r], stream=st_)
+                done = torch.cuda.Event()
+                done.record(st_)
+                cs.wait_event(done)
+            x_read.record(cs)
+            with torch.cuda.stream(ds):
+                ds.wait_event(x_read)
+                outh.copy_(so, non_blocking=True)
+                d2h_done.record(ds)
+            x_free[b], out_free[b] = x_read, d2h_done
+        for b in range(2):
+            if out_free[b] is not None:
+                cs.wait_event(out_free[b])  # the last read-backs are inside the timed region
+
+    e2e_steps(2)
+    torch.cuda.synchronize()
     e0.record()
-    for _ in range(args.steps):
-        q.copy_(qh, non_blocking=True)
-        k.copy_(kh, non_blocking=True)
-        v.copy_(vh, non_blocking=True)
-        step()
-        outh.copy_(out, non_blocking=True)
+    e2e_steps(args.steps)
     e1.record()
     torch.cuda.synchronize()
+    last = sets[(args.steps - 1) & 1][3]
+    readback_ok = bool(torch.equal(outh.view(torch.int16), last.cpu().view(torch.int16)))
     e2e_ms = e0.elapsed_time(e1) / args.steps
     peaks, kind = load_peaks()
     line = {"metric": METRIC, "value": round(tflops, 3), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
@@ -924,11 +967,12 @@ def run_varlen_bench(args):
                          "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": round(tflops / peaks["bf16_tflops"], 4),
                          "peak_source": f"{kind} bf16_tflops (burst)", "algorithmic_flops_per_step": flops,
-                         "traffic": None},
+                         "traffic": recorded_traffic("varlen_step")},
             "gpu_launches": 2 * A * args.steps, "clocks": clocks,
             "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                     "h2d_bytes_per_step": 3 * qh.numel() * 2, "d2h_bytes_per_step": outh.numel() * 2,
-                    "ms_per_step": round(e2e_ms, 4), "pipeline": "copies and compute one after another"}}
+                    "ms_per_step": round(e2e_ms, 4), "readback_verified": readback_ok,
+                    "pipeline": "H2D / compute / D2H on three streams; two buffer sets take the steps in turn"}}
     if not args.no_cpu_baseline:
         import oracle
         oracle.build()

@@ -103,3 +103,13 @@ def test_single_attention_call_line():
     assert d["config"]["l2"] == "flushed_between_steps"
     assert d["roofline"]["algorithmic_flops_per_launch"] == pytest.approx(4.0 * 3 * 300 * 700 * 128)
     assert d["e2e"]["h2d_bytes_per_step"] == 2 * 128 * 3 * (300 + 2 * 700)
+
+
+@pytest.mark.gpu
+def test_varlen_line_pipelined_e2e():
+    # packed varlen documents: eight ranks' remap + attention; the e2e leg double-buffers
+    d = run_bench("--kernel", "varlen", "--steps", "3", "--warmup", "3", "--no-cpu-baseline", "--no-clocks")
+    assert d["config"]["workload"] == "varlen" and d["value"] > 0
+    assert d["e2e"]["readback_verified"] is True and "two buffer sets" in d["e2e"]["pipeline"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 3 * 32768 * 12 * 128 * 2
+    assert d["one_rank"]["balanced_tflops"] > 0
