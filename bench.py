@@ -1011,7 +1011,7 @@ def run_per_rank(args, rank, world, local_rank):
     try:
         G = Groups(wl.U, wl.A)
         inp = workloads.make_inputs(wl)
-        layer = RankLayer(wl, G, dev)
+        layer = RankLayer(wl, G, dev, layout=LAYOUTS[args.layout])
         layer.load(*(inp.shard(t, rank).to(dev) for t in (inp.q, inp.k, inp.v)),
                    None if inp.jk is None else inp.jk.to(dev), None if inp.jv is None else inp.jv.to(dev),
                    inp.image_mask, inp.joint_mask)

@@ -70,11 +70,11 @@ class LibraryOps:
     def __init__(self, balanced: bool = True):
         self.balanced = balanced
 
-    def pack(self, x, staging, U):
-        ctx_pack_qkv_ex(x[0], x[1], x[2], staging, U, CTX_LAYOUT_TQKV)
+    def pack(self, x, staging, U, layout=CTX_LAYOUT_TQKV):
+        ctx_pack_qkv_ex(x[0], x[1], x[2], staging, U, layout)
 
-    def unpack(self, src, q, k, v, U, B, S_l, h_l, D):
-        ctx_unpack_qkv_ex(src, q, k, v, U, B, S_l, h_l, D, CTX_LAYOUT_TQKV)
+    def unpack(self, src, q, k, v, U, B, S_l, h_l, D, layout=CTX_LAYOUT_TQKV):
+        ctx_unpack_qkv_ex(src, q, k, v, U, B, S_l, h_l, D, layout)
 
     def merge_mask(self, image_mask, joint_mask, B, S, J, front, out):
         ctx_merge_joint_attn_mask(image_mask, joint_mask, B, S, J, out, joint_front=front)
@@ -93,9 +93,12 @@ class LibraryOps:
 
 
 class RankLayer:
-    """The layer as one rank of a U x A job runs it (see the module text)."""
+    """The layer as one rank of a U x A job runs it (see the module text).
+    `layout` is the staging layout of the Ulysses exchange: [U,3,B,S_l,h_l,D]
+    or the interleaved [U,B,S_l,h_l,3D]; either way chunk r of the flat
+    buffer is what rank r of the group receives."""
 
-    def __init__(self, wl, groups: Groups, device, ops=None, dtype=torch.bfloat16):
+    def __init__(self, wl, groups: Groups, device, ops=None, dtype=torch.bfloat16, layout=CTX_LAYOUT_TQKV):
         U, A, B, S, H, D, J = wl.U, wl.A, wl.B, wl.S, wl.H, wl.D, wl.joint
         if (groups.U, groups.A) != (U, A):
             raise ValueError("groups built for another U x A")
@@ -103,7 +106,7 @@ class RankLayer:
             raise ValueError("one rank per process needs B = 1 (the gathered rows of an A group are contiguous)")
         if S % (U * A):
             raise ValueError("S must divide by U*A")
-        self.wl, self.G, self.dev = wl, groups, torch.device(device)
+        self.wl, self.G, self.dev, self.layout = wl, groups, torch.device(device), layout
         self.ops = ops if ops is not None else LibraryOps()
         self.S_l, self.h_l = S // (U * A), -(-H // U)
         self.rows = U * self.S_l                          # local query rows: S / A
@@ -112,7 +115,8 @@ class RankLayer:
         kw = dict(dtype=dtype, device=self.dev)
         S_l, h_l, Sk = self.S_l, self.h_l, self.Sk
         self.x = torch.zeros((3, B, S_l, H, D), **kw)     # this rank's input rows
-        self.staging = torch.empty((U, 3, B, S_l, h_l, D), **kw)
+        self.staging = torch.empty((U, 3, B, S_l, h_l, D) if layout == CTX_LAYOUT_TQKV else (U, B, S_l, h_l, 3 * D),
+                                   **kw)
         self.recv = torch.empty_like(self.staging) if U > 1 else None
         self.q = torch.empty((B, self.rows, h_l, D), **kw)
         self.k_loc = torch.empty((B, self.rows, h_l, D), **kw)
@@ -150,14 +154,17 @@ class RankLayer:
         wl, ops, G = self.wl, self.ops, self.G
         U, B, S, D = wl.U, wl.B, wl.S, wl.D
         S_l, h_l = self.S_l, self.h_l
-        # 1-3: Ulysses exchange inside the U group (at U = 1 the staging buffer is the input)
-        if U > 1:
-            ops.pack(self.x, self.staging, U)
-            dist.all_to_all_single(self.recv.view(-1), self.staging.view(-1), group=G.ulysses)
-            src = self.recv
+        # 1-3: Ulysses exchange inside the U group (at U = 1 the [U,3,B,S_l,h_l,D]
+        # staging buffer is the input bit for bit, so nothing is packed)
+        if U > 1 or self.layout != CTX_LAYOUT_TQKV:
+            ops.pack(self.x, self.staging, U, self.layout)
+            src = self.staging
+            if U > 1:
+                dist.all_to_all_single(self.recv.view(-1), self.staging.view(-1), group=G.ulysses)
+                src = self.recv
         else:
             src = self.x.view(1, 3, B, S_l, h_l, D)
-        ops.unpack(src, self.q, self.k_loc, self.v_loc, U, B, S_l, h_l, D)
+        ops.unpack(src, self.q, self.k_loc, self.v_loc, U, B, S_l, h_l, D, self.layout)
         # 4: K/V AllGather inside the A group, straight into the gathered image rows
         img = slice(self.img0, self.img0 + S)  # one contiguous range at B = 1: gather flat
         dist.all_gather_into_tensor(self.kg[:, img].view(-1), self.k_loc.view(-1), group=G.agkv)

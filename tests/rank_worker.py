@@ -27,11 +27,11 @@ class OracleOps:
     def __init__(self, orc, H):
         self.orc, self.H = orc, H
 
-    def pack(self, x, staging, U):
-        staging.copy_(bf16(self.orc.pack_qkv_ex(u16(x[0]), u16(x[1]), u16(x[2]), U)))
+    def pack(self, x, staging, U, layout=0):
+        staging.copy_(bf16(self.orc.pack_qkv_ex(u16(x[0]), u16(x[1]), u16(x[2]), U, layout)))
 
-    def unpack(self, src, q, k, v, U, B, S_l, h_l, D):
-        for dst, r in zip((q, k, v), self.orc.unpack_qkv_ex(u16(src), U)):
+    def unpack(self, src, q, k, v, U, B, S_l, h_l, D, layout=0):
+        for dst, r in zip((q, k, v), self.orc.unpack_qkv_ex(u16(src), U, layout)):
             dst.copy_(bf16(r))
 
     def merge_mask(self, image_mask, joint_mask, B, S, J, front, out):
@@ -57,7 +57,7 @@ class OracleOps:
         y.copy_(bf16(self.orc.unpack_out_ex(u16(recv), U, self.H)))
 
 
-def run_rank(rank, world, port, wl):
+def run_rank(rank, world, port, wl, layout=0):
     import oracle
     import workloads
     from diffusion_transformer_context_gb300.ranks import Groups, RankLayer
@@ -69,7 +69,7 @@ def run_rank(rank, world, port, wl):
         oracle.build()
         inp = workloads.make_inputs(wl)
         G = Groups(wl.U, wl.A)
-        layer = RankLayer(wl, G, "cpu", ops=OracleOps(oracle, wl.H))
+        layer = RankLayer(wl, G, "cpu", ops=OracleOps(oracle, wl.H), layout=layout)
         layer.load(inp.shard(inp.q, rank), inp.shard(inp.k, rank), inp.shard(inp.v, rank), inp.jk, inp.jv,
                    inp.image_mask, inp.joint_mask)
         y = layer.step()

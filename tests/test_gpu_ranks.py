@@ -30,12 +30,13 @@ def _free_port():
         return s.getsockname()[1]
 
 
+@pytest.mark.parametrize("layout", [0, 1], ids=["tqkv", "interleaved"])
 @pytest.mark.parametrize("wl", [
     workloads.custom("pr_u1a1", B=1, S=700, H=3, D=128, U=1, A=1),
     workloads.custom("pr_u1a1_joint_masks_front", B=1, S=512, H=4, D=128, U=1, A=1, joint=64,
                      text_len_range=(1, 64), joint_front=True, image_pad_range=(0, 40)),
 ], ids=lambda w: w.name)
-def test_single_rank_job_matches_the_simulated_layer_and_the_oracle(ctx, orc, wl):
+def test_single_rank_job_matches_the_simulated_layer_and_the_oracle(ctx, orc, wl, layout):
     from diffusion_transformer_context_gb300.ranks import Groups, RankLayer
     from diffusion_transformer_context_gb300.simulate import SimLayer
 
@@ -43,7 +44,7 @@ def test_single_rank_job_matches_the_simulated_layer_and_the_oracle(ctx, orc, wl
                             device_id=torch.device("cuda", 0))
     try:
         inp = workloads.make_inputs(wl)
-        layer = RankLayer(wl, Groups(1, 1), "cuda")
+        layer = RankLayer(wl, Groups(1, 1), "cuda", layout=layout)
         layer.load(inp.q.cuda(), inp.k.cuda(), inp.v.cuda(), None if inp.jk is None else inp.jk.cuda(),
                    None if inp.jv is None else inp.jv.cuda(), inp.image_mask, inp.joint_mask)
         y = layer.step().clone()

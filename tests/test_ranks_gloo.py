@@ -33,3 +33,15 @@ def _free_port():
 def test_ranks_as_processes_match_the_composed_oracle(wl):
     world = wl.U * wl.A
     mp.spawn(run_rank, args=(world, _free_port(), wl), nprocs=world, join=True)
+
+
+@pytest.mark.parametrize("wl", [
+    workloads.custom("ri_u2a2_h5_joint", B=1, S=64, H=5, D=16, U=2, A=2, joint=6, text_len_range=(1, 6)),
+    workloads.custom("ri_u1a2", B=1, S=32, H=3, D=8, U=1, A=2),
+], ids=lambda w: w.name)
+def test_ranks_interleaved_staging_match_the_composed_oracle(wl):
+    """The same job with the interleaved staging layout [U,B,S_l,h_l,3D]
+    (sglang PR #33667 excerpt): the chunks the all-to-all moves change, the
+    layer's results do not."""
+    world = wl.U * wl.A
+    mp.spawn(run_rank, args=(world, _free_port(), wl, 1), nprocs=world, join=True)
