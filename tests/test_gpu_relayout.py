@@ -196,10 +196,11 @@ def test_unpack_out_ex_drops_pad_heads(ctx, orc, B, S_l, h_l, H, D, U):
     assert y.intact() and np.array_equal(u16(y.t), orc.unpack_out_ex(u16(recv), U, H))
 
 
-def test_beyond_2pow31_elements(ctx, orc):
+@pytest.mark.parametrize("layout", [0, 1], ids=["tqkv", "interleaved"])
+def test_beyond_2pow31_elements(ctx, orc, layout):
     """Pack and unpack of tensors with more than 2^31 elements each (64-bit
-    run and vector indices): per-rank Q/K/V [1, 65541, 256, 128], U = 8
-    (staging 12.9 GB). Each input is a seeded [1, 512, 256, 128] block
+    offsets): per-rank Q/K/V [1, 65541, 256, 128], U = 8 (staging 12.9 GB),
+    in either staging layout. Each input is a seeded [1, 512, 256, 128] block
     repeated along the rows on the device; sampled rows (always the last ones)
     are compared bit for bit with the oracle applied to the same rows."""
     B, S_l, H, D, U, blk = 1, (1 << 16) + 5, 256, 128, 8, 512
@@ -209,18 +210,20 @@ def test_beyond_2pow31_elements(ctx, orc):
     blocks = [_bits((B, blk, H, D), gen) for _ in range(3)]
     reps = -(-S_l // blk)
     q, k, v = (b.cuda().repeat(1, reps, 1, 1)[:, :S_l].contiguous() for b in blocks)
-    st = torch.empty((U, 3, B, S_l, h_l, D), dtype=torch.bfloat16, device="cuda")
-    ctx.ctx_pack_qkv(q, k, v, st, U)
+    shape = (U, 3, B, S_l, h_l, D) if layout == 0 else (U, B, S_l, h_l, 3 * D)
+    st = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+    ctx.ctx_pack_qkv_ex(q, k, v, st, U, layout)
     del q, k, v
     outs = [torch.empty((B, U * S_l, h_l, D), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
-    ctx.ctx_unpack_qkv(st, *outs, U)
+    ctx.ctx_unpack_qkv_ex(st, *outs, U, B, S_l, h_l, D, layout)
     torch.cuda.synchronize()
     rows = np.concatenate([workloads.sample_rows(S_l, 64), np.arange(S_l - 8, S_l)])
     for s in rows:
         src = [u16(b[:, s % blk:s % blk + 1]) for b in blocks]
-        exp_st = orc.pack_qkv(*src, U)                      # [U, 3, B, 1, h_l, D]
-        assert np.array_equal(u16(st[:, :, :, s:s + 1]), exp_st), s
-        exp_un = orc.unpack_qkv(exp_st, U)                  # 3 x [B, U, h_l, D]: row r <- source r
+        exp_st = orc.pack_qkv_ex(*src, U, layout)           # the row s of every destination
+        got_st = st[:, :, :, s:s + 1] if layout == 0 else st[:, :, s:s + 1]
+        assert np.array_equal(u16(got_st), exp_st), s
+        exp_un = orc.unpack_qkv_ex(exp_st, U, layout)       # 3 x [B, U, h_l, D]: row r <- source r
         for t in range(3):
             got = u16(outs[t][:, s::S_l][:, :U])
             assert np.array_equal(got, exp_un[t]), (s, t)
