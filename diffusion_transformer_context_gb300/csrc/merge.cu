@@ -207,7 +207,8 @@ cudaError_t launch_typed_merge(const LseMergeArgs &a, cudaStream_t stream)
     const uint4 *op = static_cast<const uint4 *>(a.o_parts);
     uint4 *out = static_cast<uint4 *>(a.out);
     auto grid_for = [&](long long units, long long units_per_block) {
-        return static_cast<unsigned>(std::max(1LL, std::min(0x7fffffffLL, (units + units_per_block - 1) / units_per_block)));
+        const long long blocks = (units + units_per_block - 1) / units_per_block;
+        return static_cast<unsigned>(std::max(1LL, std::min(0x7fffffffLL, blocks)));
     };
     bool done = false;
     const bool i32 = rows <= 0x7fffffffLL;  // every row index, and (b*H + h)*Sq + i, fits in 32 bits
